@@ -1,0 +1,372 @@
+"""Benchmark of the paged KV-cache decode step on GB300.
+
+One step = the whole hot path over one batch: append each sequence's new
+key/value through its block table (Eq. 21.6 of "KV cache: Generation state,
+latency, and allocation"), then paged decode attention over every cached
+position.  Default workload: the Llama-3.1-8B-style GQA layer (32 query heads,
+8 KV heads, d_h 128, bf16 KV, 16-token blocks), B = 32 sequences of 8 192
+cached tokens, blocks randomly permuted across the pool.
+
+Metric: effective KV GB/s = algorithmic bytes of a step / step time (KV bytes
+of every valid position read once, block-table entries, q, the appended rows,
+out and lse), and decode tokens/s = B / step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own pool and batch (sequences shard with no
+collective, weak scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+import numpy as np  # noqa: E402
+
+METRIC = "decode-attention effective KV GB/s and fraction of GB300 HBM roofline; tokens/s"
+UNIT = "GB/s"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- bytes
+def step_bytes(w) -> dict:
+    """Algorithmic bytes of one decode step of workload w (one layer)."""
+    s = w.elem_bytes
+    lens = w.lens_post.astype(np.int64)
+    kv = int(lens.sum()) * 2 * w.H_KV * w.d_h * s
+    table = int(((lens + w.bs - 1) // w.bs).sum()) * 4
+    q = w.B * w.H_Q * w.d_h * 2
+    out = w.B * w.H_Q * w.d_h * 4 + w.B * w.H_Q * 4
+    append = 2 * w.B * w.H_KV * w.d_h * (2 + s)
+    lens_b = w.B * 4 * 2
+    return {"kv": kv, "table": table, "q": q, "out": out, "append": append, "lens": lens_b,
+            "attn_kernel": kv + table + q + out + w.B * 4,
+            "total": kv + table + q + out + append + lens_b}
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_kvc_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
+    if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_attn_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if line.startswith("<!-- ") and ":" in line:
+            k, v = line[5:].split("-->")[0].split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_sha") != source_digest() or fields.get("workload") != workload:
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 9:
+                rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle (CPU) side
+def oracle_sample(w, ld, budget_s: float, units_max=None):
+    """Time the oracle (append into its pool image + decode) on a bounded sample
+    of (sequence, KV head) units of the workload, batched into one call so every
+    host thread works.  Returns (bytes/s, seconds, units, description, threads)."""
+    import oracle
+    from harness import logical_lists
+    K, V, cu = logical_lists(w, ld, ld.k_ctx, ld.v_ctx, ld.k_new, ld.v_new)
+    g = w.g
+    units = [(b, h) for b in range(w.B) for h in range(w.H_KV)]
+
+    def prepare(sel):
+        qs, ks, vs, cus, ns = [], [], [], [0], []
+        for (b, h) in sel:
+            n = int(w.lens_post[b])
+            rows = slice(int(cu[b]), int(cu[b]) + n)
+            qs.append(ld.q[b, h * g:(h + 1) * g])
+            ks.append(K[rows, h:h + 1])
+            vs.append(V[rows, h:h + 1])
+            cus.append(cus[-1] + n)
+            ns.append(n)
+        return (np.ascontiguousarray(np.stack(qs)), np.ascontiguousarray(np.concatenate(ks)),
+                np.ascontiguousarray(np.concatenate(vs)), np.array(cus, np.int64), np.array(ns, np.int64))
+
+    def run(sel):
+        qb, kb, vb, cub, nb = prepare(sel)
+        t0 = time.perf_counter()
+        for i, (b, h) in enumerate(sel):     # the append of each unit's new row (Eq. 21.6) into a pool image
+            img = oracle.PoolImage(1, int(nb[i]), 1, 1, w.d_h, 2)
+            img.write_tokens(0, np.zeros((1, 1), np.int32), np.array([nb[i] - 1], np.int32),
+                             np.array([0, 1], np.int64), ld.k_new[b:b + 1, h:h + 1], ld.v_new[b:b + 1, h:h + 1])
+        oracle.decode(qb, kb, vb, cub, nb, 1, scale=w.scale)
+        return int(nb.sum()) * 2 * w.d_h * w.elem_bytes, time.perf_counter() - t0
+
+    _, t1 = run(units[:1])
+    k = max(1, min(len(units), int(budget_s / max(t1, 1e-6))))
+    if units_max:
+        k = min(k, units_max)
+    nbytes, dt = run(units[:k])
+    threads = min(oracle.num_threads(), k * g)
+    desc = (f"{k} of {len(units)} (sequence, KV head) units of {w.name} (each {int(w.lens_post[0])} positions, "
+            f"{g} query heads): oracle append + fp64 decode")
+    return nbytes / dt, dt, k, desc, threads
+
+
+def run_reference(args, w, ld, rank):
+    """The oracle arm: each step a bounded sample of the same workload on host cores."""
+    per_step = max(0.01, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    rate, dt, k, desc, cores = oracle_sample(w, ld, per_step)
+    samples = []
+    for i in range(args.warmup + args.steps):
+        r, t, _, _, _ = oracle_sample(w, ld, per_step, units_max=k)
+        if i >= args.warmup:
+            samples.append((r, t))
+    value = float(np.mean([r for r, _ in samples])) / 1e9
+    ms = float(np.mean([t for _, t in samples])) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc + " per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w):
+    return {"workload": w.name, "B": w.B, "H_Q": w.H_Q, "H_KV": w.H_KV, "d_h": w.d_h, "block_size": w.bs,
+            "layers": w.L, "context": int(w.lens_pre.max()), "attended": int(w.lens_post.max()),
+            "kv_dtype": w.dtype, "num_blocks": w.num_blocks,
+            "l2": f"inputs larger than L2: {step_bytes(w)['kv'] / 1e9:.2f} GB of KV per step vs {L2_BYTES / 2**20:.0f} MiB L2"}
+
+
+# ---------------------------------------------------------------- GPU side
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="kvc", choices=["kvc", "reference"])
+    ap.add_argument("--workload", default="llama_gqa")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    import synth
+    from harness import layer_data
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = synth.make_workload(args.workload, seed=args.seed)
+        run_reference(args, w, layer_data(w, 0), rank)
+        return
+
+    import torch
+    import paged_kv_cache_kvc_gb300 as kvc
+    from harness import GpuCase, dev_bits
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    kvc.load()
+
+    w = synth.make_workload(args.workload, seed=args.seed + rank)     # each rank: its own batch
+    assert w.L == 1, "bench times one layer's step"
+    ld = layer_data(w, 0)
+    g = GpuCase(kvc, w, fill_byte=0)
+    g.load_context(0, ld)
+    q, k_new, v_new = g.step_inputs(ld)
+    out = torch.empty((w.B, w.H_Q, w.d_h), dtype=torch.float32, device="cuda")
+    lse = torch.empty((w.B, w.H_Q), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sb = step_bytes(w)
+
+    def step():
+        kvc.kvc_append(g.pool, 0, g.bt_dec, g.lens_pre, k_new, v_new)
+        kvc.kvc_decode_attn(g.pool, 0, q, g.bt_dec, g.lens_post, out, lse, scale=w.scale)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+
+    # ---- device-resident timed region, per-launch events around the attention call
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = kvc.kvc_launch_count()
+    with ClockSampler(local) as clk:
+        barrier()
+        t_start.record(stream)
+        for i in range(K):
+            kvc.kvc_append(g.pool, 0, g.bt_dec, g.lens_pre, k_new, v_new)
+            ev_a[i].record(stream)
+            kvc.kvc_decode_attn(g.pool, 0, q, g.bt_dec, g.lens_post, out, lse, scale=w.scale)
+            ev_b[i].record(stream)
+        t_end.record(stream)
+        barrier()
+    launches = kvc.kvc_launch_count() - launches0
+    ms = t_start.elapsed_time(t_end) / K
+    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]))
+    clocks = clk.summary()
+    assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+
+    # ---- end to end through the public API: pinned host inputs in, results out, every step
+    q_h = torch.empty_like(q, device="cpu").pin_memory()
+    k_h = torch.empty_like(k_new, device="cpu").pin_memory()
+    v_h = torch.empty_like(v_new, device="cpu").pin_memory()
+    bt_h = g.bt_dec.cpu().pin_memory()
+    lp_h, lq_h = g.lens_pre.cpu().pin_memory(), g.lens_post.cpu().pin_memory()
+    q_h.copy_(q)
+    k_h.copy_(k_new)
+    v_h.copy_(v_new)
+    out_h = torch.empty_like(out, device="cpu").pin_memory()
+    lse_h = torch.empty_like(lse, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, bt_h, lp_h, lq_h))
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e_start.record(stream)
+    for i in range(K):
+        q.copy_(q_h, non_blocking=True)
+        k_new.copy_(k_h, non_blocking=True)
+        v_new.copy_(v_h, non_blocking=True)
+        g.bt_dec.copy_(bt_h, non_blocking=True)
+        g.lens_pre.copy_(lp_h, non_blocking=True)
+        g.lens_post.copy_(lq_h, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+    e_end.record(stream)
+    barrier()
+    e2e_ms = e_start.elapsed_time(e_end) / K
+
+    # ---- max over ranks
+    vals = torch.tensor([ms, e2e_ms, attn_ms], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    ms, e2e_ms, attn_ms = [float(x) for x in vals.cpu()]
+    total_bytes = sb["total"] * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+    e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+    hbm, peak_kind = peaks()
+    achieved = sb["attn_kernel"] / (attn_ms * 1e-3) / 1e9
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, dt, k, desc, cores = oracle_sample(w, ld, args.cpu_budget)
+        cpu = {"value": rate / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{desc}; {dt:.1f} s"}
+    if rank == 0:
+        splits_note = "one kernel per call" if launches == 2 * K else f"{launches / K:.1f} launches per step"
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": w.dtype, "data": "synthetic", "config": config_dict(w),
+                "tokens_per_s": w.B * world / (ms * 1e-3),
+                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "ms_per_step": e2e_ms, "tokens_per_s": w.B * world / (e2e_ms * 1e-3)},
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                             "frac": achieved / hbm, "traffic": profiled_traffic(w.name),
+                             "kernel": "decode_kernel (kvc_decode_attn)", "peak_source": f"{peak_kind} hbm_gbs",
+                             "algorithmic_bytes_per_launch": sb["attn_kernel"], "launch_ms": attn_ms,
+                             "note": splits_note},
+                "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
+                "step_bytes": sb}
+        print(json.dumps(line), flush=True)
+    g.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,241 @@
+/*
+ * kvc.h -- C ABI of libkvc, a paged KV cache and its decode step on NVIDIA
+ * GB300 (sm_103a).
+ *
+ * What is computed follows three pages:
+ *   "KV cache: Generation state, latency, and allocation" (aisyseng.dev,
+ *   chapter 21), "KV Cache Explained: The Memory Problem Behind Fast LLM
+ *   Inference" (archcrux.com) and the xf_kv_cache page (aicassindra.com).
+ * Each entry point names the passage that defines its operation.
+ *
+ * Conventions for every call
+ *   - Pointers marked "device" are caller-owned CUDA device memory of the
+ *     pool's device; the library never frees them and keeps none after the
+ *     call returns.  The pool owns its own device memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued asynchronously on it; the status reports argument validation
+ *     and launch errors synchronously.  Problems that only the device can see
+ *     (a table entry outside the pool, a position past its table row, a
+ *     bounded wait that expired) never fault the GPU: the kernel skips the
+ *     access and records an error bit, returned by kvc_pool_sync_status.
+ *   - Calls on one pool share its workspace and error word: order them on one
+ *     stream (or serialise them).  A call made while the device is current
+ *     on another GPU than the pool's returns KVC_ERR_ARG.
+ *   - Block tables are int32 [B][max_blocks], row-major; entry j of row b is
+ *     the physical block holding positions [j*bs, (j+1)*bs) of sequence b, or
+ *     -1 when none is allocated.  One table serves every layer (a block id
+ *     names the same block in every layer's region).
+ *
+ * Pool layout in HBM (layout version 1): one allocation; layer l, physical
+ * block p, keys (kv = 0) or values (kv = 1), KV head h, slot s, channel c is
+ * the element at index
+ *        ((((l * N + p) * H_KV + h) * 2 + kv) * bs + s) * d_h + c
+ * of bf16 (2 bytes) or e4m3 (1 byte) elements.  The keys and values of one
+ * (layer, block, head) are therefore one contiguous run of 2*bs*d_h elements
+ * (8 KiB for bs 16, d_h 128, bf16), which the decode kernel moves with one
+ * tensor-memory-accelerator copy per 128-byte column band.
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVC_API __attribute__((visibility("default")))
+#else
+#define KVC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kvc_pool kvc_pool;   /* opaque; owns its device memory */
+typedef void *kvc_stream_t;         /* a cudaStream_t */
+
+typedef enum {
+    KVC_BF16 = 0,       /* 2-byte bfloat16 elements, stored bit for bit */
+    KVC_FP8_E4M3 = 1    /* 1-byte OCP E4M3 ("FN") elements with fp32 per-(head, channel) scales */
+} kvc_dtype;
+
+typedef enum {
+    KVC_OK = 0,
+    KVC_ERR_ARG = 1,          /* invalid argument (null pointer, shape, layer, misaligned pointer, wrong device) */
+    KVC_ERR_OOM = 2,          /* device allocation failed */
+    KVC_ERR_BAD_BLOCK = 3,    /* a table entry read by the kernel is -1 or >= num_blocks (device-detected) */
+    KVC_ERR_RANGE = 4,        /* a position lies past its table row, or a length is negative (device-detected) */
+    KVC_ERR_ALIAS = 5,        /* reserved: two writes of one call aimed at one slot */
+    KVC_ERR_STALE = 6,        /* reserved: a table stamped for another pool generation */
+    KVC_ERR_TIMEOUT = 7,      /* a bounded device-side wait expired; results of that call are invalid */
+    KVC_ERR_CUDA = 8,         /* a CUDA runtime call failed */
+    KVC_ERR_UNSUPPORTED = 9   /* a valid shape this build has no kernel for (see each call) */
+} kvc_status;
+
+/* Pool description returned by kvc_pool_info. */
+typedef struct {
+    int32_t layout_version;         /* 1: the index formula above */
+    int32_t block_size;             /* bs, positions per block */
+    int32_t num_layers;             /* L */
+    int32_t num_kv_heads;           /* H_KV */
+    int32_t head_dim;               /* d_h */
+    int32_t dtype;                  /* kvc_dtype */
+    int32_t elem_bytes;             /* s: 2 (bf16) or 1 (e4m3) */
+    int32_t device;                 /* CUDA ordinal the pool lives on */
+    int64_t num_blocks;             /* N */
+    uint64_t block_bytes_per_layer; /* 2 * H_KV * bs * d_h * s */
+    uint64_t layer_bytes;           /* N * block_bytes_per_layer */
+    uint64_t bytes_per_token;       /* 2 * L * H_KV * d_h * s  ("KV Cache Explained", per-token size) */
+    uint64_t capacity_tokens;       /* N * bs */
+    uint64_t pool_bytes;            /* L * layer_bytes */
+    void *base;                     /* device pointer of element 0 */
+    float *scales;                  /* device fp32 [L][2][H_KV][d_h] (keys first) for e4m3 pools, else NULL */
+} kvc_pool_desc;
+
+/* ------------------------------------------------------------------ pool */
+
+/* Allocate a pool of `num_blocks` fixed-size physical blocks of `block_size`
+ * positions for `num_layers` layers on the current device
+ * ("KV cache: Generation state, latency, and allocation" 21.5: fixed-size
+ * blocks allocated as sequences grow; "KV Cache Explained", "Why
+ * PagedAttention allocates KV in blocks": the pool is initialised up front).
+ * Bytes: L * N * 2 * H_KV * bs * d_h * s, plus for e4m3 the scale array
+ * (initialised to 1.0).  Pool contents are uninitialised.
+ * Limits: 1 <= block_size <= 128, head_dim in {64, 128, 256} for bf16 and
+ * {128, 256} for e4m3, 1 <= H_KV <= 256, num_blocks >= 1, the pool's total
+ * row count L*N*H_KV*2*bs < 2^31.  Errors: KVC_ERR_ARG, KVC_ERR_OOM,
+ * KVC_ERR_CUDA; *out is NULL on error. */
+KVC_API kvc_status kvc_pool_create(int64_t num_blocks, int32_t block_size, int32_t num_layers,
+                           int32_t num_kv_heads, int32_t head_dim, kvc_dtype dtype, kvc_pool **out);
+
+/* Free the pool's device memory after synchronising the device.  NULL is a no-op. */
+KVC_API void kvc_pool_destroy(kvc_pool *pool);
+
+/* Fill *desc.  Errors: KVC_ERR_ARG for NULL arguments. */
+KVC_API kvc_status kvc_pool_info(const kvc_pool *pool, kvc_pool_desc *desc);
+
+/* Set layer `layer`'s e4m3 scales: s_k, s_v are device fp32 [H_KV][d_h]
+ * ("KV Cache Explained", "What changes when you use FP8 KV": quantized values
+ * need scales; per-(KV head, channel) granularity).  Stored as given; a
+ * scale must be a positive finite float.  Errors: KVC_ERR_ARG (bf16 pool,
+ * layer out of range, NULL), KVC_ERR_CUDA. */
+KVC_API kvc_status kvc_pool_set_scales(kvc_pool *pool, int32_t layer, const float *s_k, const float *s_v,
+                               kvc_stream_t stream);
+
+/* Calibrate layer `layer`'s e4m3 scales from bf16 tokens: absmax over the
+ * given positions per (KV head, channel), divided by 448 (the largest finite
+ * E4M3 value), in fp32; a channel whose absmax is 0 gets scale 1.
+ * k, v: device bf16 [n_tokens][H_KV][d_h].  With accumulate = 0 the running
+ * absmax is reset first; with accumulate = 1 it extends the previous calls',
+ * so a context uploaded in pieces calibrates like one array.  The scales are
+ * rewritten after every call.  Errors: KVC_ERR_ARG, KVC_ERR_CUDA. */
+KVC_API kvc_status kvc_calibrate_fp8(kvc_pool *pool, int32_t layer, const void *k, const void *v,
+                             int64_t n_tokens, int32_t accumulate, kvc_stream_t stream);
+
+/* ------------------------------------------------------------------ append */
+
+/* Append one processed token per sequence at one layer
+ * ("KV cache: Generation state, latency, and allocation" Eq. 21.6,
+ * cache_t = append(cache_{t-1}, K_t, V_t), and Table 21.1 steps 1-2).
+ * Sequence b's new key and value are written at position t = seq_lens[b]:
+ * physical block block_tables[b][t / bs], slot t mod bs.  bf16 pools store
+ * the bits unchanged; e4m3 pools store e4m3(fp32(k) / scale[h][c]) rounded to
+ * nearest even and saturated to +-448.
+ *   block_tables: device int32 [B][max_blocks]
+ *   seq_lens:     device int32 [B], tokens held BEFORE the append (the write
+ *                 position); the library never changes it
+ *   k_new, v_new: device bf16 [B][H_KV][d_h], 4-byte aligned
+ * The caller allocates block table[b][t / bs] before the call (the scheduler
+ * owns allocation).  A token whose block entry is -1 / >= N, or whose
+ * position is past the row, is skipped and recorded (KVC_ERR_BAD_BLOCK /
+ * KVC_ERR_RANGE via kvc_pool_sync_status).  B = 0 is a no-op.
+ * Errors (synchronous): KVC_ERR_ARG, KVC_ERR_CUDA. */
+KVC_API kvc_status kvc_append(kvc_pool *pool, int32_t layer, const int32_t *block_tables, int32_t max_blocks,
+                      const int32_t *seq_lens, int32_t B, const void *k_new, const void *v_new,
+                      kvc_stream_t stream);
+
+/* Write a ragged batch of tokens, e.g. a prompt's or a prefill chunk's keys
+ * and values (same passage as kvc_append, repeated for consecutive
+ * positions).  Sequence b receives rows cu_tokens[b] .. cu_tokens[b+1]-1 of
+ * k and v at positions start_pos[b], start_pos[b]+1, ...
+ *   cu_tokens: device int32 [B+1], non-decreasing prefix sums from 0
+ *   start_pos: device int32 [B]
+ *   max_tokens: host upper bound of cu_tokens[b+1]-cu_tokens[b] (grid size);
+ *               rows beyond it are not written
+ *   k, v: device bf16 [cu_tokens[B]][H_KV][d_h]
+ * Same storage rule and error behaviour as kvc_append. */
+KVC_API kvc_status kvc_write_tokens(kvc_pool *pool, int32_t layer, const int32_t *block_tables, int32_t max_blocks,
+                            const int32_t *start_pos, const int32_t *cu_tokens, int32_t B, int32_t max_tokens,
+                            const void *k, const void *v, kvc_stream_t stream);
+
+/* ------------------------------------------------------------------ attention */
+
+/* Paged decode attention at one layer
+ * ("KV cache: Generation state, latency, and allocation" 21.1: the new query
+ * reads the cached keys and its own new key, normalises the scores and mixes
+ * the values; 21.5: attention follows the block table; padded or unfilled
+ * slots are excluded; the xf_kv_cache page: GQA head sharing).
+ * For each sequence b and query head hq, with h = hq / (H_Q / H_KV) and
+ * n = seq_lens[b] positions (the appended token included):
+ *   x_t = scale * <q[b][hq], K[b][t][h]>,  t < n
+ *   out[b][hq] = sum_t softmax(x)_t V[b][t][h],   lse[b][hq] = ln sum_t exp(x_t)
+ * computed in fp32 on tensor cores (bf16 or f16 operands, fp32 accumulation)
+ * with a split-K online softmax and a log-sum-exp merge.  For e4m3 pools the
+ * key scales are folded into q and the value scales into the output.
+ *   q:        device bf16 [B][H_Q][d_h], 4-byte aligned
+ *   seq_lens: device int32 [B], positions attended (after the append);
+ *             n = 0 gives out = 0 and lse = -inf
+ *   out:      device fp32 [B][H_Q][d_h];  lse: device fp32 [B][H_Q] or NULL
+ * Requires block_size == 16, H_Q % H_KV == 0 and H_Q / H_KV <= 32
+ * (else KVC_ERR_UNSUPPORTED / KVC_ERR_ARG).  The pool's workspace for
+ * split partials grows on first use with a larger batch (a cudaMalloc, so
+ * make one call before capturing a CUDA graph; see kvc_pool_reserve).
+ * Device-detected errors as for kvc_append; the affected sequence's outputs
+ * are then zero.  Errors (synchronous): KVC_ERR_ARG, KVC_ERR_UNSUPPORTED,
+ * KVC_ERR_OOM, KVC_ERR_CUDA. */
+KVC_API kvc_status kvc_decode_attn(kvc_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
+                           const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, int32_t B,
+                           float *out, float *lse, float scale, kvc_stream_t stream);
+
+/* Causal attention of a prefill chunk over one sequence's paged cache
+ * ("KV cache: Generation state, latency, and allocation" 21.3, chunked
+ * prefill: later portions keep the earlier positions; the xf_kv_cache page,
+ * "End-to-end flow": the new tokens attend to the shared prefix, the table
+ * stitching shared and private blocks into one sequence).  Query i sits at
+ * position q_start + i and reads positions 0 .. q_start + i, so its keys and
+ * values must already be in the pool (kvc_write_tokens).
+ *   q: device bf16 [n_q][H_Q][d_h];  block_table_row: device int32 [max_blocks]
+ *   out: device fp32 [n_q][H_Q][d_h];  lse: device fp32 [n_q][H_Q] or NULL
+ * Same arithmetic, requirements and errors as kvc_decode_attn. */
+KVC_API kvc_status kvc_prefill_attn(kvc_pool *pool, int32_t layer, const void *q, int32_t n_q, int32_t num_q_heads,
+                            const int32_t *block_table_row, int32_t max_blocks, int32_t q_start,
+                            float *out, float *lse, float scale, kvc_stream_t stream);
+
+/* Pre-size the decode workspace for up to max_batch sequences of up to
+ * max_blocks table entries and num_q_heads query heads, so that later calls
+ * allocate nothing.  Errors: KVC_ERR_ARG, KVC_ERR_OOM. */
+KVC_API kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_t num_q_heads, int32_t max_blocks);
+
+/* ------------------------------------------------------------------ host utilities */
+
+/* Ideal KV payload in bytes
+ * ("KV cache: Generation state, latency, and allocation" Eq. 21.2):
+ * 2 * L * B * H_KV * T * d_h * s.  Pure host arithmetic, exact in uint64;
+ * returns UINT64_MAX if an argument is negative or the product overflows. */
+KVC_API uint64_t kvc_bytes(int64_t L, int64_t B, int64_t H_KV, int64_t T, int64_t d_h, int64_t s);
+
+/* Wait for `stream`, then return and clear the pool's device-detected error
+ * bits (the first of BAD_BLOCK, RANGE, TIMEOUT that is set), or KVC_OK.  A
+ * CUDA error seen while waiting returns KVC_ERR_CUDA. */
+KVC_API kvc_status kvc_pool_sync_status(kvc_pool *pool, kvc_stream_t stream);
+
+/* Static description of a status code. */
+KVC_API const char *kvc_status_str(kvc_status status);
+
+/* Kernels this library has launched in this process (all pools, all devices). */
+KVC_API uint64_t kvc_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H_ */

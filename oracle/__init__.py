@@ -69,6 +69,8 @@ def lib():
         L.orc_e4m3_from_float.argtypes = [ctypes.c_float]
         L.orc_fp8_scales.restype = None
         L.orc_fp8_scales.argtypes = [vp, i64, i32, i32, vp]
+        L.orc_quantize_e4m3.restype = None
+        L.orc_quantize_e4m3.argtypes = [vp, i64, i32, i32, vp, vp]
         L.orc_locate.restype = ctypes.c_int
         L.orc_locate.argtypes = [vp, i32, i64, i32, i64, vp, vp]
         L.orc_pool_offset.restype = u64
@@ -126,6 +128,16 @@ def fp8_scales(x_bits: np.ndarray) -> np.ndarray:
     n, H, d = x_bits.shape
     out = np.empty((H, d), dtype=np.float32)
     lib().orc_fp8_scales(_p(x_bits), n, H, d, _p(out))
+    return out
+
+
+def quantize_e4m3(x_bits: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """bf16 [n][H_KV][d_h] -> e4m3 codes under fp32 scales [H_KV][d_h] (the append's rule)."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    n, H, d = x_bits.shape
+    sc = np.ascontiguousarray(scales, dtype=np.float32).reshape(H, d)
+    out = np.empty((n, H, d), dtype=np.uint8)
+    lib().orc_quantize_e4m3(_p(x_bits), n, H, d, _p(sc), _p(out))
     return out
 
 

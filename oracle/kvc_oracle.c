@@ -122,6 +122,19 @@ void orc_fp8_scales(const uint16_t *x, int64_t n_tokens, int32_t H_KV, int32_t d
     }
 }
 
+/* Stored e4m3 codes of bf16 tokens x [n][H_KV][d_h] under scales [H_KV][d_h]:
+ * e4m3(fp32(x) / scale), the same rule the append applies. */
+void orc_quantize_e4m3(const uint16_t *x, int64_t n_tokens, int32_t H_KV, int32_t d_h, const float *scale,
+                       uint8_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n_tokens; ++t)
+        for (int64_t hc = 0; hc < (int64_t)H_KV * d_h; ++hc) {
+            const float xf = (float)orc_bf16_to_double(x[t * H_KV * d_h + hc]);
+            out[t * H_KV * d_h + hc] = orc_e4m3_from_float(xf / scale[hc]);
+        }
+}
+
 /* ---------------------------------------------------------------- tables
  * [P1] 21.5: position t lies in logical block floor(t / bs), slot t mod bs;
  * the block table supplies the physical block.  Entries past a sequence's

@@ -1,0 +1,202 @@
+// Decode / prefill attention entry points, split sizing and the split merge.
+#include <cmath>
+#include <cstdlib>
+
+#include "kvc_decode.cuh"
+
+namespace kvc {
+
+// Log-sum-exp merge of a sequence's split partials ("flash-decoding"):
+//   M = max_s m_s,  L = sum_s 2^(m_s - M) l_s,  out = sum_s 2^(m_s - M) o_s / L,
+//   lse = (M + log2 L) ln 2.
+// Sequences with a single split were finished by the attention kernel.
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int D)
+{
+    const int hq = blockIdx.x, b = blockIdx.y;
+    int len = p.lens ? __ldg(p.lens + b) : p.len_base + b + 1;
+    if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) len = 0;
+    const int nblk = (len + kBS - 1) / kBS;
+    const int ns = (nblk + p.chunk - 1) / p.chunk;
+    if (ns <= 1) return;
+    const size_t bq = static_cast<size_t>(b) * p.H_Q + hq;
+    const float2 *ml = p.part_ml + bq * p.max_splits;
+    const float *po = p.part_o + bq * p.max_splits * D;
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s].x);
+    float L = 0.f;
+    for (int s = 0; s < ns; ++s) L += fast_exp2(ml[s].x - M) * ml[s].y;
+    const float inv = 1.f / L;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float o = 0.f;
+        for (int s = 0; s < ns; ++s) o += fast_exp2(ml[s].x - M) * po[static_cast<size_t>(s) * D + d];
+        p.out[bq * D + d] = o * inv;
+    }
+    if (threadIdx.x == 0 && p.lse) p.lse[bq] = (M + log2f(L)) * kLn2;
+}
+
+// Blocks per split.  Sequences are independent and every CTA reads only its
+// own blocks, so the kernel is bound by HBM as long as enough CTAs stream at
+// once; splitting a sequence costs a partial write and a merge.  Aim for one
+// CTA per resident slot, with at least 16 blocks (4 per warp) per CTA and at
+// most 1024.  KVC_SPLIT_CHUNK overrides (rounded up to a multiple of 4).
+void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits)
+{
+    int ch = 0;
+    if (const char *e = std::getenv("KVC_SPLIT_CHUNK")) ch = std::atoi(e);
+    if (ch <= 0) {
+        const long slots = static_cast<long>(pool->num_sms) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+        long ns = units > 0 ? slots / units : 1;
+        if (ns < 1) ns = 1;
+        ch = static_cast<int>((max_blocks + ns - 1) / ns);
+        if (ch < 16) ch = 16;
+        if (ch > 1024) ch = 1024;
+    }
+    ch = (ch + 3) & ~3;
+    *chunk = ch;
+    *max_splits = (max_blocks + ch - 1) / ch;
+}
+
+static kvc_status ensure_workspace(kvc_pool *pool, size_t bytes)
+{
+    if (bytes <= pool->ws_bytes) return KVC_OK;
+    if (pool->ws) {
+        cudaError_t e = cudaFree(pool->ws);
+        pool->ws = nullptr;
+        pool->ws_bytes = 0;
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    if (cudaMalloc(&pool->ws, bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        pool->ws = nullptr;
+        return KVC_ERR_OOM;
+    }
+    pool->ws_bytes = bytes;
+    return KVC_OK;
+}
+
+static size_t workspace_bytes(int B, int H_Q, int max_splits, int D)
+{
+    const size_t n = static_cast<size_t>(B) * H_Q * max_splits;
+    return n * D * sizeof(float) + n * sizeof(float2) + 256;
+}
+
+kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream)
+{
+    kvc_pool *pool = const_cast<kvc_pool *>(cpool);
+    if (!k.fn || k.ctas_per_sm <= 0) return KVC_ERR_CUDA;
+    choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits);
+    if (p.max_splits > 65535) return KVC_ERR_UNSUPPORTED;
+    if (p.max_splits > 1) {
+        kvc_status st = ensure_workspace(pool, workspace_bytes(p.B, p.H_Q, p.max_splits, pool->D));
+        if (st != KVC_OK) return st;
+        const size_t n = static_cast<size_t>(p.B) * p.H_Q * p.max_splits;
+        p.part_o = static_cast<float *>(pool->ws);
+        p.part_ml = reinterpret_cast<float2 *>(static_cast<float *>(pool->ws) + n * pool->D);
+    } else {
+        p.part_o = nullptr;
+        p.part_ml = nullptr;
+    }
+    const dim3 grid(p.max_splits, p.H_KV, p.B);
+    void *args[] = {const_cast<CUtensorMap *>(&pool->tmap), &p};
+    cudaError_t e = cudaLaunchKernel(k.fn, grid, dim3(kThreads), args, k.smem, stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (p.max_splits > 1) {
+        merge_kernel<<<dim3(p.H_Q, p.B), 128, 0, stream>>>(p, pool->D);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_status(e);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    return KVC_OK;
+}
+
+static bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+static kvc_status common_attn_checks(kvc_pool *pool, int32_t layer, const void *q, int32_t H_Q, const int32_t *bt,
+                                     int32_t max_blocks, float *out, float *lse, float scale)
+{
+    if (!pool || !q || !bt || !out) return KVC_ERR_ARG;
+    if (layer < 0 || layer >= pool->L) return KVC_ERR_ARG;
+    if (H_Q <= 0 || H_Q % pool->H_KV != 0) return KVC_ERR_ARG;
+    if (H_Q / pool->H_KV > 32) return KVC_ERR_UNSUPPORTED;
+    if (pool->bs != kBS || !pool->tmap_ok) return KVC_ERR_UNSUPPORTED;
+    if (max_blocks <= 0 || max_blocks > (1 << 26)) return KVC_ERR_ARG;
+    if (!std::isfinite(scale)) return KVC_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4)) || !aligned(bt, 4)) return KVC_ERR_ARG;
+    return check_device(pool);
+}
+
+static void fill_common(DecodeParams &p, const kvc_pool *pool, int32_t layer, const void *q, int32_t H_Q,
+                        const int32_t *bt, int32_t max_blocks, float *out, float *lse, float scale)
+{
+    p.q = static_cast<const uint16_t *>(q);
+    p.bt = bt;
+    p.max_blocks = max_blocks;
+    p.H_Q = H_Q;
+    p.H_KV = pool->H_KV;
+    p.g = H_Q / pool->H_KV;
+    p.layer = layer;
+    p.N = pool->N;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.s_k = pool->scales ? pool->scales + static_cast<size_t>(layer) * 2 * pool->H_KV * pool->D : nullptr;
+    p.s_v = p.s_k ? p.s_k + static_cast<size_t>(pool->H_KV) * pool->D : nullptr;
+    p.out = out;
+    p.lse = lse;
+    p.err = pool->err;
+}
+
+static kvc_status dispatch(kvc_pool *pool, DecodeParams &p, cudaStream_t stream)
+{
+    return pool->dtype == KVC_FP8_E4M3 ? launch_decode_fp8(pool, p, stream) : launch_decode_bf16(pool, p, stream);
+}
+
+}  // namespace kvc
+
+using namespace kvc;
+
+extern "C" kvc_status kvc_decode_attn(kvc_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
+                                      const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
+                                      int32_t B, float *out, float *lse, float scale, kvc_stream_t stream)
+{
+    if (B < 0 || B > 65535) return KVC_ERR_ARG;
+    if (B == 0) return pool ? KVC_OK : KVC_ERR_ARG;
+    if (!seq_lens || !aligned(seq_lens, 4)) return KVC_ERR_ARG;
+    kvc_status st = common_attn_checks(pool, layer, q, num_q_heads, block_tables, max_blocks, out, lse, scale);
+    if (st != KVC_OK) return st;
+    DecodeParams p{};
+    fill_common(p, pool, layer, q, num_q_heads, block_tables, max_blocks, out, lse, scale);
+    p.lens = seq_lens;
+    p.bt_stride = max_blocks;
+    p.len_base = 0;
+    p.B = B;
+    return dispatch(pool, p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvc_status kvc_prefill_attn(kvc_pool *pool, int32_t layer, const void *q, int32_t n_q,
+                                       int32_t num_q_heads, const int32_t *block_table_row, int32_t max_blocks,
+                                       int32_t q_start, float *out, float *lse, float scale, kvc_stream_t stream)
+{
+    if (n_q < 0 || n_q > 65535 || q_start < 0) return KVC_ERR_ARG;
+    if (n_q == 0) return pool ? KVC_OK : KVC_ERR_ARG;
+    kvc_status st = common_attn_checks(pool, layer, q, num_q_heads, block_table_row, max_blocks, out, lse, scale);
+    if (st != KVC_OK) return st;
+    if (static_cast<int64_t>(q_start) + n_q > static_cast<int64_t>(max_blocks) * kBS) return KVC_ERR_RANGE;
+    DecodeParams p{};
+    fill_common(p, pool, layer, q, num_q_heads, block_table_row, max_blocks, out, lse, scale);
+    // query i is a decode over the same row with length q_start + i + 1
+    p.lens = nullptr;
+    p.bt_stride = 0;
+    p.len_base = q_start;
+    p.B = n_q;
+    return dispatch(pool, p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_t num_q_heads, int32_t max_blocks)
+{
+    if (!pool || max_batch < 0 || num_q_heads <= 0 || max_blocks <= 0) return KVC_ERR_ARG;
+    kvc_status st = check_device(pool);
+    if (st != KVC_OK) return st;
+    // the largest split count any batch of this size can get is the 16-block floor
+    const int max_splits = (max_blocks + 15) / 16;
+    return ensure_workspace(pool, workspace_bytes(max_batch, num_q_heads, max_splits, pool->D));
+}

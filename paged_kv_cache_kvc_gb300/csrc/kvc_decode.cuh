@@ -1,0 +1,439 @@
+// Paged decode attention over a block table, split-K with an online softmax.
+//
+// What it computes ("KV cache: Generation state, latency, and allocation"
+// 21.1 and 21.5): for sequence b, KV head h and each of its g query heads,
+// softmax(scale * q K^T) V over the n = lens[b] positions that the table maps,
+// excluding every slot at or past n.
+//
+// Work decomposition
+//   grid (split, h, b); 128 threads = 4 warps.  A CTA owns logical blocks
+//   [split*chunk, min(nblk, (split+1)*chunk)) of (b, h) and all g query heads
+//   that share KV head h, so each KV byte leaves HBM once.  Warp w takes the
+//   CTA's blocks w, w+4, w+8, ... and keeps its own running max / sum / output.
+//   Each warp runs a private ring of R shared-memory stages: one elected lane
+//   issues tensor-memory-accelerator (TMA) tile loads of a block's 16 key rows
+//   and 16 value rows (one contiguous run in the pool) per 128-byte column band,
+//   completing on the stage's mbarrier; the warp waits (bounded), computes, and
+//   refills the stage with the block R ahead.
+//
+// Per 16-token block, on tensor cores (mma.sync m16n8k16, fp32 accumulation):
+//   S^T[16 tok x 8q] = K[16 x D] * Q^T[D x 8q]        (tokens are the M dimension,
+//                                                      so g <= 8 pads only to N = 8)
+//   online softmax over the tokens (warp shuffles across the 8 lanes of a column)
+//   O^T[D x 8q]     += V^T[D x 16] * P^T[16 x 8q]     (P^T by movmatrix from S^T)
+// bf16 pools feed bf16 operands; P is split into a bf16 high and low part
+// (two mma) so the value mixture keeps ~16 bits of each weight.  e4m3 pools
+// convert codes to f16 in registers (exact) and fold the key scales into q
+// (f16) and the value scales into the output.
+//
+// TMA writes the tiles with the 128-byte swizzle: within each 128-byte row of
+// a band, 16-byte chunk c sits at c ^ (row mod 8), so the ldmatrix and 16-byte
+// loads below hit 8 distinct bank groups.
+#pragma once
+#include <cfloat>
+#include <cmath>
+
+#include "kvc_internal.h"
+#include "kvc_ptx.cuh"
+
+namespace kvc {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kBS = 16;                 // positions per block = mma M tile
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D, bool FP8>
+struct DecodeCfg {
+    static constexpr int ELEM = FP8 ? 1 : 2;
+    static constexpr int ROW_BYTES = D * ELEM;
+    static constexpr int BANDS = ROW_BYTES / 128;          // 128-byte column bands (one TMA box each)
+    static constexpr int BAND_BYTES = 2 * kBS * 128;       // 32 rows (keys then values) x 128 B
+    static constexpr int STAGE = BANDS * BAND_BYTES;
+    static constexpr int R0 = 98304 / (kWarps * STAGE);
+    static constexpr int R = R0 < 2 ? 2 : (R0 > 4 ? 4 : R0);   // ring depth per warp
+    static constexpr int KSTEPS = D / 16;
+    static constexpr int MT = D / 16;
+    static constexpr int BOX_X = 128 / ELEM;               // elements per band row
+    static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte bands");
+};
+
+template <int D, int NT, bool FP8>
+__host__ __device__ constexpr int decode_smem_bytes()
+{
+    using C = DecodeCfg<D, FP8>;
+    constexpr int stages = kWarps * C::R * C::STAGE;
+    constexpr int combine = (kWarps * NT * 8 * 2 + kWarps * NT * 8 * D) * 4;
+    constexpr int region = stages > combine ? stages : combine;
+    return 1024 /* alignment slack */ + region + kWarps * C::R * 8 /* mbarriers */;
+}
+
+// byte offset of (row, 16-byte chunk) inside a stage, 128-byte swizzle
+__device__ __forceinline__ uint32_t swz(int row, int ch)
+{
+    const int band = ch >> 3, c = ch & 7;
+    return static_cast<uint32_t>((band * 2 * kBS + row) * 128 + ((c ^ (row & 7)) << 4));
+}
+
+template <int D, int NT, bool FP8, bool PSPLIT>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                          const DecodeParams p)
+{
+    using C = DecodeCfg<D, FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tg = lane & 3;
+    const int hq0 = h * p.g;
+
+    int len = p.lens ? __ldg(p.lens + b) : p.len_base + b + 1;
+    if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) {
+        if (split == 0 && threadIdx.x == 0) atomicOr(p.err, KVC_EBIT_RANGE);
+        len = 0;
+    }
+    const int nblk = (len + kBS - 1) / kBS;
+    if (nblk == 0) {   // empty sequence: zero output, lse = -inf
+        if (split == 0) {
+            for (int i = threadIdx.x; i < p.g * D; i += kThreads)
+                p.out[(static_cast<size_t>(b) * p.H_Q + hq0) * D + i] = 0.f;
+            if (p.lse && threadIdx.x < p.g) p.lse[static_cast<size_t>(b) * p.H_Q + hq0 + threadIdx.x] = -INFINITY;
+        }
+        return;
+    }
+    const int blk0 = split * p.chunk;
+    if (blk0 >= nblk) return;
+    const int nloc = min(nblk, blk0 + p.chunk) - blk0;
+    const int32_t *bt_row = p.bt + static_cast<int64_t>(b) * p.bt_stride + blk0 + warp;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (decode_smem_bytes<D, NT, FP8>() - 1024 - kWarps * C::R * 8));
+    if (lane == 0) {
+        for (int s = 0; s < C::R; ++s) mbar_init(smem_u32(&bars[warp * C::R + s]), 1);
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 0) prefetch_tensormap(&tmap);
+    __syncthreads();
+
+    const int nmine = nloc > warp ? (nloc - warp + kWarps - 1) / kWarps : 0;   // this warp's blocks
+    const uint32_t st_base = smem_u32(smem + warp * C::R * C::STAGE);
+    const uint32_t bar_base = smem_u32(&bars[warp * C::R]);
+    const int64_t row_layer = static_cast<int64_t>(p.layer) * p.N;
+
+    // Table entries of this warp's blocks, 32 at a time in registers: lane i
+    // holds local block 32*k + i of the current batch (t_cur) and the next (t_next).
+    auto load_entry = [&](int jj) -> int32_t { return jj < nmine ? __ldg(bt_row + kWarps * jj) : -1; };
+    int32_t t_cur = load_entry(lane), t_next = load_entry(32 + lane);
+    auto entry = [&](int jj, int jbase) -> int32_t {
+        const int32_t v = (jj - jbase < 32) ? t_cur : t_next;
+        return __shfl_sync(kFull, v, (jj - jbase) & 31);
+    };
+    auto issue = [&](int jj, int jbase) {   // warp-collective; lane 0 issues
+        const int32_t phys = entry(jj, jbase);
+        if (lane == 0) {
+            const uint32_t bar = bar_base + 8u * static_cast<uint32_t>(jj % C::R);
+            if (phys < 0 || static_cast<int64_t>(phys) >= p.N) {
+                atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
+                mbar_arrive(bar);   // complete the phase without data; the consumer skips it
+            } else {
+                const int32_t y = static_cast<int32_t>(((row_layer + phys) * p.H_KV + h) * (2 * kBS));
+                const uint32_t dst = st_base + static_cast<uint32_t>((jj % C::R) * C::STAGE);
+                mbar_arrive_expect_tx(bar, C::STAGE);
+#pragma unroll
+                for (int band = 0; band < C::BANDS; ++band)
+                    tma_load_2d(dst + band * C::BAND_BYTES, &tmap, bar, band * C::BOX_X, y);
+            }
+        }
+    };
+
+    // ---- query fragments (B operand, k = channel, n = query head of the group)
+    uint32_t qf[NT][C::KSTEPS][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int qi = 8 * j + gq;
+        const bool real = qi < p.g;
+        const uint16_t *qrow = p.q + (static_cast<size_t>(b) * p.H_Q + hq0 + (real ? qi : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            if constexpr (!FP8) {
+                qf[j][kk][0] = real ? *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 2 * tg) : 0u;
+                qf[j][kk][1] = real ? *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 8 + 2 * tg) : 0u;
+            } else {
+                // channel slots permuted: thread tg owns channels [tg*D/4, (tg+1)*D/4), four per k-step
+                const int c0 = (D / 4) * tg + 4 * kk;
+                const uint2 raw = real ? *reinterpret_cast<const uint2 *>(qrow + c0) : make_uint2(0u, 0u);
+                const float *sk = p.s_k + static_cast<size_t>(h) * D + c0;
+                qf[j][kk][0] = pack_f16(bf16_lo(raw.x) * __ldg(sk + 0), bf16_hi(raw.x) * __ldg(sk + 1));
+                qf[j][kk][1] = pack_f16(bf16_lo(raw.y) * __ldg(sk + 2), bf16_hi(raw.y) * __ldg(sk + 3));
+            }
+        }
+    }
+
+    float m_run[NT][2], l_run[NT][2];
+    float oacc[C::MT][NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        m_run[j][0] = m_run[j][1] = -INFINITY;
+        l_run[j][0] = l_run[j][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) oacc[mt][j][0] = oacc[mt][j][1] = oacc[mt][j][2] = oacc[mt][j][3] = 0.f;
+    }
+
+    for (int jj = 0; jj < min(C::R, nmine); ++jj) issue(jj, 0);
+
+    int j = 0;
+    bool timed_out = false;
+    for (; j < nmine; ++j) {
+        const int jbase = j & ~31;
+        if (j > 0 && (j & 31) == 0) {
+            t_cur = t_next;
+            t_next = load_entry(j + 32 + lane);
+        }
+        const int s = j % C::R;
+        const bool ok = mbar_wait_bounded(bar_base + 8u * s, static_cast<uint32_t>((j / C::R) & 1));
+        if (!__all_sync(kFull, ok)) {
+            timed_out = true;
+            break;
+        }
+        const int32_t phys = entry(j, jbase);
+        if (phys >= 0 && static_cast<int64_t>(phys) < p.N) {
+            const uint32_t st = st_base + static_cast<uint32_t>(s * C::STAGE);
+            const int valid = min(kBS, len - (blk0 + warp + kWarps * j) * kBS);
+
+            // value rows past the sequence end may hold anything (NaN included): zero them
+            if (valid < kBS) {
+                const int nz = (kBS - valid) * C::BANDS * 8;
+                for (int i = lane; i < nz; i += 32) sts128_zero(st + swz(kBS + valid + i / (C::BANDS * 8), i % (C::BANDS * 8)));
+                __syncwarp();
+            }
+
+            // ---- S^T = K Q^T
+            float sc[NT][4];
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn) sc[jn][0] = sc[jn][1] = sc[jn][2] = sc[jn][3] = 0.f;
+            if constexpr (!FP8) {
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    uint32_t a[4];
+                    ldsm_x4(a, st + swz((lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)));
+#pragma unroll
+                    for (int jn = 0; jn < NT; ++jn) mma_bf16(sc[jn], a, qf[jn][kk]);
+                }
+            } else {
+                uint32_t kw[2][D / 16];   // rows gq, gq+8: this thread's D/4 code bytes each
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int u = 0; u < D / 64; ++u) {
+                        const uint4 v = lds128(st + swz(gq + 8 * r, (D / 64) * tg + u));
+                        kw[r][4 * u + 0] = v.x;
+                        kw[r][4 * u + 1] = v.y;
+                        kw[r][4 * u + 2] = v.z;
+                        kw[r][4 * u + 3] = v.w;
+                    }
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    uint32_t a[4];
+                    a[0] = e4m3x2_to_f16x2(kw[0][kk]);
+                    a[1] = e4m3x2_to_f16x2(kw[1][kk]);
+                    a[2] = e4m3x2_to_f16x2(kw[0][kk] >> 16);
+                    a[3] = e4m3x2_to_f16x2(kw[1][kk] >> 16);
+#pragma unroll
+                    for (int jn = 0; jn < NT; ++jn) mma_f16(sc[jn], a, qf[jn][kk]);
+                }
+            }
+
+            // ---- online softmax (log2 domain); column = query head, rows = tokens gq, gq+8
+            uint32_t pb[NT][2], pl[NT][2];
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int tok = gq + ((c >> 1) << 3);
+                    sc[jn][c] = tok < valid ? sc[jn][c] * p.scale_log2 : -INFINITY;
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float bm = fmaxf(sc[jn][c], sc[jn][c + 2]);
+                    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
+                    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+                    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
+                    const float mn = fmaxf(m_run[jn][c], bm);    // finite: every block has a valid token
+                    const float alpha = fast_exp2(m_run[jn][c] - mn);
+                    const float p0 = fast_exp2(sc[jn][c] - mn), p1 = fast_exp2(sc[jn][c + 2] - mn);
+                    m_run[jn][c] = mn;
+                    l_run[jn][c] = l_run[jn][c] * alpha + p0 + p1;
+                    sc[jn][c] = p0;
+                    sc[jn][c + 2] = p1;
+#pragma unroll
+                    for (int mt = 0; mt < C::MT; ++mt) {
+                        oacc[mt][jn][c] *= alpha;
+                        oacc[mt][jn][c + 2] *= alpha;
+                    }
+                }
+                if constexpr (!FP8) {
+                    const uint32_t h0 = pack_bf16(sc[jn][0], sc[jn][1]), h1 = pack_bf16(sc[jn][2], sc[jn][3]);
+                    pb[jn][0] = movmatrix_trans(h0);
+                    pb[jn][1] = movmatrix_trans(h1);
+                    if constexpr (PSPLIT) {
+                        pl[jn][0] = movmatrix_trans(pack_bf16(sc[jn][0] - bf16_lo(h0), sc[jn][1] - bf16_hi(h0)));
+                        pl[jn][1] = movmatrix_trans(pack_bf16(sc[jn][2] - bf16_lo(h1), sc[jn][3] - bf16_hi(h1)));
+                    }
+                } else {
+                    pb[jn][0] = movmatrix_trans(pack_f16(sc[jn][0], sc[jn][1]));
+                    pb[jn][1] = movmatrix_trans(pack_f16(sc[jn][2], sc[jn][3]));
+                }
+            }
+
+            // ---- O^T += V^T P^T
+            if constexpr (!FP8) {
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    uint32_t a[4];
+                    ldsm_x4_trans(a, st + swz(kBS + (lane & 7) + ((lane >> 4) & 1) * 8, 2 * mt + ((lane >> 3) & 1)));
+#pragma unroll
+                    for (int jn = 0; jn < NT; ++jn) {
+                        mma_bf16(oacc[mt][jn], a, pb[jn]);
+                        if constexpr (PSPLIT) mma_bf16(oacc[mt][jn], a, pl[jn]);
+                    }
+                }
+            } else {
+                // output channels permuted: m-row r of tile mt is channel gq*D/8 + 2*mt (+1 for r >= 8)
+                uint32_t vw[4][D / 32];   // value rows 2tg, 2tg+1, 2tg+8, 2tg+9; D/8 code bytes each
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int u = 0; u < D / 128; ++u) {
+                        const uint4 v = lds128(st + swz(kBS + 2 * tg + (r & 1) + (r >> 1) * 8, (D / 128) * gq + u));
+                        vw[r][4 * u + 0] = v.x;
+                        vw[r][4 * u + 1] = v.y;
+                        vw[r][4 * u + 2] = v.z;
+                        vw[r][4 * u + 3] = v.w;
+                    }
+#pragma unroll
+                for (int w = 0; w < D / 32; ++w) {
+                    const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], 0x5140);
+                    const uint32_t y01 = __byte_perm(vw[0][w], vw[1][w], 0x7362);
+                    const uint32_t x89 = __byte_perm(vw[2][w], vw[3][w], 0x5140);
+                    const uint32_t y89 = __byte_perm(vw[2][w], vw[3][w], 0x7362);
+                    const uint32_t a0[4] = {e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16),
+                                            e4m3x2_to_f16x2(x89), e4m3x2_to_f16x2(x89 >> 16)};
+                    const uint32_t a1[4] = {e4m3x2_to_f16x2(y01), e4m3x2_to_f16x2(y01 >> 16),
+                                            e4m3x2_to_f16x2(y89), e4m3x2_to_f16x2(y89 >> 16)};
+#pragma unroll
+                    for (int jn = 0; jn < NT; ++jn) {
+                        mma_f16(oacc[2 * w][jn], a0, pb[jn]);
+                        mma_f16(oacc[2 * w + 1][jn], a1, pb[jn]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (j + C::R < nmine) {
+            if (lane == 0) fence_proxy_async_smem();
+            issue(j + C::R, jbase);
+        }
+    }
+
+    if (timed_out) {   // record, then let copies already in flight land before the CTA exits
+        if (lane == 0) {
+            atomicOr(p.err, KVC_EBIT_TIMEOUT);
+            for (int jj = j; jj < min(nmine, j + C::R); ++jj)
+                (void)mbar_wait_bounded(bar_base + 8u * (jj % C::R), static_cast<uint32_t>((jj / C::R) & 1), 100000000ull);
+        }
+        __syncwarp();
+    }
+
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float l = l_run[jn][c];
+            l += __shfl_xor_sync(kFull, l, 4);
+            l += __shfl_xor_sync(kFull, l, 8);
+            l += __shfl_xor_sync(kFull, l, 16);
+            l_run[jn][c] = l;
+        }
+
+    // ---- combine the four warps (shared memory reused), then write
+    __syncthreads();
+    constexpr int QW = NT * 8;
+    float *cm = reinterpret_cast<float *>(smem);
+    float *cl = cm + kWarps * QW;
+    float *co = cl + kWarps * QW;
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+            if (gq == 0) {
+                cm[warp * QW + 8 * jn + 2 * tg + c] = m_run[jn][c];
+                cl[warp * QW + 8 * jn + 2 * tg + c] = l_run[jn][c];
+            }
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int qi = 8 * jn + 2 * tg + (c & 1);
+                const int dim = FP8 ? gq * (D / 8) + 2 * mt + (c >> 1) : 16 * mt + gq + 8 * (c >> 1);
+                co[(warp * QW + qi) * D + dim] = oacc[mt][jn][c];
+            }
+    }
+    __syncthreads();
+
+    const int ns = (nblk + p.chunk - 1) / p.chunk;
+    for (int i = threadIdx.x; i < p.g * D; i += kThreads) {
+        const int qi = i / D, d = i - qi * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * QW + qi]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float e = fast_exp2(cm[w * QW + qi] - M);   // warps without blocks: exp2(-inf) = 0
+            L += e * cl[w * QW + qi];
+            O += e * co[(w * QW + qi) * D + d];
+        }
+        if constexpr (FP8) O *= __ldg(p.s_v + static_cast<size_t>(h) * D + d);
+        const size_t bq = static_cast<size_t>(b) * p.H_Q + hq0 + qi;
+        if (ns == 1) {
+            p.out[bq * D + d] = O / L;
+            if (d == 0 && p.lse) p.lse[bq] = (M + log2f(L)) * kLn2;
+        } else {
+            const size_t pi = bq * p.max_splits + split;
+            p.part_o[pi * D + d] = O;
+            if (d == 0) p.part_ml[pi] = make_float2(M, L);
+        }
+    }
+}
+
+// Fetch (and on first use configure) the kernel instance for a shape.
+struct DecodeKernel {
+    const void *fn;
+    int smem;
+    int ctas_per_sm;
+};
+
+template <int D, int NT, bool FP8, bool PSPLIT>
+DecodeKernel decode_instance()
+{
+    static DecodeKernel k = [] {
+        DecodeKernel r;
+        r.fn = reinterpret_cast<const void *>(&decode_kernel<D, NT, FP8, PSPLIT>);
+        r.smem = decode_smem_bytes<D, NT, FP8>();
+        r.ctas_per_sm = 0;
+        if (cudaFuncSetAttribute(&decode_kernel<D, NT, FP8, PSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 r.smem) == cudaSuccess) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_kernel<D, NT, FP8, PSPLIT>, kThreads,
+                                                              r.smem) == cudaSuccess)
+                r.ctas_per_sm = n;
+        }
+        return r;
+    }();
+    return k;
+}
+
+kvc_status run_decode(const kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream);
+
+}  // namespace kvc

@@ -1,0 +1,34 @@
+// bf16-pool instances of the decode-attention kernel.
+#include <cstdlib>
+
+#include "kvc_decode.cuh"
+
+namespace kvc {
+
+template <int D>
+static DecodeKernel pick_bf16(int NT, bool psplit)
+{
+    if (NT == 1) return psplit ? decode_instance<D, 1, false, true>() : decode_instance<D, 1, false, false>();
+    if (NT == 2) return psplit ? decode_instance<D, 2, false, true>() : decode_instance<D, 2, false, false>();
+    return psplit ? decode_instance<D, 4, false, true>() : decode_instance<D, 4, false, false>();
+}
+
+kvc_status launch_decode_bf16(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream)
+{
+    // KVC_PSPLIT=0 feeds the softmax weights to the value mixture as one bf16
+    // operand instead of a high/low pair (faster, ~8 fewer bits per weight).
+    static const bool psplit = [] {
+        const char *e = std::getenv("KVC_PSPLIT");
+        return !(e && e[0] == '0');
+    }();
+    const int NT = p.g <= 8 ? 1 : (p.g <= 16 ? 2 : 4);
+    DecodeKernel k;
+    switch (pool->D) {
+    case 64: k = pick_bf16<64>(NT, psplit); break;
+    case 128: k = pick_bf16<128>(NT, psplit); break;
+    default: return KVC_ERR_UNSUPPORTED;
+    }
+    return run_decode(pool, p, k, stream);
+}
+
+}  // namespace kvc

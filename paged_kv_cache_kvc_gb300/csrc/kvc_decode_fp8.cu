@@ -1,0 +1,16 @@
+// e4m3-pool instances of the decode-attention kernel.
+#include "kvc_decode.cuh"
+
+namespace kvc {
+
+kvc_status launch_decode_fp8(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream)
+{
+    const int NT = p.g <= 8 ? 1 : (p.g <= 16 ? 2 : 4);
+    if (pool->D != 128) return KVC_ERR_UNSUPPORTED;
+    DecodeKernel k = NT == 1 ? decode_instance<128, 1, true, false>()
+                   : NT == 2 ? decode_instance<128, 2, true, false>()
+                             : decode_instance<128, 4, true, false>();
+    return run_decode(pool, p, k, stream);
+}
+
+}  // namespace kvc

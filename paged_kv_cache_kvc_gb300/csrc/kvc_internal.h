@@ -1,0 +1,67 @@
+// Internal declarations shared by the libkvc translation units.
+#pragma once
+#include <atomic>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/kvc.h"
+
+// Device-detected error bits (pool error word).
+#define KVC_EBIT_BAD_BLOCK 1u
+#define KVC_EBIT_RANGE 2u
+#define KVC_EBIT_TIMEOUT 4u
+
+struct kvc_pool {
+    int64_t N;            // physical blocks
+    int32_t bs, L, H_KV, D, dtype, s, device;
+    uint8_t *base;        // pool bytes
+    size_t layer_bytes, pool_bytes;
+    float *scales;        // [L][2][H_KV][D] (e4m3 pools)
+    float *absmax;        // [L][2][H_KV][D] running absmax for kvc_calibrate_fp8
+    uint32_t *err;        // device error word
+    CUtensorMap tmap;     // rows of D elements; box {128 B, 2*bs rows}; 128-byte swizzle
+    bool tmap_ok;
+    void *ws;             // split-K partials
+    size_t ws_bytes;
+    int num_sms;
+};
+
+namespace kvc {
+
+extern std::atomic<uint64_t> g_launches;
+
+// Decode / prefill attention launch parameters (one layer).
+struct DecodeParams {
+    const uint16_t *q;       // bf16 [B][H_Q][D]
+    const int32_t *bt;       // block table rows
+    const int32_t *lens;     // [B] positions attended, or nullptr: len(b) = len_base + b + 1
+    int64_t bt_stride;       // elements between table rows (0: every row is the same row)
+    int32_t max_blocks;
+    int32_t len_base;
+    int32_t B, H_Q, H_KV, g;
+    int32_t layer;
+    int32_t chunk;           // logical blocks per split (multiple of 4)
+    int32_t max_splits;
+    int64_t N;
+    float scale_log2;        // softmax scale * log2(e)
+    const float *s_k;        // this layer's e4m3 scales [H_KV][D] (keys), else nullptr
+    const float *s_v;        // (values)
+    float *out;              // fp32 [B][H_Q][D]
+    float *lse;              // fp32 [B][H_Q] or nullptr
+    float *part_o;           // [B][H_Q][max_splits][D]
+    float2 *part_ml;         // [B][H_Q][max_splits]  (running max in log2 units, sum)
+    uint32_t *err;
+};
+
+kvc_status cuda_status(cudaError_t e);
+kvc_status check_device(const kvc_pool *pool);
+
+// Launchers implemented per element type.
+kvc_status launch_decode_bf16(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream);
+kvc_status launch_decode_fp8(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream);
+
+// Split-K sizing: blocks per split and the split count for a batch.
+void choose_split(const kvc_pool *pool, int B, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits);
+
+}  // namespace kvc

@@ -1,0 +1,401 @@
+"""CUDA path vs the oracle, element by element, through the C ABI.
+
+Append and token writes: bit-exact on every byte of the pool (untouched bytes
+keep their fill).  Attention: max |out - ref| <= 1e-2 (bf16 KV) / 3e-2 (e4m3
+KV) and |lse - ref| <= 2e-3 * max(1, |ref|).  Invariants that the GPU's
+arithmetic order cannot change (block permutation, poisoned padding) are
+checked bit for bit.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from harness import (GpuCase, OracleCase, check_attention, dev_bits, dev_i32, first_mismatch, layer_data,
+                     logical_lists)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(kvc, w, layers=(0,), fill=0xFF, bytes_check=True, decode_layers=None):
+    """Load context, append, decode on the GPU and in the oracle; compare."""
+    g = GpuCase(kvc, w, fill_byte=fill)
+    orc = OracleCase(w, fill_byte=fill)
+    errs = []
+    try:
+        for layer in layers:
+            ld = layer_data(w, layer)
+            g.load_context(layer, ld)
+            out, lse = g.step(layer, ld)
+            torch.cuda.synchronize()
+            assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+            dec = decode_layers is None or layer in decode_layers
+            ref = orc.run_layer(ld, decode=dec, image=bytes_check)
+            if w.dtype == "fp8":
+                got_sc = g.pool.scales_view()[layer].cpu().numpy()
+                assert np.array_equal(got_sc.view(np.uint32), ref["scales"].view(np.uint32)), "scales differ"
+            if bytes_check:
+                n, first = first_mismatch(g.layer_bytes(layer), ref["image"].bytes)
+                assert n == 0, f"layer {layer}: {n} pool bytes differ, first at {first}"
+            if dec:
+                errs.append(check_attention(out, lse, ref["out"], ref["lse"], w.dtype, f"{w.name} layer {layer}"))
+    finally:
+        g.close()
+    return errs
+
+
+# ------------------------------------------------------------------ the workloads
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny(kvc, seed):
+    _run(kvc, synth.make_workload("tiny", seed=seed))
+
+
+def test_llama_gqa(kvc):
+    _run(kvc, synth.make_workload("llama_gqa", seed=0))
+
+
+@pytest.mark.parametrize("name", ["sweep_hkv8_bf16", "sweep_hkv8_fp8", "sweep_hkv32_bf16", "sweep_hkv32_fp8",
+                                  "sweep_hkv1_bf16", "sweep_hkv1_fp8"])
+def test_sweep(kvc, name):
+    _run(kvc, synth.make_workload(name, seed=0))
+
+
+def test_full_pool_every_layer(kvc):
+    """32 layers sharing one table: bytes of every layer bit-exact; attention of
+    four layers (first, last and two inside) against the oracle."""
+    w = synth.make_workload("full_pool", seed=0)
+    _run(kvc, w, layers=range(w.L), decode_layers={0, 7, 20, 31})
+
+
+def test_ragged_prefix_and_prefill_chunk(kvc):
+    w = synth.make_workload("ragged_prefix", seed=0)
+    g = GpuCase(kvc, w)
+    orc = OracleCase(w)
+    try:
+        ld = layer_data(w, 0)
+        g.load_context(0, ld)
+        out, lse = g.step(0, ld)
+        ref = orc.run_layer(ld)
+        check_attention(out, lse, ref["out"], ref["lse"], "bf16", "ragged decode")
+        # the 600-token chunk of row 64: written after the shared 1200-token prefix, then causal attention
+        p = w.prefill
+        kc = w.ctx_tokens(0, 0, p.seq, p.q_start, p.total)
+        vc = w.ctx_tokens(0, 1, p.seq, p.q_start, p.total)
+        row = dev_i32(w.block_tables[p.seq:p.seq + 1])
+        kvc.kvc_write_tokens(g.pool, 0, row, dev_i32([p.q_start]), dev_i32([0, p.n_q]), dev_bits(kc), dev_bits(vc))
+        qc = w.prefill_q(0)
+        o2 = torch.empty((p.n_q, w.H_Q, w.d_h), dtype=torch.float32, device="cuda")
+        l2 = torch.empty((p.n_q, w.H_Q), dtype=torch.float32, device="cuda")
+        kvc.kvc_prefill_attn(g.pool, 0, dev_bits(qc), row[0], p.q_start, o2, l2, scale=w.scale)
+        torch.cuda.synchronize()
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+        shared_k, shared_v = ld.k_ctx[:w.shared_prefix], ld.v_ctx[:w.shared_prefix]
+        K = np.concatenate([shared_k, kc])
+        V = np.concatenate([shared_v, vc])
+        ro, rl = oracle.prefill(qc, K, V, p.q_start, w.H_KV, scale=w.scale)
+        check_attention(o2, l2, ro, rl, "bf16", "prefill chunk")
+        # pool bytes, prefill chunk included
+        ref["image"].write_tokens(0, w.block_tables[p.seq:p.seq + 1], np.array([p.q_start], np.int32),
+                                  np.array([0, p.n_q], np.int64), kc, vc)
+        n, first = first_mismatch(g.layer_bytes(0), ref["image"].bytes)
+        assert n == 0, f"{n} pool bytes differ, first at {first}"
+    finally:
+        g.close()
+
+
+def test_prefix_sharing_equals_private_copies(kvc):
+    """The shared-block run equals a run where every row holds a private copy
+    of the prefix blocks: bit-identical outputs (same arithmetic order)."""
+    w = synth.make_workload("ragged_prefix", seed=1)
+    g = GpuCase(kvc, w)
+    try:
+        ld = layer_data(w, 0)
+        g.load_context(0, ld)
+        out_a, lse_a = [t.clone() for t in g.step(0, ld)]
+    finally:
+        g.close()
+    # private copies: remap each row's prefix blocks to fresh ids appended to the pool
+    sb = w.shared_prefix // w.bs
+    bt = w.block_tables.copy()
+    N0 = w.num_blocks
+    for r in range(w.B):
+        bt[r, :sb] = N0 + r * sb + np.arange(sb, dtype=np.int32)
+    w2 = synth.workloads.Workload(w.name, w.seed, w.B, w.H_Q, w.H_KV, w.d_h, w.bs, w.L, w.dtype,
+                                  N0 + w.B * sb, w.lens_pre, bt[:w.B])
+    ld2 = layer_data(w2, 0)
+    # same values: the rows' prefixes come from the shared stream in w; copy them in as private context
+    ks, vs, cu = [], [], [0]
+    for b in range(w.B):
+        a, e = int(ld.cu[1 + b]), int(ld.cu[2 + b])
+        ks += [ld.k_ctx[:w.shared_prefix], ld.k_ctx[a:e]]
+        vs += [ld.v_ctx[:w.shared_prefix], ld.v_ctx[a:e]]
+        cu.append(cu[-1] + w.shared_prefix + e - a)
+    ld2.k_ctx, ld2.v_ctx = np.concatenate(ks), np.concatenate(vs)
+    ld2.cu, ld2.start, ld2.rows = np.array(cu, np.int32), np.zeros(w.B, np.int32), np.arange(w.B, dtype=np.int32)
+    ld2.q, ld2.k_new, ld2.v_new = ld.q, ld.k_new, ld.v_new
+    g2 = GpuCase(kvc, w2)
+    try:
+        g2.load_context(0, ld2)
+        out_b, lse_b = g2.step(0, ld2)
+        assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
+    finally:
+        g2.close()
+
+
+# ------------------------------------------------------------------ edge cases
+def _custom(**kw):
+    return synth.make_workload("custom", **kw)
+
+
+@pytest.mark.parametrize("d_h", [64, 128])
+def test_short_and_boundary_lengths(kvc, d_h):
+    """First token (empty context), lengths on and around block boundaries, a
+    ragged tail in the last block, over several split sizes."""
+    lens = [0, 1, 14, 15, 16, 17, 31, 32, 33, 47, 64, 100, 255, 511]
+    w = _custom(B=len(lens), H_Q=8, H_KV=2, d_h=d_h, lens=lens, spare_blocks=5, extra_cols=3)
+    for chunk in (None, "4", "8", "16"):
+        if chunk:
+            os.environ["KVC_SPLIT_CHUNK"] = chunk
+        try:
+            _run(kvc, w)
+        finally:
+            os.environ.pop("KVC_SPLIT_CHUNK", None)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("H_KV", [32, 16, 8, 4, 2, 1])
+def test_group_sizes(kvc, H_KV, dtype):
+    """GQA group sizes 1 (MHA) .. 32 (MQA) with ragged lengths."""
+    lens = [3, 77, 300, 1029]
+    _run(kvc, _custom(B=len(lens), H_Q=32, H_KV=H_KV, d_h=128, lens=lens, dtype=dtype, seed=H_KV))
+
+
+def test_split_counts_agree(kvc):
+    """Changing the split size changes only rounding: all within tolerance of the oracle."""
+    w = _custom(B=3, H_Q=16, H_KV=4, d_h=128, lens=[2000, 4097, 777])
+    for chunk in ("4", "12", "64", "1024"):
+        os.environ["KVC_SPLIT_CHUNK"] = chunk
+        try:
+            _run(kvc, w, bytes_check=False)
+        finally:
+            os.environ.pop("KVC_SPLIT_CHUNK", None)
+
+
+def test_block_permutation_bit_identical(kvc):
+    """Same logical sequences, physical blocks permuted and tables rewritten:
+    bit-identical outputs (logical order is what attention sees)."""
+    w = _custom(B=4, H_Q=32, H_KV=8, d_h=128, lens=[700, 1300, 64, 2049], spare_blocks=11)
+    res = []
+    for perm_seed in (0, 1):
+        remap = synth.permutation(perm_seed, 77, w.num_blocks)
+        bt = np.where(w.block_tables >= 0, remap[np.maximum(w.block_tables, 0)], -1).astype(np.int32)
+        w2 = synth.workloads.Workload(w.name, w.seed, w.B, w.H_Q, w.H_KV, w.d_h, w.bs, w.L, w.dtype,
+                                      w.num_blocks, w.lens_pre, bt)
+        g = GpuCase(kvc, w2)
+        try:
+            ld = layer_data(w2, 0)
+            g.load_context(0, ld)
+            res.append([t.clone() for t in g.step(0, ld)])
+        finally:
+            g.close()
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_padding_poison_bit_identical(kvc, dtype):
+    """Pool pre-filled with NaN/Inf patterns vs zeros: unused slots and blocks
+    never change the output ("KV cache: ..." 21.1: padded slots are excluded)."""
+    w = _custom(B=5, H_Q=32, H_KV=8, d_h=128, lens=[1, 17, 250, 1000, 33], spare_blocks=9, dtype=dtype)
+    res = []
+    for fill in (0x00, 0xFF, 0x7F):
+        g = GpuCase(kvc, w, fill_byte=fill)
+        try:
+            ld = layer_data(w, 0)
+            g.load_context(0, ld)
+            res.append([t.clone() for t in g.step(0, ld)])
+        finally:
+            g.close()
+    for r in res[1:]:
+        assert torch.equal(res[0][0], r[0]) and torch.equal(res[0][1], r[1])
+
+
+def test_head_duplication_agrees(kvc):
+    """MQA data duplicated into 8 and 32 KV heads gives the same attention (within tolerance)."""
+    lens = [130, 900]
+    w1 = _custom(B=2, H_Q=32, H_KV=1, d_h=128, lens=lens)
+    ld1 = layer_data(w1, 0)
+    outs = []
+    for H_KV in (1, 8, 32):
+        w = _custom(B=2, H_Q=32, H_KV=H_KV, d_h=128, lens=lens)
+        ld = layer_data(w, 0)
+        ld.k_ctx, ld.v_ctx = np.repeat(ld1.k_ctx, H_KV, 1), np.repeat(ld1.v_ctx, H_KV, 1)
+        ld.k_new, ld.v_new, ld.q = np.repeat(ld1.k_new, H_KV, 1), np.repeat(ld1.v_new, H_KV, 1), ld1.q
+        g = GpuCase(kvc, w)
+        try:
+            g.load_context(0, ld)
+            outs.append([t.cpu().numpy() for t in g.step(0, ld)])
+        finally:
+            g.close()
+    ref = OracleCase(w1).run_layer(ld1, image=False)
+    for o, l in outs:
+        check_attention(o, l, ref["out"], ref["lse"], "bf16", "duplicated heads")
+
+
+def test_empty_batch_and_empty_sequence(kvc):
+    w = _custom(B=2, H_Q=8, H_KV=2, d_h=128, lens=[5, 9])
+    g = GpuCase(kvc, w)
+    try:
+        q = torch.zeros((0, 8, 128), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty((0, 8, 128), dtype=torch.float32, device="cuda")
+        kvc.kvc_decode_attn(g.pool, 0, q, g.bt_dec[:0], g.lens_post[:0], out)   # B = 0: no-op
+        ld = layer_data(w, 0)
+        g.load_context(0, ld)
+        q, _, _ = g.step_inputs(ld)
+        out = torch.full((2, 8, 128), 7.0, device="cuda")
+        lse = torch.full((2, 8), 7.0, device="cuda")
+        kvc.kvc_decode_attn(g.pool, 0, q, g.bt_dec, dev_i32([0, 3]), out, lse, scale=w.scale)
+        torch.cuda.synchronize()
+        assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+        assert torch.all(torch.isfinite(out[1])) and torch.all(torch.isfinite(lse[1]))
+    finally:
+        g.close()
+
+
+def test_device_detected_errors_do_not_fault(kvc):
+    """A table entry outside the pool or a length past the table row is
+    skipped and reported by kvc_pool_sync_status; the pool stays usable."""
+    w = _custom(B=2, H_Q=8, H_KV=2, d_h=128, lens=[40, 20], spare_blocks=2)
+    g = GpuCase(kvc, w, fill_byte=0)
+    try:
+        ld = layer_data(w, 0)
+        g.load_context(0, ld)
+        before = g.layer_bytes(0)
+        bad = w.block_tables.copy()
+        bad[0, 40 // 16] = w.num_blocks + 5          # the block the append of row 0 lands in
+        q, k, v = g.step_inputs(ld)
+        kvc.kvc_append(g.pool, 0, dev_i32(bad), g.lens_pre, k, v)
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_ERR_BAD_BLOCK
+        after = g.layer_bytes(0)
+        # row 1's append landed, row 0's was skipped
+        img = oracle.PoolImage(w.num_blocks, w.bs, 1, w.H_KV, w.d_h, 2)
+        img.bytes[:] = before
+        img.append(0, bad, w.lens_pre, ld.k_new, ld.v_new)
+        assert np.array_equal(after, img.bytes)
+        out = torch.empty((2, 8, 128), device="cuda")
+        kvc.kvc_decode_attn(g.pool, 0, q, dev_i32(bad), g.lens_post, out, scale=w.scale)
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_ERR_BAD_BLOCK
+        too_long = dev_i32([w.max_blocks * 16 + 1, 3])
+        kvc.kvc_decode_attn(g.pool, 0, q, g.bt_dec, too_long, out, scale=w.scale)
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_ERR_RANGE
+        assert torch.all(out[0] == 0)
+        kvc.kvc_decode_attn(g.pool, 0, q, g.bt_dec, g.lens_post, out, scale=w.scale)
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+    finally:
+        g.close()
+
+
+def test_host_argument_errors(kvc):
+    w = _custom(B=1, H_Q=8, H_KV=2, d_h=128, lens=[5])
+    g = GpuCase(kvc, w)
+    try:
+        q = torch.zeros((1, 6, 128), dtype=torch.bfloat16, device="cuda")     # 6 % 4 KV heads... H_Q % H_KV != 0
+        q7 = torch.zeros((1, 7, 128), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty((1, 7, 128), device="cuda")
+        with pytest.raises(kvc.KvcError) as e:
+            kvc.kvc_decode_attn(g.pool, 0, q7, g.bt_dec, g.lens_post, out)
+        assert e.value.status == kvc.KVC_ERR_ARG
+        with pytest.raises(kvc.KvcError) as e:
+            kvc.kvc_decode_attn(g.pool, 1, q, g.bt_dec, g.lens_post, out)      # layer out of range
+        assert e.value.status == kvc.KVC_ERR_ARG
+        with pytest.raises(kvc.KvcError) as e:
+            kvc.kvc_prefill_attn(g.pool, 0, q, g.bt_dec[0], w.max_blocks * 16, out)
+        assert e.value.status == kvc.KVC_ERR_RANGE
+    finally:
+        g.close()
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_pool_create(10, 16, 1, 2, 96, kvc.KVC_BF16)                     # head_dim 96 unsupported
+
+
+def test_table_21_1_through_the_abi(kvc):
+    """Table 21.1 replayed on a real pool with 4-position blocks: A=[7,2] holds 6
+    tokens, B=[9] holds 4; A's positions 6, 7 land in block 2 slots 2, 3 and,
+    once block 5 is mapped, position 8 in block 5 slot 0; B is untouched."""
+    N, bs, H, d = 10, 4, 1, 64
+    pool = kvc.kvc_pool_create(N, bs, 1, H, d, kvc.KVC_BF16)
+    try:
+        pool.bytes_view().fill_(0)
+        img = oracle.PoolImage(N, bs, 1, H, d, 2, fill=0)
+        bt = np.array([[7, 2, -1], [9, -1, -1]], dtype=np.int32)
+        ctx = synth.normal_bf16(5, 1, 10 * H * d).reshape(10, H, d)
+        cu = np.array([0, 6, 10], np.int32)
+        kvc.kvc_write_tokens(pool, 0, dev_i32(bt), dev_i32([0, 0]), dev_i32(cu), dev_bits(ctx), dev_bits(ctx))
+        img.write_tokens(0, bt, np.array([0, 0], np.int32), cu.astype(np.int64), ctx, ctx)
+        for pos, extend in ((6, None), (7, None), (8, 5)):
+            if extend is not None:
+                bt[0, 2] = extend
+            k = synth.normal_bf16(6, pos, H * d).reshape(1, H, d)
+            kvc.kvc_append(pool, 0, dev_i32(bt[:1]), dev_i32([pos]), dev_bits(k), dev_bits(k))
+            img.append(0, bt[:1], np.array([pos], np.int32), k, k)
+            torch.cuda.synchronize()
+            assert kvc.kvc_pool_sync_status(pool) == kvc.KVC_OK
+            assert np.array_equal(pool.bytes_view().cpu().numpy(), img.bytes)
+        # where the three appends landed (Table 21.1 steps 1-2)
+        got = pool.bytes_view().cpu().numpy()
+        for pos, (phys, slot) in ((6, (2, 2)), (7, (2, 3)), (8, (5, 0))):
+            k = synth.normal_bf16(6, pos, H * d)
+            off = img.offset(0, phys, 0, 0, slot, 0) * 2
+            assert np.array_equal(got[off:off + 2 * d].view(np.uint16), k)
+    finally:
+        pool.close()
+
+
+@pytest.mark.parametrize("scale", [1.0, 1.0 / 448, 0.0123, 2.0 ** -10])
+def test_e4m3_append_matches_codec_for_every_bf16(kvc, scale):
+    """Every bf16 bit pattern appended through an e4m3 pool: the stored code is
+    the oracle's RNE-saturating encoding of fp32(x) / scale (NaN inputs: NaN codes)."""
+    H, d = 1, 128
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    n_tok = 65536 // (H * d)
+    N = n_tok // 16
+    pool = kvc.kvc_pool_create(N, 16, 1, H, d, kvc.KVC_FP8_E4M3)
+    try:
+        s = torch.full((H, d), scale, dtype=torch.float32, device="cuda")
+        kvc.kvc_pool_set_scales(pool, 0, s, s)
+        x = bits.reshape(n_tok, H, d)
+        bt = np.arange(N, dtype=np.int32).reshape(1, N)
+        kvc.kvc_write_tokens(pool, 0, dev_i32(bt), dev_i32([0]), dev_i32([0, n_tok]), dev_bits(x), dev_bits(x))
+        torch.cuda.synchronize()
+        img = oracle.PoolImage(N, 16, 1, H, d, 1)
+        img.scales[0] = np.float32(scale)
+        img.write_tokens(0, bt, np.array([0], np.int32), np.array([0, n_tok], np.int64), x, x)
+        got = pool.bytes_view().cpu().numpy()
+        xf = synth.bf16_bits_to_f32(bits)
+        st, kg, _ = img.gather(0, bt[0], n_tok)
+        # locate each input's stored code in both images
+        pos_codes_gpu = np.empty(65536, np.uint8)
+        gimg = oracle.PoolImage(N, 16, 1, H, d, 1)
+        gimg.bytes[:] = got
+        _, kgg, _ = gimg.gather(0, bt[0], n_tok)
+        pos_codes_gpu[:] = kgg.reshape(-1)
+        ref = kg.reshape(-1)
+        nan_in = np.isnan(xf)
+        assert np.array_equal(pos_codes_gpu[~nan_in], ref[~nan_in])
+        assert np.all((pos_codes_gpu[nan_in] & 0x7F) == 0x7F)
+    finally:
+        pool.close()
+
+
+def test_launches_are_counted(kvc):
+    w = synth.make_workload("tiny", seed=0)
+    g = GpuCase(kvc, w)
+    try:
+        ld = layer_data(w, 0)
+        g.load_context(0, ld)
+        n0 = kvc.kvc_launch_count()
+        g.step(0, ld)
+        assert kvc.kvc_launch_count() - n0 >= 2
+    finally:
+        g.close()
