@@ -182,10 +182,13 @@ def oracle_sample(w, ld, budget_s: float, units_max=None):
     k = max(1, min(len(units), int(budget_s / max(t1, 1e-6))))
     if units_max:
         k = min(k, units_max)
-    nbytes, dt = run(units[:k])
+    nbytes, dt, passes = 0, 0.0, 0
+    while passes == 0 or (units_max is None and dt < budget_s and passes < 1000):
+        b_, t_ = run(units[:k])        # whole passes over the sample until the budget is spent
+        nbytes, dt, passes = nbytes + b_, dt + t_, passes + 1
     threads = min(oracle.num_threads(), k * g)
-    desc = (f"{k} of {len(units)} (sequence, KV head) units of {w.name} (each {int(w.lens_post[0])} positions, "
-            f"{g} query heads): oracle append + fp64 decode")
+    desc = (f"{passes} pass(es) over {k} of {len(units)} (sequence, KV head) units of {w.name} "
+            f"(each {int(w.lens_post[0])} positions, {g} query heads): oracle append + fp64 decode")
     return nbytes / dt, dt, k, desc, threads
 
 
