@@ -215,6 +215,31 @@ KVC_API kvc_status kvc_prefill_attn(kvc_pool *pool, int32_t layer, const void *q
  * allocate nothing.  Errors: KVC_ERR_ARG, KVC_ERR_OOM. */
 KVC_API kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_t num_q_heads, int32_t max_blocks);
 
+/* Decode attention that allocates no device memory.  The pages have no
+ * counterpart to this call; it exists for callers that must not allocate in
+ * the middle of a decode step: engines whose device memory is fully
+ * pre-reserved by their own caching allocator (a cudaMalloc would fail or
+ * fragment memory promised to KV blocks), and latency-critical loops where
+ * cudaMalloc / cudaFree would synchronise the device and stall other streams.
+ * Same arguments, arithmetic and results as kvc_decode_attn, but the split
+ * partials live in a fixed 8 MiB device array inside the library (held by
+ * every GPU that loads the library until the process exits) instead of the
+ * pool's workspace, so no cudaMalloc, cudaFree or allocating routine runs.
+ * Limit: when the batch is split, B * H_Q * splits * (d_h + 2) floats must fit
+ * in 8 MiB (2^21 floats), where splits is the split count kvc_decode_attn
+ * would choose; a larger request returns KVC_ERR_ARG before any launch.
+ * The first call on a device looks up the array's device address (a
+ * cudaGetSymbolAddress with that device current); make that first call before
+ * any stream capture.  Every call on a device shares the one array, and it
+ * keeps the last call's contents (nothing in it needs to start at zero:
+ * every partial read is written by the same call first), so calls that
+ * overlap on the GPU (other streams, other threads, other pools of the same
+ * device) race and must be serialised by the caller. */
+KVC_API kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
+                                           const int32_t *block_tables, int32_t max_blocks,
+                                           const int32_t *seq_lens, int32_t B, float *out, float *lse,
+                                           float scale, kvc_stream_t stream);
+
 /* ------------------------------------------------------------------ host utilities */
 
 /* Ideal KV payload in bytes

@@ -44,7 +44,7 @@ class kvc_pool_desc(ctypes.Structure):
 
 EXPORTS = ["kvc_pool_create", "kvc_pool_destroy", "kvc_pool_info", "kvc_pool_set_scales", "kvc_calibrate_fp8",
            "kvc_append", "kvc_write_tokens", "kvc_decode_attn", "kvc_prefill_attn", "kvc_pool_reserve",
-           "kvc_bytes", "kvc_pool_sync_status", "kvc_status_str", "kvc_launch_count"]
+           "kvc_bytes", "kvc_pool_sync_status", "kvc_status_str", "kvc_launch_count", "kvc_decode_attn_noalloc"]
 
 
 def load(path: str = LIB_PATH):
@@ -66,6 +66,8 @@ def load(path: str = LIB_PATH):
     L.kvc_write_tokens.restype, L.kvc_write_tokens.argtypes = st, [vp, i32, vp, i32, vp, vp, i32, i32, vp, vp, vp]
     L.kvc_decode_attn.restype = st
     L.kvc_decode_attn.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, vp, vp, ctypes.c_float, vp]
+    L.kvc_decode_attn_noalloc.restype = st
+    L.kvc_decode_attn_noalloc.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, vp, vp, ctypes.c_float, vp]
     L.kvc_prefill_attn.restype = st
     L.kvc_prefill_attn.argtypes = [vp, i32, vp, i32, i32, vp, i32, i32, vp, vp, ctypes.c_float, vp]
     L.kvc_pool_reserve.restype, L.kvc_pool_reserve.argtypes = st, [vp, i32, i32, i32]
@@ -211,6 +213,24 @@ def kvc_decode_attn(pool, layer, q, block_tables, seq_lens, out, lse=None, scale
                                   _dev(seq_lens, torch.int32, "seq_lens"), B, _dev(out, torch.float32, "out"),
                                   _dev(lse, torch.float32, "lse", optional=True), float(scale), _stream(stream)),
            "kvc_decode_attn")
+
+
+def kvc_decode_attn_noalloc(pool, layer, q, block_tables, seq_lens, out, lse=None, scale=None, stream=None):
+    """kvc_decode_attn without any device allocation: split partials go to the
+    library's fixed 8 MiB per-device array.  For callers that may not allocate
+    during a decode step (memory pre-reserved by their own allocator, or loops
+    that cannot afford cudaMalloc's device synchronisation).  Calls that overlap
+    on one GPU share the array and race; the first call on a device looks up the
+    array's address and should precede any stream capture."""
+    B, H_Q, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    _check(load().kvc_decode_attn_noalloc(_h(pool), layer, _dev(q, torch.bfloat16, "q"), H_Q,
+                                          _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+                                          _dev(seq_lens, torch.int32, "seq_lens"), B, _dev(out, torch.float32, "out"),
+                                          _dev(lse, torch.float32, "lse", optional=True), float(scale),
+                                          _stream(stream)),
+           "kvc_decode_attn_noalloc (a split batch needing more than the 8 MiB scratch is rejected)")
 
 
 def kvc_prefill_attn(pool, layer, q, block_table_row, q_start, out, lse=None, scale=None, stream=None):

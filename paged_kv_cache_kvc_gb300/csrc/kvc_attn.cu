@@ -200,3 +200,17 @@ extern "C" kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_
     const int max_splits = (max_blocks + 15) / 16;
     return ensure_workspace(pool, workspace_bytes(max_batch, num_q_heads, max_splits, pool->D));
 }
+
+namespace kvc {
+
+// Launch the split merge on its own (partials already written by the decode kernel).
+kvc_status launch_split_merge(const DecodeParams &p, int D, cudaStream_t stream)
+{
+    merge_kernel<<<dim3(p.H_Q, p.B), 128, 0, stream>>>(p, D);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return KVC_OK;
+}
+
+}  // namespace kvc

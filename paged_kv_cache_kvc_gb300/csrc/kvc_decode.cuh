@@ -436,4 +436,9 @@ DecodeKernel decode_instance()
 
 kvc_status run_decode(const kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream);
 
+// Kernel instance selection without launching (used by the allocation-free entry point).
+DecodeKernel select_decode_bf16(int D, int g);
+DecodeKernel select_decode_fp8(int D, int g);
+kvc_status launch_split_merge(const DecodeParams &p, int D, cudaStream_t stream);
+
 }  // namespace kvc

@@ -32,3 +32,18 @@ kvc_status launch_decode_bf16(const kvc_pool *pool, DecodeParams &p, cudaStream_
 }
 
 }  // namespace kvc
+
+namespace kvc {
+
+// The bf16 kernel instance kvc_decode_attn would launch for head width D and group size g.
+DecodeKernel select_decode_bf16(int D, int g)
+{
+    const char *e = std::getenv("KVC_PSPLIT");
+    const bool psplit = !(e && e[0] == '0');
+    const int NT = g <= 8 ? 1 : (g <= 16 ? 2 : 4);
+    if (D == 64) return pick_bf16<64>(NT, psplit);
+    if (D == 128) return pick_bf16<128>(NT, psplit);
+    return DecodeKernel{nullptr, 0, 0};
+}
+
+}  // namespace kvc

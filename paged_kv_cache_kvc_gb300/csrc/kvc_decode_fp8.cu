@@ -14,3 +14,17 @@ kvc_status launch_decode_fp8(const kvc_pool *pool, DecodeParams &p, cudaStream_t
 }
 
 }  // namespace kvc
+
+namespace kvc {
+
+// The e4m3 kernel instance kvc_decode_attn would launch for head width D and group size g.
+DecodeKernel select_decode_fp8(int D, int g)
+{
+    const int NT = g <= 8 ? 1 : (g <= 16 ? 2 : 4);
+    if (D != 128) return DecodeKernel{nullptr, 0, 0};
+    return NT == 1 ? decode_instance<128, 1, true, false>()
+         : NT == 2 ? decode_instance<128, 2, true, false>()
+                   : decode_instance<128, 4, true, false>();
+}
+
+}  // namespace kvc

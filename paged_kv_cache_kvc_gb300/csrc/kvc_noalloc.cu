@@ -1,0 +1,109 @@
+// Decode attention that allocates nothing: the split-K partials live in a
+// fixed, file-scope device array instead of the pool's cudaMalloc'd workspace.
+//
+// Some callers may not allocate device memory in the middle of a decode step:
+// a serving loop whose device memory is entirely pre-reserved by its own
+// caching allocator (a cudaMalloc there fails, or fragments memory the engine
+// has promised to KV blocks), and latency-critical loops where cudaMalloc /
+// cudaFree would synchronise the device and stall every other stream.  For
+// them, kvc_decode_attn_noalloc runs the same kernels as kvc_decode_attn with
+// partials in kvc_noalloc_scratch.
+#include <cmath>
+#include <mutex>
+
+#include "kvc_decode.cuh"
+
+namespace kvc {
+
+// 8 MiB per device, held by every GPU that loads the library until the process exits.
+constexpr size_t kNoallocScratchFloats = size_t(2) << 20;
+static __device__ __align__(256) float kvc_noalloc_scratch[kNoallocScratchFloats];
+
+// Device address of the scratch array, looked up once per device with that
+// device current.  (In host code the array's name is only a host-side stand-in.)
+static float *noalloc_scratch_ptr(int device)
+{
+    constexpr int kMaxDevices = 128;
+    static std::mutex mu;
+    static float *ptrs[kMaxDevices] = {};
+    if (device < 0 || device >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[device]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, kvc_noalloc_scratch) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        ptrs[device] = static_cast<float *>(p);
+    }
+    return ptrs[device];
+}
+
+static bool is_aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+}  // namespace kvc
+
+using namespace kvc;
+
+extern "C" kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
+                                              const int32_t *block_tables, int32_t max_blocks,
+                                              const int32_t *seq_lens, int32_t B, float *out, float *lse,
+                                              float scale, kvc_stream_t stream)
+{
+    if (B < 0 || B > 65535) return KVC_ERR_ARG;
+    if (B == 0) return pool ? KVC_OK : KVC_ERR_ARG;
+    if (!pool || !q || !block_tables || !seq_lens || !out) return KVC_ERR_ARG;
+    if (layer < 0 || layer >= pool->L) return KVC_ERR_ARG;
+    if (num_q_heads <= 0 || num_q_heads % pool->H_KV != 0) return KVC_ERR_ARG;
+    if (num_q_heads / pool->H_KV > 32) return KVC_ERR_UNSUPPORTED;
+    if (pool->bs != kBS || !pool->tmap_ok) return KVC_ERR_UNSUPPORTED;
+    if (max_blocks <= 0 || max_blocks > (1 << 26) || !std::isfinite(scale)) return KVC_ERR_ARG;
+    if (!is_aligned(q, 16) || !is_aligned(out, 16) || (lse && !is_aligned(lse, 4)) || !is_aligned(block_tables, 4) ||
+        !is_aligned(seq_lens, 4))
+        return KVC_ERR_ARG;
+    kvc_status st = check_device(pool);
+    if (st != KVC_OK) return st;
+    float *scratch = noalloc_scratch_ptr(pool->device);   // first call on a device: symbol lookup
+    if (!scratch) return KVC_ERR_CUDA;
+
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.bt = block_tables;
+    p.lens = seq_lens;
+    p.bt_stride = max_blocks;
+    p.max_blocks = max_blocks;
+    p.len_base = 0;
+    p.B = B;
+    p.H_Q = num_q_heads;
+    p.H_KV = pool->H_KV;
+    p.g = num_q_heads / pool->H_KV;
+    p.layer = layer;
+    p.N = pool->N;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.s_k = pool->scales ? pool->scales + static_cast<size_t>(layer) * 2 * pool->H_KV * pool->D : nullptr;
+    p.s_v = p.s_k ? p.s_k + static_cast<size_t>(pool->H_KV) * pool->D : nullptr;
+    p.out = out;
+    p.lse = lse;
+    p.err = pool->err;
+
+    const DecodeKernel k =
+        pool->dtype == KVC_FP8_E4M3 ? select_decode_fp8(pool->D, p.g) : select_decode_bf16(pool->D, p.g);
+    if (!k.fn) return KVC_ERR_UNSUPPORTED;
+    if (k.ctas_per_sm <= 0) return KVC_ERR_CUDA;
+    choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits);
+    if (p.max_splits > 65535) return KVC_ERR_UNSUPPORTED;
+    if (p.max_splits > 1) {
+        // partials: o [B][H_Q][splits][D] then (max, sum) [B][H_Q][splits]; every slot read is written first
+        const size_t n = static_cast<size_t>(p.B) * p.H_Q * p.max_splits;
+        if (n * (static_cast<size_t>(pool->D) + 2) > kNoallocScratchFloats) return KVC_ERR_ARG;
+        p.part_o = scratch;
+        p.part_ml = reinterpret_cast<float2 *>(scratch + n * pool->D);
+    }
+    const dim3 grid(p.max_splits, p.H_KV, p.B);
+    void *args[] = {const_cast<CUtensorMap *>(&pool->tmap), &p};
+    const cudaError_t e = cudaLaunchKernel(k.fn, grid, dim3(kThreads), args, k.smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (p.max_splits > 1) return launch_split_merge(p, pool->D, static_cast<cudaStream_t>(stream));
+    return KVC_OK;
+}
