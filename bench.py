@@ -220,6 +220,21 @@ def config_dict(w):
             "l2": f"inputs larger than L2: {step_bytes(w)['kv'] / 1e9:.2f} GB of KV per step vs {L2_BYTES / 2**20:.0f} MiB L2"}
 
 
+# ---------------------------------------------------------------- multi-rank aggregation
+def max_over_ranks(values, dist, device="cpu"):
+    """Element-wise MAX of per-rank timings (every rank gets the result)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def weak_scaling_value(bytes_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's time."""
+    return bytes_per_rank * world / (max_ms * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- GPU side
 def main():
     ap = argparse.ArgumentParser()
@@ -336,13 +351,9 @@ def main():
     e2e_ms = e_start.elapsed_time(e_end) / K
 
     # ---- max over ranks
-    vals = torch.tensor([ms, e2e_ms, attn_ms], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms, e2e_ms, attn_ms = [float(x) for x in vals.cpu()]
-    total_bytes = sb["total"] * world
-    value = total_bytes / (ms * 1e-3) / 1e9
-    e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+    ms, e2e_ms, attn_ms = max_over_ranks([ms, e2e_ms, attn_ms], dist, "cuda")
+    value = weak_scaling_value(sb["total"], world, ms)
+    e2e_value = weak_scaling_value(sb["total"], world, e2e_ms)
     hbm, peak_kind = peaks()
     achieved = sb["attn_kernel"] / (attn_ms * 1e-3) / 1e9
     cpu = None
