@@ -196,6 +196,24 @@ KVC_API kvc_status kvc_decode_attn(kvc_pool *pool, int32_t layer, const void *q,
                            const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, int32_t B,
                            float *out, float *lse, float scale, kvc_stream_t stream);
 
+/* One decode step at one layer in a single launch: kvc_append followed by
+ * kvc_decode_attn ("KV cache: Generation state, latency, and allocation"
+ * Eq. 21.6 and 21.1: the pass appends its token's key and value, and the new
+ * query reads every cached key plus its own).  seq_lens holds the counts
+ * BEFORE the append; sequence b's k_new/v_new rows are stored at position
+ * seq_lens[b] exactly as kvc_append stores them, and attention runs over
+ * seq_lens[b] + 1 positions.  The CTA that owns a sequence's last block
+ * writes the new rows to the pool and into its staged copy of that block, so
+ * the pool bytes and the outputs are bit-identical to the two separate calls.
+ * The block receiving an append must not be mapped by another sequence of the
+ * same call (shared blocks are copied before a write: 21.5, copy-on-write).
+ *   k_new, v_new: device bf16 [B][H_KV][d_h], 16-byte aligned
+ * Other arguments, requirements and errors as kvc_decode_attn. */
+KVC_API kvc_status kvc_decode_step(kvc_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
+                                   const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, int32_t B,
+                                   const void *k_new, const void *v_new, float *out, float *lse, float scale,
+                                   kvc_stream_t stream);
+
 /* Causal attention of a prefill chunk over one sequence's paged cache
  * ("KV cache: Generation state, latency, and allocation" 21.3, chunked
  * prefill: later portions keep the earlier positions; the xf_kv_cache page,

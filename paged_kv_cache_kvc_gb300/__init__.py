@@ -44,7 +44,7 @@ class kvc_pool_desc(ctypes.Structure):
 
 EXPORTS = ["kvc_pool_create", "kvc_pool_destroy", "kvc_pool_info", "kvc_pool_set_scales", "kvc_calibrate_fp8",
            "kvc_append", "kvc_write_tokens", "kvc_decode_attn", "kvc_prefill_attn", "kvc_pool_reserve",
-           "kvc_bytes", "kvc_pool_sync_status", "kvc_status_str", "kvc_launch_count", "kvc_decode_attn_noalloc"]
+           "kvc_bytes", "kvc_pool_sync_status", "kvc_status_str", "kvc_launch_count", "kvc_decode_attn_noalloc", "kvc_decode_step"]
 
 
 def load(path: str = LIB_PATH):
@@ -66,6 +66,8 @@ def load(path: str = LIB_PATH):
     L.kvc_write_tokens.restype, L.kvc_write_tokens.argtypes = st, [vp, i32, vp, i32, vp, vp, i32, i32, vp, vp, vp]
     L.kvc_decode_attn.restype = st
     L.kvc_decode_attn.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, vp, vp, ctypes.c_float, vp]
+    L.kvc_decode_step.restype = st
+    L.kvc_decode_step.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, vp, vp, vp, vp, ctypes.c_float, vp]
     L.kvc_decode_attn_noalloc.restype = st
     L.kvc_decode_attn_noalloc.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, vp, vp, ctypes.c_float, vp]
     L.kvc_prefill_attn.restype = st
@@ -213,6 +215,20 @@ def kvc_decode_attn(pool, layer, q, block_tables, seq_lens, out, lse=None, scale
                                   _dev(seq_lens, torch.int32, "seq_lens"), B, _dev(out, torch.float32, "out"),
                                   _dev(lse, torch.float32, "lse", optional=True), float(scale), _stream(stream)),
            "kvc_decode_attn")
+
+
+def kvc_decode_step(pool, layer, q, block_tables, seq_lens_pre, k_new, v_new, out, lse=None, scale=None,
+                    stream=None):
+    """Append (at seq_lens_pre[b]) and decode attention (over seq_lens_pre[b] + 1) in one launch."""
+    B, H_Q, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    _check(load().kvc_decode_step(_h(pool), layer, _dev(q, torch.bfloat16, "q"), H_Q,
+                                  _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+                                  _dev(seq_lens_pre, torch.int32, "seq_lens"), B, _dev(k_new, torch.bfloat16, "k_new"),
+                                  _dev(v_new, torch.bfloat16, "v_new"), _dev(out, torch.float32, "out"),
+                                  _dev(lse, torch.float32, "lse", optional=True), float(scale), _stream(stream)),
+           "kvc_decode_step")
 
 
 def kvc_decode_attn_noalloc(pool, layer, q, block_tables, seq_lens, out, lse=None, scale=None, stream=None):

@@ -13,7 +13,7 @@ namespace kvc {
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int D)
 {
     const int hq = blockIdx.x, b = blockIdx.y;
-    int len = p.lens ? __ldg(p.lens + b) : p.len_base + b + 1;
+    int len = seq_len(p, b);
     if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) len = 0;
     const int nblk = (len + kBS - 1) / kBS;
     const int ns = (nblk + p.chunk - 1) / p.chunk;
@@ -35,20 +35,23 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int D)
 }
 
 // Blocks per split.  Sequences are independent and every CTA reads only its
-// own blocks, so the kernel is bound by HBM as long as enough CTAs stream at
-// once; splitting a sequence costs a partial write and a merge.  Aim for one
-// CTA per resident slot, with at least 16 blocks (4 per warp) per CTA and at
-// most 1024.  KVC_SPLIT_CHUNK overrides (rounded up to a multiple of 4).
-void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits)
+// own blocks, so the kernel is bound by HBM once enough bytes are in flight;
+// each CTA keeps 4 warps x (R - 1) stages in flight, so HBM wants more CTAs
+// than one per resident slot.  Measured on GB300: about 1.7 CTAs per resident
+// slot is best (a split costs a partial write and the merge).  Blocks per
+// split stay between 16 (x the query n-tiles: a split's partials grow with
+// the group size) and 1024.  KVC_SPLIT_CHUNK overrides (rounded up to 4).
+void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits,
+                  int n_tiles)
 {
     int ch = 0;
     if (const char *e = std::getenv("KVC_SPLIT_CHUNK")) ch = std::atoi(e);
     if (ch <= 0) {
-        const long slots = static_cast<long>(pool->num_sms) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
-        long ns = units > 0 ? slots / units : 1;
+        const double slots = static_cast<double>(pool->num_sms) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+        long ns = units > 0 ? std::lround(1.7 * slots / units) : 1;
         if (ns < 1) ns = 1;
         ch = static_cast<int>((max_blocks + ns - 1) / ns);
-        if (ch < 16) ch = 16;
+        if (ch < 16 * n_tiles) ch = 16 * n_tiles;
         if (ch > 1024) ch = 1024;
     }
     ch = (ch + 3) & ~3;
@@ -71,20 +74,21 @@ static kvc_status ensure_workspace(kvc_pool *pool, size_t bytes)
         return KVC_ERR_OOM;
     }
     pool->ws_bytes = bytes;
-    return KVC_OK;
+    return cuda_status(cudaMemset(pool->ws, 0, bytes));   // the arrival counters start at zero
 }
 
+// partials o [B][H_Q][splits][D], (max, sum) [B][H_Q][splits], then arrival counters [B][H_KV]
 static size_t workspace_bytes(int B, int H_Q, int max_splits, int D)
 {
     const size_t n = static_cast<size_t>(B) * H_Q * max_splits;
-    return n * D * sizeof(float) + n * sizeof(float2) + 256;
+    return n * D * sizeof(float) + n * sizeof(float2) + static_cast<size_t>(B) * H_Q * sizeof(uint32_t) + 256;
 }
 
 kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream)
 {
     kvc_pool *pool = const_cast<kvc_pool *>(cpool);
     if (!k.fn || k.ctas_per_sm <= 0) return KVC_ERR_CUDA;
-    choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits);
+    choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits, n_tiles(p.g));
     if (p.max_splits > 65535) return KVC_ERR_UNSUPPORTED;
     if (p.max_splits > 1) {
         kvc_status st = ensure_workspace(pool, workspace_bytes(p.B, p.H_Q, p.max_splits, pool->D));
@@ -92,16 +96,20 @@ kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel
         const size_t n = static_cast<size_t>(p.B) * p.H_Q * p.max_splits;
         p.part_o = static_cast<float *>(pool->ws);
         p.part_ml = reinterpret_cast<float2 *>(static_cast<float *>(pool->ws) + n * pool->D);
+        // the last split CTA merges its group in the kernel when that is a small job (g * splits
+        // partial rows); otherwise one merge CTA per (sequence, query head) does it afterwards
+        p.counters = (p.g * p.max_splits <= 64) ? reinterpret_cast<uint32_t *>(p.part_ml + n) : nullptr;
     } else {
         p.part_o = nullptr;
         p.part_ml = nullptr;
+        p.counters = nullptr;
     }
     const dim3 grid(p.max_splits, p.H_KV, p.B);
     void *args[] = {const_cast<CUtensorMap *>(&pool->tmap), &p};
     cudaError_t e = cudaLaunchKernel(k.fn, grid, dim3(kThreads), args, k.smem, stream);
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    if (p.max_splits > 1) {
+    if (p.max_splits > 1 && !p.counters) {
         merge_kernel<<<dim3(p.H_Q, p.B), 128, 0, stream>>>(p, pool->D);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_status(e);
@@ -169,6 +177,29 @@ extern "C" kvc_status kvc_decode_attn(kvc_pool *pool, int32_t layer, const void 
     p.bt_stride = max_blocks;
     p.len_base = 0;
     p.B = B;
+    return dispatch(pool, p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvc_status kvc_decode_step(kvc_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
+                                      const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
+                                      int32_t B, const void *k_new, const void *v_new, float *out, float *lse,
+                                      float scale, kvc_stream_t stream)
+{
+    if (B < 0 || B > 65535) return KVC_ERR_ARG;
+    if (B == 0) return pool ? KVC_OK : KVC_ERR_ARG;
+    if (!seq_lens || !aligned(seq_lens, 4) || !k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16))
+        return KVC_ERR_ARG;
+    kvc_status st = common_attn_checks(pool, layer, q, num_q_heads, block_tables, max_blocks, out, lse, scale);
+    if (st != KVC_OK) return st;
+    DecodeParams p{};
+    fill_common(p, pool, layer, q, num_q_heads, block_tables, max_blocks, out, lse, scale);
+    p.lens = seq_lens;
+    p.bt_stride = max_blocks;
+    p.len_base = 0;
+    p.B = B;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.pool = pool->base;
     return dispatch(pool, p, static_cast<cudaStream_t>(stream));
 }
 

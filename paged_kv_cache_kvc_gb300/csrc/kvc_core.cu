@@ -398,6 +398,10 @@ extern "C" kvc_status kvc_pool_sync_status(kvc_pool *pool, kvc_stream_t stream)
         cudaMemcpy(&bits, pool->err, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess ||
         cudaMemset(pool->err, 0, sizeof(bits)) != cudaSuccess)
         return KVC_ERR_CUDA;
+    if ((bits & KVC_EBIT_TIMEOUT) && pool->ws) {
+        // an expired wait may have left split arrival counters short of their count: restart them at zero
+        if (cudaMemset(pool->ws, 0, pool->ws_bytes) != cudaSuccess) return KVC_ERR_CUDA;
+    }
     if (bits & KVC_EBIT_BAD_BLOCK) return KVC_ERR_BAD_BLOCK;
     if (bits & KVC_EBIT_RANGE) return KVC_ERR_RANGE;
     if (bits & KVC_EBIT_TIMEOUT) return KVC_ERR_TIMEOUT;

@@ -76,6 +76,51 @@ __device__ __forceinline__ uint32_t swz(int row, int ch)
     return static_cast<uint32_t>((band * 2 * kBS + row) * 128 + ((c ^ (row & 7)) << 4));
 }
 
+// Positions attended by sequence b: lens[b] (+1 when the step's token is appended
+// in the same launch), or len_base + b + 1 for a prefill chunk's query b.
+__device__ __forceinline__ int seq_len(const DecodeParams &p, int b)
+{
+    if (!p.lens) return p.len_base + b + 1;
+    return __ldg(p.lens + b) + (p.k_new ? 1 : 0);
+}
+
+// Fused append ("KV cache: Generation state, latency, and allocation" Eq. 21.6):
+// store sequence b's new key and value rows of head h at (phys, slot) in the
+// pool, and put the same stored bytes into the landed stage, so attention uses
+// exactly what the pool now holds.  Lanes [0, CH) take the key row, [CH, 2CH)
+// the value row, one 16-byte chunk each.
+template <int D, bool FP8>
+__device__ __forceinline__ void append_row(const DecodeParams &p, uint32_t st, int b, int h, int64_t phys, int slot,
+                                           int lane)
+{
+    using C = DecodeCfg<D, FP8>;
+    constexpr int CH = C::ROW_BYTES / 16;
+    static_assert(2 * CH <= 32, "one warp covers both rows");
+    if (lane >= 2 * CH) return;
+    const int kv = lane / CH, ch = lane - kv * CH;
+    const uint16_t *src = (kv ? p.v_new : p.k_new) + (static_cast<size_t>(b) * p.H_KV + h) * D;
+    uint4 val;
+    if constexpr (!FP8) {
+        val = *reinterpret_cast<const uint4 *>(src + ch * 8);
+    } else {
+        const uint4 x0 = *reinterpret_cast<const uint4 *>(src + ch * 16);
+        const uint4 x1 = *reinterpret_cast<const uint4 *>(src + ch * 16 + 8);
+        const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const float *sc = (kv ? p.s_v : p.s_k) + static_cast<size_t>(h) * D + ch * 16;
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float f = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+            const uint32_t q = __nv_cvt_float_to_fp8(__fdiv_rn(f, __ldg(sc + i)), __NV_SATFINITE, __NV_E4M3);
+            o[i >> 2] |= q << (8 * (i & 3));
+        }
+        val = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    const int64_t e = ((((static_cast<int64_t>(p.layer) * p.N + phys) * p.H_KV + h) * 2 + kv) * kBS + slot) * D;
+    *reinterpret_cast<uint4 *>(p.pool + e * C::ELEM + ch * 16) = val;
+    sts128(st + swz(kv * kBS + slot, ch), val);
+}
+
 template <int D, int NT, bool FP8, bool PSPLIT>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmap,
                                                           const DecodeParams p)
@@ -89,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int gq = lane >> 2, tg = lane & 3;
     const int hq0 = h * p.g;
 
-    int len = p.lens ? __ldg(p.lens + b) : p.len_base + b + 1;
+    int len = seq_len(p, b);
     if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) {
         if (split == 0 && threadIdx.x == 0) atomicOr(p.err, KVC_EBIT_RANGE);
         len = 0;
@@ -205,8 +250,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             if (valid < kBS) {
                 const int nz = (kBS - valid) * C::BANDS * 8;
                 for (int i = lane; i < nz; i += 32) sts128_zero(st + swz(kBS + valid + i / (C::BANDS * 8), i % (C::BANDS * 8)));
-                __syncwarp();
             }
+            // the step's own token (fused append) is the last valid slot of the last block
+            if (p.k_new && blk0 + warp + kWarps * j == nblk - 1) append_row<D, FP8>(p, st, b, h, phys, valid - 1, lane);
+            __syncwarp();
 
             // ---- S^T = K Q^T
             float sc[NT][4];
@@ -235,10 +282,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 #pragma unroll
                 for (int kk = 0; kk < C::KSTEPS; ++kk) {
                     uint32_t a[4];
-                    a[0] = e4m3x2_to_f16x2(kw[0][kk]);
-                    a[1] = e4m3x2_to_f16x2(kw[1][kk]);
-                    a[2] = e4m3x2_to_f16x2(kw[0][kk] >> 16);
-                    a[3] = e4m3x2_to_f16x2(kw[1][kk] >> 16);
+                    e4m3x4_to_f16x2x2(kw[0][kk], a[0], a[2]);
+                    e4m3x4_to_f16x2x2(kw[1][kk], a[1], a[3]);
 #pragma unroll
                     for (int jn = 0; jn < NT; ++jn) mma_f16(sc[jn], a, qf[jn][kk]);
                 }
@@ -317,10 +362,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     const uint32_t y01 = __byte_perm(vw[0][w], vw[1][w], 0x7362);
                     const uint32_t x89 = __byte_perm(vw[2][w], vw[3][w], 0x5140);
                     const uint32_t y89 = __byte_perm(vw[2][w], vw[3][w], 0x7362);
-                    const uint32_t a0[4] = {e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16),
-                                            e4m3x2_to_f16x2(x89), e4m3x2_to_f16x2(x89 >> 16)};
-                    const uint32_t a1[4] = {e4m3x2_to_f16x2(y01), e4m3x2_to_f16x2(y01 >> 16),
-                                            e4m3x2_to_f16x2(y89), e4m3x2_to_f16x2(y89 >> 16)};
+                    uint32_t a0[4], a1[4];
+                    e4m3x4_to_f16x2x2(x01, a0[0], a0[1]);
+                    e4m3x4_to_f16x2x2(x89, a0[2], a0[3]);
+                    e4m3x4_to_f16x2x2(y01, a1[0], a1[1]);
+                    e4m3x4_to_f16x2x2(y89, a1[2], a1[3]);
 #pragma unroll
                     for (int jn = 0; jn < NT; ++jn) {
                         mma_f16(oacc[2 * w][jn], a0, pb[jn]);
@@ -405,6 +451,39 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             if (d == 0) p.part_ml[pi] = make_float2(M, L);
         }
     }
+    if (ns == 1 || !p.counters) return;   // without counters the host launches the merge kernel
+
+    // ---- split-K merge by the last split CTA of (b, h) to finish: the partial
+    // writes above are released by the fence before the count, and acquired
+    // by the fence after the last CTA sees ns - 1 earlier arrivals.
+    __shared__ uint32_t last_flag;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t prev = atomicAdd(p.counters + static_cast<size_t>(b) * p.H_KV + h, 1u);
+        last_flag = (prev == static_cast<uint32_t>(ns - 1)) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!last_flag) return;
+    __threadfence();
+    for (int i = threadIdx.x; i < p.g * D; i += kThreads) {
+        const int qi = i / D, d = i - qi * D;
+        const size_t bq = static_cast<size_t>(b) * p.H_Q + hq0 + qi;
+        const float2 *ml = p.part_ml + bq * p.max_splits;
+        const float *po = p.part_o + bq * p.max_splits * D + d;
+        float M = -INFINITY;
+        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, __ldcg(&ml[sp].x));
+        float L = 0.f, O = 0.f;
+        for (int sp = 0; sp < ns; ++sp) {
+            const float2 v = __ldcg(ml + sp);
+            const float e = fast_exp2(v.x - M);
+            L += e * v.y;
+            O += e * __ldcg(po + static_cast<size_t>(sp) * D);
+        }
+        p.out[bq * D + d] = O / L;
+        if (d == 0 && p.lse) p.lse[bq] = (M + log2f(L)) * kLn2;
+    }
+    if (threadIdx.x == 0) p.counters[static_cast<size_t>(b) * p.H_KV + h] = 0u;   // ready for the next launch
 }
 
 // Fetch (and on first use configure) the kernel instance for a shape.

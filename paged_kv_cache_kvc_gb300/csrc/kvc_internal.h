@@ -52,6 +52,13 @@ struct DecodeParams {
     float *part_o;           // [B][H_Q][max_splits][D]
     float2 *part_ml;         // [B][H_Q][max_splits]  (running max in log2 units, sum)
     uint32_t *err;
+    // fused append (kvc_decode_step): the step's new key / value rows, bf16 [B][H_KV][D],
+    // written at position lens[b] before attending to lens[b] + 1 positions; nullptr = none
+    const uint16_t *k_new;
+    const uint16_t *v_new;
+    uint8_t *pool;           // pool base (the fused append's global store)
+    // split-K arrival counters [B][H_KV], zero between launches; nullptr = merge in a separate kernel
+    uint32_t *counters;
 };
 
 kvc_status cuda_status(cudaError_t e);
@@ -62,6 +69,9 @@ kvc_status launch_decode_bf16(const kvc_pool *pool, DecodeParams &p, cudaStream_
 kvc_status launch_decode_fp8(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream);
 
 // Split-K sizing: blocks per split and the split count for a batch.
-void choose_split(const kvc_pool *pool, int B, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits);
+void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits,
+                  int n_tiles);
+// 8-wide query n-tiles a group of g query heads occupies in the decode kernel.
+inline int n_tiles(int g) { return g <= 8 ? 1 : (g <= 16 ? 2 : 4); }
 
 }  // namespace kvc

@@ -139,6 +139,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void sts128_zero(uint32_t addr)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
@@ -183,11 +189,15 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
-// two e4m3 codes (byte 0 -> low half, byte 1 -> high half) to f16x2, exact
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+// four e4m3 codes (bytes 0..3 of x) to two f16x2: bytes (0,1) -> lo, bytes (2,3) -> hi; exact
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t &lo, uint32_t &hi)
 {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
 }
 
 __device__ __forceinline__ float fast_exp2(float x)

@@ -399,3 +399,45 @@ def test_launches_are_counted(kvc):
         assert kvc.kvc_launch_count() - n0 >= 2
     finally:
         g.close()
+
+
+@pytest.mark.parametrize("case", ["tiny", "boundary", "boundary_split4", "fp8_gqa", "mqa", "mha_fp8"])
+def test_fused_step_equals_append_then_decode(kvc, case):
+    """kvc_decode_step (append + attention in one launch) leaves the same pool
+    bytes and gives bit-identical outputs to kvc_append then kvc_decode_attn."""
+    lens = [0, 1, 15, 16, 31, 100, 1023]
+    w = {"tiny": lambda: synth.make_workload("tiny", seed=1),
+         "boundary": lambda: _custom(B=len(lens), H_Q=32, H_KV=8, d_h=128, lens=lens),
+         "boundary_split4": lambda: _custom(B=len(lens), H_Q=32, H_KV=8, d_h=128, lens=lens),
+         "fp8_gqa": lambda: _custom(B=3, H_Q=32, H_KV=8, d_h=128, lens=[7, 500, 2047], dtype="fp8"),
+         "mqa": lambda: _custom(B=2, H_Q=32, H_KV=1, d_h=128, lens=[300, 65]),
+         "mha_fp8": lambda: _custom(B=2, H_Q=16, H_KV=16, d_h=128, lens=[48, 17], dtype="fp8")}[case]()
+    if case == "boundary_split4":
+        os.environ["KVC_SPLIT_CHUNK"] = "4"
+    try:
+        ld = layer_data(w, 0)
+        res = []
+        for fused in (False, True):
+            g = GpuCase(kvc, w, fill_byte=0xA5)
+            try:
+                g.load_context(0, ld)
+                q, k, v = g.step_inputs(ld)
+                out = torch.empty((w.B, w.H_Q, w.d_h), device="cuda")
+                lse = torch.empty((w.B, w.H_Q), device="cuda")
+                if fused:
+                    kvc.kvc_decode_step(g.pool, 0, q, g.bt_dec, g.lens_pre, k, v, out, lse, scale=w.scale)
+                else:
+                    kvc.kvc_append(g.pool, 0, g.bt_dec, g.lens_pre, k, v)
+                    kvc.kvc_decode_attn(g.pool, 0, q, g.bt_dec, g.lens_post, out, lse, scale=w.scale)
+                torch.cuda.synchronize()
+                assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+                res.append((g.layer_bytes(0), out.cpu(), lse.cpu()))
+            finally:
+                g.close()
+        n, first = first_mismatch(res[0][0], res[1][0])
+        assert n == 0, f"{n} pool bytes differ, first at {first}"
+        assert torch.equal(res[0][1], res[1][1]) and torch.equal(res[0][2], res[1][2])
+        ref = OracleCase(w).run_layer(ld, image=False)
+        check_attention(res[1][1], res[1][2], ref["out"], ref["lse"], w.dtype, f"fused {case}")
+    finally:
+        os.environ.pop("KVC_SPLIT_CHUNK", None)
