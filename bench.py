@@ -56,12 +56,16 @@ def step_bytes(w) -> dict:
             "total": kv + table + q + out + append + lens_b}
 
 
+# the sources the decode kernel is compiled from (its ncu counters go stale when one changes)
+KERNEL_SOURCES = ["kvc_decode.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_decode_bf16.cu", "kvc_decode_fp8.cu",
+                  "kvc_attn.cu"]
+
+
 def source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_kvc_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -217,7 +221,8 @@ def config_dict(w):
     return {"workload": w.name, "B": w.B, "H_Q": w.H_Q, "H_KV": w.H_KV, "d_h": w.d_h, "block_size": w.bs,
             "layers": w.L, "context": int(w.lens_pre.max()), "attended": int(w.lens_post.max()),
             "kv_dtype": w.dtype, "num_blocks": w.num_blocks,
-            "l2": f"inputs larger than L2: {step_bytes(w)['kv'] / 1e9:.2f} GB of KV per step vs {L2_BYTES / 2**20:.0f} MiB L2"}
+            "l2": f"inputs larger than L2: {step_bytes(w)['kv'] * w.L / 1e9:.2f} GB of KV per step vs "
+                  f"{L2_BYTES / 2**20:.0f} MiB L2"}
 
 
 # ---------------------------------------------------------------- multi-rank aggregation
@@ -274,18 +279,30 @@ def main():
     kvc.load()
 
     w = synth.make_workload(args.workload, seed=args.seed + rank)     # each rank: its own batch
-    assert w.L == 1, "bench times one layer's step"
-    ld = layer_data(w, 0)
+    L = w.L
     g = GpuCase(kvc, w, fill_byte=0)
-    g.load_context(0, ld)
-    q, k_new, v_new = g.step_inputs(ld)
-    out = torch.empty((w.B, w.H_Q, w.d_h), dtype=torch.float32, device="cuda")
-    lse = torch.empty((w.B, w.H_Q), dtype=torch.float32, device="cuda")
+    q, k_new, v_new, outs, lses = [], [], [], [], []
+    ld = None
+    for layer in range(L):          # every layer's context into the pool; keep only the step's inputs
+        ld_l = layer_data(w, layer)
+        g.load_context(layer, ld_l)
+        a, b_, c = g.step_inputs(ld_l)
+        q.append(a)
+        k_new.append(b_)
+        v_new.append(c)
+        outs.append(torch.empty((w.B, w.H_Q, w.d_h), dtype=torch.float32, device="cuda"))
+        lses.append(torch.empty((w.B, w.H_Q), dtype=torch.float32, device="cuda"))
+        if layer == 0:
+            ld = ld_l               # the CPU baseline samples layer 0
+        torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    sb = step_bytes(w)
+    sb1 = step_bytes(w)
+    sb = {k: v * L for k, v in sb1.items()}
 
-    def step():     # append + paged decode attention: one fused launch (kvc_decode_step)
-        kvc.kvc_decode_step(g.pool, 0, q, g.bt_dec, g.lens_pre, k_new, v_new, out, lse, scale=w.scale)
+    def step():     # each layer: append + paged decode attention, one fused launch (kvc_decode_step)
+        for layer in range(L):
+            kvc.kvc_decode_step(g.pool, layer, q[layer], g.bt_dec, g.lens_pre, k_new[layer], v_new[layer],
+                                outs[layer], lses[layer], scale=w.scale)
 
     def barrier():
         if dist is not None:
@@ -297,7 +314,17 @@ def main():
     barrier()
     assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
 
-    # ---- device-resident timed region; events on the launching stream bracket every step's launch
+    run = step
+    graph = None
+    if L > 1:       # a multi-layer step replays as one CUDA graph of L launches
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        barrier()
+        run = graph.replay
+
+    # ---- device-resident timed region; events on the launching stream bracket every step
     K = args.steps
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -308,42 +335,38 @@ def main():
         t_start.record(stream)
         for i in range(K):
             ev_a[i].record(stream)
-            step()
+            run()
             ev_b[i].record(stream)
         t_end.record(stream)
         barrier()
-    launches = kvc.kvc_launch_count() - launches0
+    launches = kvc.kvc_launch_count() - launches0 if graph is None else K * L
     ms = t_start.elapsed_time(t_end) / K
-    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]))
+    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_a, ev_b)])) / L    # per launch
     clocks = clk.summary()
     assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
 
     # ---- end to end through the public API: pinned host inputs in, results out, every step
-    q_h = torch.empty_like(q, device="cpu").pin_memory()
-    k_h = torch.empty_like(k_new, device="cpu").pin_memory()
-    v_h = torch.empty_like(v_new, device="cpu").pin_memory()
-    bt_h = g.bt_dec.cpu().pin_memory()
-    lp_h, lq_h = g.lens_pre.cpu().pin_memory(), g.lens_post.cpu().pin_memory()
-    q_h.copy_(q)
-    k_h.copy_(k_new)
-    v_h.copy_(v_new)
-    out_h = torch.empty_like(out, device="cpu").pin_memory()
-    lse_h = torch.empty_like(lse, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, bt_h, lp_h, lq_h))
-    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    pin = lambda t: t.cpu().pin_memory()
+    q_h, k_h, v_h = [pin(t) for t in q], [pin(t) for t in k_new], [pin(t) for t in v_new]
+    bt_h, lp_h = pin(g.bt_dec), pin(g.lens_pre)
+    out_h = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    lse_h = [torch.empty_like(t, device="cpu").pin_memory() for t in lses]
+    h2d = sum(t.numel() * t.element_size() for t in q_h + k_h + v_h + [bt_h, lp_h])
+    d2h = sum(t.numel() * 4 for t in out_h + lse_h)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     e_start.record(stream)
     for i in range(K):
-        q.copy_(q_h, non_blocking=True)
-        k_new.copy_(k_h, non_blocking=True)
-        v_new.copy_(v_h, non_blocking=True)
         g.bt_dec.copy_(bt_h, non_blocking=True)
         g.lens_pre.copy_(lp_h, non_blocking=True)
-        g.lens_post.copy_(lq_h, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        for layer in range(L):
+            q[layer].copy_(q_h[layer], non_blocking=True)
+            k_new[layer].copy_(k_h[layer], non_blocking=True)
+            v_new[layer].copy_(v_h[layer], non_blocking=True)
+            kvc.kvc_decode_step(g.pool, layer, q[layer], g.bt_dec, g.lens_pre, k_new[layer], v_new[layer],
+                                outs[layer], lses[layer], scale=w.scale)
+            out_h[layer].copy_(outs[layer], non_blocking=True)
+            lse_h[layer].copy_(lses[layer], non_blocking=True)
     e_end.record(stream)
     barrier()
     e2e_ms = e_start.elapsed_time(e_end) / K
@@ -353,14 +376,15 @@ def main():
     value = weak_scaling_value(sb["total"], world, ms)
     e2e_value = weak_scaling_value(sb["total"], world, e2e_ms)
     hbm, peak_kind = peaks()
-    achieved = sb["total"] / (attn_ms * 1e-3) / 1e9
+    achieved = sb1["total"] / (attn_ms * 1e-3) / 1e9
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rate, dt, k, desc, cores = oracle_sample(w, ld, args.cpu_budget)
         cpu = {"value": rate / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{desc}; {dt:.1f} s"}
     if rank == 0:
-        splits_note = "one launch per step" if launches == K else f"{launches / K:.1f} launches per step"
+        splits_note = (f"{L} launches per step (one per layer)" + (", replayed as one CUDA graph" if graph else "")
+                       if launches == K * L else f"{launches / K:.1f} launches per step")
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
                 "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": w.dtype, "data": "synthetic", "config": config_dict(w),
@@ -371,7 +395,7 @@ def main():
                              "frac": achieved / hbm, "traffic": profiled_traffic(w.name),
                              "kernel": "decode_kernel with fused append (kvc_decode_step)",
                              "peak_source": f"{peak_kind} hbm_gbs",
-                             "algorithmic_bytes_per_launch": sb["total"], "launch_ms": attn_ms,
+                             "algorithmic_bytes_per_launch": sb1["total"], "launch_ms": attn_ms,
                              "note": splits_note},
                 "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
                 "step_bytes": sb}
