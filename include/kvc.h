@@ -258,6 +258,71 @@ KVC_API kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, const 
                                            const int32_t *seq_lens, int32_t B, float *out, float *lse,
                                            float scale, kvc_stream_t stream);
 
+/* ------------------------------------------------------------------ block allocator (host) */
+
+/* Host-side block allocator that produces the block tables the calls above
+ * consume ("KV cache: Generation state, latency, and allocation" 21.5 and
+ * Table 21.1 steps 1-5; 21.4 prefix identity; "KV Cache Explained", "Why
+ * PagedAttention allocates KV in blocks" and "Follow the 32 GiB pool until it
+ * cannot allocate one more block").  Pure host code: no device memory, not
+ * thread-safe (one caller at a time).
+ *   - Blocks come from a FIFO free queue (initial order `free_order`, a
+ *     permutation of [0, N), or ascending when NULL); when it is empty, the
+ *     least recently released evictable cached block is reclaimed; when both
+ *     are empty a reservation fails with KVC_ERR_OOM and changes nothing.
+ *   - Every block has a reference count: one per sequence mapping it.
+ *   - A sequence releases its references; a block at count 0 returns to the
+ *     free queue, or (retain_cached = 1, and the block is a published full
+ *     block) stays as an evictable cached entry that a prefix match revives.
+ *   - Copy-on-write: a reservation whose next write lands in a shared, partly
+ *     filled block maps a fresh block instead and reports the (old, new) pair,
+ *     which the caller copies on the device (kvc_copy_blocks) before writing.
+ * Sequence ids are small integers; a released id is reused by the next new
+ * sequence (lowest first).  Errors: KVC_ERR_ARG for unknown ids or bad
+ * sizes, KVC_ERR_OOM as above, KVC_ERR_ALIAS for a commit into a shared block. */
+typedef struct kvc_alloc kvc_alloc;
+
+KVC_API kvc_status kvc_alloc_create(int64_t num_blocks, int32_t block_size, const int32_t *free_order,
+                                    int32_t retain_cached, kvc_alloc **out);
+KVC_API void kvc_alloc_destroy(kvc_alloc *alloc);
+/* A new, empty sequence. */
+KVC_API kvc_status kvc_alloc_new_seq(kvc_alloc *alloc, int32_t *seq);
+/* A new sequence sharing the first n_tokens positions of src (its blocks
+ * gain a reference; a partly filled last block is shared until written). */
+KVC_API kvc_status kvc_alloc_fork(kvc_alloc *alloc, int32_t src, int32_t n_tokens, int32_t *seq);
+/* Make room for n_tokens more positions: map new blocks as the sequence
+ * crosses block boundaries (Table 21.1 step 2), copy-on-write as above.
+ * cow_pairs: host int32 [max_cow][2] (old, new); *n_cow receives 0 or 1. */
+KVC_API kvc_status kvc_alloc_reserve(kvc_alloc *alloc, int32_t seq, int32_t n_tokens, int32_t *cow_pairs,
+                                     int32_t max_cow, int32_t *n_cow);
+/* Record that n_tokens more positions were written (after kvc_append /
+ * kvc_write_tokens). */
+KVC_API kvc_status kvc_alloc_commit(kvc_alloc *alloc, int32_t seq, int32_t n_tokens);
+/* Drop the sequence's references (Table 21.1 steps 4-5). */
+KVC_API kvc_status kvc_alloc_release(kvc_alloc *alloc, int32_t seq);
+/* Register the identities h_i = hash(h_{i-1}, tokens_i), h_0 = hash(salt), of
+ * the sequence's full blocks covering tokens[0, n_tokens) (21.4). */
+KVC_API kvc_status kvc_alloc_publish(kvc_alloc *alloc, int32_t seq, const int32_t *tokens, int32_t n_tokens,
+                                     uint64_t salt);
+/* A new sequence mapping the longest run of published full blocks whose
+ * identities match tokens (same salt, exact token ids: a hash collision is a
+ * miss); *hit_tokens = positions covered. */
+KVC_API kvc_status kvc_alloc_match(kvc_alloc *alloc, const int32_t *tokens, int32_t n_tokens, uint64_t salt,
+                                   int32_t *seq, int32_t *hit_tokens);
+KVC_API kvc_status kvc_alloc_seq_info(const kvc_alloc *alloc, int32_t seq, int64_t *len, int32_t *n_blocks);
+/* Host block-table rows (int32 [n][max_blocks], -1 padded) and lengths of the given sequences. */
+KVC_API kvc_status kvc_alloc_block_tables(const kvc_alloc *alloc, const int32_t *seqs, int32_t n, int32_t max_blocks,
+                                          int32_t *table, int32_t *lens);
+KVC_API kvc_status kvc_alloc_counts(const kvc_alloc *alloc, int64_t *n_free, int64_t *n_used, int64_t *n_cached);
+/* Reference count of a block, or -1 for an id outside the pool. */
+KVC_API int32_t kvc_alloc_refcount(const kvc_alloc *alloc, int32_t block);
+
+/* Device copy of whole blocks, every layer, keys and values (the copy of
+ * copy-on-write, "KV cache: ..." 21.5).  pairs: device int32 [n][2] (src, dst).
+ * An id outside the pool is skipped and recorded (KVC_ERR_BAD_BLOCK via
+ * kvc_pool_sync_status).  Errors: KVC_ERR_ARG, KVC_ERR_CUDA. */
+KVC_API kvc_status kvc_copy_blocks(kvc_pool *pool, const int32_t *pairs, int32_t n, kvc_stream_t stream);
+
 /* ------------------------------------------------------------------ host utilities */
 
 /* Ideal KV payload in bytes

@@ -44,7 +44,10 @@ class kvc_pool_desc(ctypes.Structure):
 
 EXPORTS = ["kvc_pool_create", "kvc_pool_destroy", "kvc_pool_info", "kvc_pool_set_scales", "kvc_calibrate_fp8",
            "kvc_append", "kvc_write_tokens", "kvc_decode_attn", "kvc_prefill_attn", "kvc_pool_reserve",
-           "kvc_bytes", "kvc_pool_sync_status", "kvc_status_str", "kvc_launch_count", "kvc_decode_attn_noalloc", "kvc_decode_step"]
+           "kvc_bytes", "kvc_pool_sync_status", "kvc_status_str", "kvc_launch_count", "kvc_decode_attn_noalloc", "kvc_decode_step",
+           "kvc_alloc_create", "kvc_alloc_destroy", "kvc_alloc_new_seq", "kvc_alloc_fork", "kvc_alloc_reserve",
+           "kvc_alloc_commit", "kvc_alloc_release", "kvc_alloc_publish", "kvc_alloc_match", "kvc_alloc_seq_info",
+           "kvc_alloc_block_tables", "kvc_alloc_counts", "kvc_alloc_refcount", "kvc_copy_blocks"]
 
 
 def load(path: str = LIB_PATH):
@@ -77,6 +80,20 @@ def load(path: str = LIB_PATH):
     L.kvc_pool_sync_status.restype, L.kvc_pool_sync_status.argtypes = st, [vp, vp]
     L.kvc_status_str.restype, L.kvc_status_str.argtypes = ctypes.c_char_p, [st]
     L.kvc_launch_count.restype, L.kvc_launch_count.argtypes = u64, []
+    L.kvc_alloc_create.restype, L.kvc_alloc_create.argtypes = st, [i64, i32, vp, i32, ctypes.POINTER(vp)]
+    L.kvc_alloc_destroy.restype, L.kvc_alloc_destroy.argtypes = None, [vp]
+    L.kvc_alloc_new_seq.restype, L.kvc_alloc_new_seq.argtypes = st, [vp, vp]
+    L.kvc_alloc_fork.restype, L.kvc_alloc_fork.argtypes = st, [vp, i32, i32, vp]
+    L.kvc_alloc_reserve.restype, L.kvc_alloc_reserve.argtypes = st, [vp, i32, i32, vp, i32, vp]
+    L.kvc_alloc_commit.restype, L.kvc_alloc_commit.argtypes = st, [vp, i32, i32]
+    L.kvc_alloc_release.restype, L.kvc_alloc_release.argtypes = st, [vp, i32]
+    L.kvc_alloc_publish.restype, L.kvc_alloc_publish.argtypes = st, [vp, i32, vp, i32, u64]
+    L.kvc_alloc_match.restype, L.kvc_alloc_match.argtypes = st, [vp, vp, i32, u64, vp, vp]
+    L.kvc_alloc_seq_info.restype, L.kvc_alloc_seq_info.argtypes = st, [vp, i32, vp, vp]
+    L.kvc_alloc_block_tables.restype, L.kvc_alloc_block_tables.argtypes = st, [vp, vp, i32, i32, vp, vp]
+    L.kvc_alloc_counts.restype, L.kvc_alloc_counts.argtypes = st, [vp, vp, vp, vp]
+    L.kvc_alloc_refcount.restype, L.kvc_alloc_refcount.argtypes = i32, [vp, i32]
+    L.kvc_copy_blocks.restype, L.kvc_copy_blocks.argtypes = st, [vp, vp, i32, vp]
     _lib = L
     return L
 
@@ -279,3 +296,101 @@ def kvc_status_str(status: int) -> str:
 
 def kvc_launch_count() -> int:
     return int(load().kvc_launch_count())
+
+
+# ---------------------------------------------------------------------- block allocator (host)
+class Allocator:
+    """Owning handle of a kvc_alloc: the host block allocator (free queue,
+    reference counts, copy-on-write, retention, prefix lookup).  Methods map
+    one to one onto the kvc_alloc_* calls."""
+
+    def __init__(self, num_blocks, block_size, free_order=None, retain_cached=False):
+        import numpy as np
+        L = load()
+        self._np = np
+        self.block_size = block_size
+        out = ctypes.c_void_p()
+        fo = None if free_order is None else np.ascontiguousarray(free_order, dtype=np.int32)
+        _check(L.kvc_alloc_create(num_blocks, block_size, None if fo is None else fo.ctypes.data,
+                                  int(bool(retain_cached)), ctypes.byref(out)), "kvc_alloc_create")
+        self.handle = out.value
+
+    def close(self):
+        if self.handle:
+            load().kvc_alloc_destroy(ctypes.c_void_p(self.handle))
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _h(self):
+        return ctypes.c_void_p(self.handle)
+
+    def new_seq(self) -> int:
+        s = ctypes.c_int32()
+        _check(load().kvc_alloc_new_seq(self._h(), ctypes.byref(s)), "kvc_alloc_new_seq")
+        return s.value
+
+    def fork(self, src, n_tokens) -> int:
+        s = ctypes.c_int32()
+        _check(load().kvc_alloc_fork(self._h(), src, n_tokens, ctypes.byref(s)), "kvc_alloc_fork")
+        return s.value
+
+    def reserve(self, seq, n_tokens):
+        """Returns the copy-on-write pairs [(old, new)] the caller must copy before writing."""
+        pairs = (ctypes.c_int32 * 2)()
+        n = ctypes.c_int32()
+        _check(load().kvc_alloc_reserve(self._h(), seq, n_tokens, pairs, 1, ctypes.byref(n)), "kvc_alloc_reserve")
+        return [(pairs[0], pairs[1])] if n.value else []
+
+    def commit(self, seq, n_tokens):
+        _check(load().kvc_alloc_commit(self._h(), seq, n_tokens), "kvc_alloc_commit")
+
+    def release(self, seq):
+        _check(load().kvc_alloc_release(self._h(), seq), "kvc_alloc_release")
+
+    def publish(self, seq, tokens, salt=0):
+        t = self._np.ascontiguousarray(tokens, dtype=self._np.int32)
+        _check(load().kvc_alloc_publish(self._h(), seq, t.ctypes.data if t.size else None, t.size, salt),
+               "kvc_alloc_publish")
+
+    def match(self, tokens, salt=0):
+        """(new sequence id, positions covered by matched full blocks)."""
+        t = self._np.ascontiguousarray(tokens, dtype=self._np.int32)
+        s, hit = ctypes.c_int32(), ctypes.c_int32()
+        _check(load().kvc_alloc_match(self._h(), t.ctypes.data if t.size else None, t.size, salt, ctypes.byref(s),
+                                      ctypes.byref(hit)), "kvc_alloc_match")
+        return s.value, hit.value
+
+    def seq_info(self, seq):
+        ln, nb = ctypes.c_int64(), ctypes.c_int32()
+        _check(load().kvc_alloc_seq_info(self._h(), seq, ctypes.byref(ln), ctypes.byref(nb)), "kvc_alloc_seq_info")
+        return ln.value, nb.value
+
+    def block_tables(self, seqs, max_blocks):
+        np = self._np
+        s = np.ascontiguousarray(seqs, dtype=np.int32)
+        table = np.empty((len(s), max_blocks), dtype=np.int32)
+        lens = np.empty(len(s), dtype=np.int32)
+        _check(load().kvc_alloc_block_tables(self._h(), s.ctypes.data, len(s), max_blocks, table.ctypes.data,
+                                             lens.ctypes.data), "kvc_alloc_block_tables")
+        return table, lens
+
+    def counts(self):
+        f, u, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(load().kvc_alloc_counts(self._h(), ctypes.byref(f), ctypes.byref(u), ctypes.byref(c)),
+               "kvc_alloc_counts")
+        return {"free": f.value, "used": u.value, "cached": c.value}
+
+    def refcount(self, block) -> int:
+        return int(load().kvc_alloc_refcount(self._h(), block))
+
+
+def kvc_copy_blocks(pool, pairs, stream=None):
+    """pairs: CUDA int32 [n][2] (src, dst): copy whole blocks, every layer."""
+    n = pairs.shape[0]
+    _check(load().kvc_copy_blocks(_h(pool), _dev(pairs, torch.int32, "pairs") if n else None, n, _stream(stream)),
+           "kvc_copy_blocks")

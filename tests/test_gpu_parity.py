@@ -441,3 +441,97 @@ def test_fused_step_equals_append_then_decode(kvc, case):
         check_attention(res[1][1], res[1][2], ref["out"], ref["lse"], w.dtype, f"fused {case}")
     finally:
         os.environ.pop("KVC_SPLIT_CHUNK", None)
+
+
+def test_copy_blocks_every_layer(kvc):
+    """kvc_copy_blocks copies a block's keys and values in every layer, bit for bit."""
+    N, L, H, d = 12, 3, 2, 128
+    pool = kvc.kvc_pool_create(N, 16, L, H, d, kvc.KVC_BF16)
+    try:
+        view = pool.bytes_view()
+        src = torch.from_numpy(synth.u64(9, 1, view.numel() // 8).view(np.uint8).copy()).cuda()
+        view.copy_(src)
+        pairs = [(3, 7), (0, 11), (5, 5)]
+        kvc.kvc_copy_blocks(pool, dev_i32(np.array(pairs, np.int32)))
+        torch.cuda.synchronize()
+        assert kvc.kvc_pool_sync_status(pool) == kvc.KVC_OK
+        ref = src.cpu().numpy().copy()
+        blk = 2 * H * 16 * d * 2
+        per_layer = N * blk
+        for l in range(L):
+            for s, t in pairs:
+                ref[l * per_layer + t * blk:l * per_layer + (t + 1) * blk] = \
+                    ref[l * per_layer + s * blk:l * per_layer + (s + 1) * blk]
+        assert np.array_equal(view.cpu().numpy(), ref)
+        kvc.kvc_copy_blocks(pool, dev_i32(np.array([[1, N + 4]], np.int32)))     # outside the pool: skipped
+        assert kvc.kvc_pool_sync_status(pool) == kvc.KVC_ERR_BAD_BLOCK
+    finally:
+        pool.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_allocator_copy_on_write_decode(kvc, dtype):
+    """Tables from the host allocator drive the kernels: B forks A inside a
+    partly filled block; before B's append the allocator maps a fresh block and
+    kvc_copy_blocks copies the shared one; both then decode against the oracle."""
+    L, H_Q, H, d, bs, N = 2, 16, 4, 128, 16, 32
+    alloc = kvc.Allocator(N, bs)
+    A = alloc.new_seq()
+    alloc.reserve(A, 40)
+    w = synth.make_workload("custom", B=2, H_Q=H_Q, H_KV=H, d_h=d, lens=[40, 40], L=L, dtype=dtype, seed=11)
+    pool = kvc.kvc_pool_create(N, bs, L, H, d, kvc.KVC_FP8_E4M3 if dtype == "fp8" else kvc.KVC_BF16)
+    try:
+        pool.bytes_view().fill_(0x11)
+        s = 1 if dtype == "fp8" else 2
+        img = oracle.PoolImage(N, bs, L, H, d, s, fill=0x11)
+        ctx = {l: (w.ctx_tokens(l, 0, 0, 0, 40), w.ctx_tokens(l, 1, 0, 0, 40)) for l in range(L)}
+        tA, _ = alloc.block_tables([A], 3)
+        for l in range(L):
+            k, v = ctx[l]
+            if dtype == "fp8":
+                kvc.kvc_calibrate_fp8(pool, l, dev_bits(k), dev_bits(v))
+                img.scales[l] = np.stack([oracle.fp8_scales(k), oracle.fp8_scales(v)])
+            kvc.kvc_write_tokens(pool, l, dev_i32(tA), dev_i32([0]), dev_i32([0, 40]), dev_bits(k), dev_bits(v))
+            img.write_tokens(l, tA, np.array([0], np.int32), np.array([0, 40], np.int64), k, v)
+        alloc.commit(A, 40)
+        B = alloc.fork(A, 40)                       # block 2 holds 8 of 16 positions: shared, partly filled
+        cow = alloc.reserve(B, 1)
+        assert len(cow) == 1 and cow[0][0] == int(tA[0, 2])
+        kvc.kvc_copy_blocks(pool, dev_i32(np.array(cow, np.int32)))
+        blk = img.bytes.size // (L * N)
+        for l in range(L):
+            o, n = cow[0]
+            base = l * N * blk
+            img.bytes[base + n * blk:base + (n + 1) * blk] = img.bytes[base + o * blk:base + (o + 1) * blk]
+        assert alloc.reserve(A, 1) == []           # A's copy of the block is private again
+        table, lens = alloc.block_tables([A, B], 3)
+        assert table[0, 2] != table[1, 2] and lens.tolist() == [40, 40]
+        bt, lp = dev_i32(table), dev_i32(lens)
+        for l in range(L):
+            q = w.q(l)
+            kn, vn = w.kv_new(l, 0), w.kv_new(l, 1)
+            out = torch.empty((2, H_Q, d), device="cuda")
+            lse = torch.empty((2, H_Q), device="cuda")
+            kvc.kvc_decode_step(pool, l, dev_bits(q), bt, lp, dev_bits(kn), dev_bits(vn), out, lse, scale=w.scale)
+            torch.cuda.synchronize()
+            assert kvc.kvc_pool_sync_status(pool) == kvc.KVC_OK
+            img.append(l, table, lens, kn, vn)
+            k, v = ctx[l]
+            if dtype == "fp8":
+                sk, sv = img.scales[l]
+                kq, vq = oracle.quantize_e4m3(k, sk), oracle.quantize_e4m3(v, sv)
+                nk, nv = oracle.quantize_e4m3(kn, sk), oracle.quantize_e4m3(vn, sv)
+                scales = img.scales[l]
+            else:
+                kq, vq, nk, nv, scales = k, v, kn, vn, None
+            K = np.concatenate([kq, nk[0:1], kq, nk[1:2]])
+            V = np.concatenate([vq, nv[0:1], vq, nv[1:2]])
+            ro, rl = oracle.decode(q, K, V, np.array([0, 41, 82]), np.array([41, 41]), H, scales=scales, scale=w.scale)
+            check_attention(out, lse, ro, rl, dtype, f"copy-on-write layer {l}")
+        alloc.commit(A, 1)
+        alloc.commit(B, 1)
+        n, first = first_mismatch(pool.bytes_view().cpu().numpy(), img.bytes)
+        assert n == 0, f"{n} pool bytes differ, first at {first}"
+    finally:
+        pool.close()
+        alloc.close()
