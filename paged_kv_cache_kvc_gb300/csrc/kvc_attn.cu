@@ -1,4 +1,5 @@
 // Decode / prefill attention entry points, split sizing and the split merge.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 
@@ -10,15 +11,16 @@ namespace kvc {
 //   M = max_s m_s,  L = sum_s 2^(m_s - M) l_s,  out = sum_s 2^(m_s - M) o_s / L,
 //   lse = (M + log2 L) ln 2.
 // Sequences with a single split were finished by the attention kernel.
+// grid (H_Q, query positions): one CTA per output row.
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int D)
 {
-    const int hq = blockIdx.x, b = blockIdx.y;
-    int len = seq_len(p, b);
+    const int hq = blockIdx.x, pos = blockIdx.y;
+    int len = seq_len(p, pos / p.ppu);
     if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) len = 0;
     const int nblk = (len + kBS - 1) / kBS;
     const int ns = (nblk + p.chunk - 1) / p.chunk;
     if (ns <= 1) return;
-    const size_t bq = static_cast<size_t>(b) * p.H_Q + hq;
+    const size_t bq = static_cast<size_t>(pos) * p.H_Q + hq;
     const float2 *ml = p.part_ml + bq * p.max_splits;
     const float *po = p.part_o + bq * p.max_splits * D;
     float M = -INFINITY;
@@ -88,17 +90,17 @@ kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel
 {
     kvc_pool *pool = const_cast<kvc_pool *>(cpool);
     if (!k.fn || k.ctas_per_sm <= 0) return KVC_ERR_CUDA;
-    choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits, n_tiles(p.g));
+    choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits, n_tiles(p.ppu * p.g));
     if (p.max_splits > 65535) return KVC_ERR_UNSUPPORTED;
     if (p.max_splits > 1) {
-        kvc_status st = ensure_workspace(pool, workspace_bytes(p.B, p.H_Q, p.max_splits, pool->D));
+        kvc_status st = ensure_workspace(pool, workspace_bytes(p.n_pos, p.H_Q, p.max_splits, pool->D));
         if (st != KVC_OK) return st;
-        const size_t n = static_cast<size_t>(p.B) * p.H_Q * p.max_splits;
+        const size_t n = static_cast<size_t>(p.n_pos) * p.H_Q * p.max_splits;
         p.part_o = static_cast<float *>(pool->ws);
         p.part_ml = reinterpret_cast<float2 *>(static_cast<float *>(pool->ws) + n * pool->D);
         // the last split CTA merges its group in the kernel when that is a small job (g * splits
         // partial rows); otherwise one merge CTA per (sequence, query head) does it afterwards
-        p.counters = (p.g * p.max_splits <= 64) ? reinterpret_cast<uint32_t *>(p.part_ml + n) : nullptr;
+        p.counters = (p.ppu * p.g * p.max_splits <= 64) ? reinterpret_cast<uint32_t *>(p.part_ml + n) : nullptr;
     } else {
         p.part_o = nullptr;
         p.part_ml = nullptr;
@@ -110,7 +112,7 @@ kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (p.max_splits > 1 && !p.counters) {
-        merge_kernel<<<dim3(p.H_Q, p.B), 128, 0, stream>>>(p, pool->D);
+        merge_kernel<<<dim3(p.H_Q, p.n_pos), 128, 0, stream>>>(p, pool->D);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_status(e);
         g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -177,6 +179,8 @@ extern "C" kvc_status kvc_decode_attn(kvc_pool *pool, int32_t layer, const void 
     p.bt_stride = max_blocks;
     p.len_base = 0;
     p.B = B;
+    p.ppu = 1;
+    p.n_pos = B;
     return dispatch(pool, p, static_cast<cudaStream_t>(stream));
 }
 
@@ -197,6 +201,8 @@ extern "C" kvc_status kvc_decode_step(kvc_pool *pool, int32_t layer, const void 
     p.bt_stride = max_blocks;
     p.len_base = 0;
     p.B = B;
+    p.ppu = 1;
+    p.n_pos = B;
     p.k_new = static_cast<const uint16_t *>(k_new);
     p.v_new = static_cast<const uint16_t *>(v_new);
     p.pool = pool->base;
@@ -214,11 +220,18 @@ extern "C" kvc_status kvc_prefill_attn(kvc_pool *pool, int32_t layer, const void
     if (static_cast<int64_t>(q_start) + n_q > static_cast<int64_t>(max_blocks) * kBS) return KVC_ERR_RANGE;
     DecodeParams p{};
     fill_common(p, pool, layer, q, num_q_heads, block_table_row, max_blocks, out, lse, scale);
-    // query i is a decode over the same row with length q_start + i + 1
+    // query i reads q_start + i + 1 positions of the same row; a unit (CTA
+    // column group) takes ppu consecutive queries x the g heads of a KV head,
+    // so each staged block serves ppu queries.  KVC_PREFILL_PPU overrides.
     p.lens = nullptr;
     p.bt_stride = 0;
     p.len_base = q_start;
-    p.B = n_q;
+    int ppu = 32 / p.g;     // measured on GB300 (600-query chunk, g = 4): 1 -> 346 us, 4 -> 143 us, 8 -> 135 us
+    if (const char *e = std::getenv("KVC_PREFILL_PPU")) ppu = std::atoi(e);
+    ppu = std::max(1, std::min(ppu, 32 / p.g));
+    p.ppu = ppu;
+    p.n_pos = n_q;
+    p.B = (n_q + ppu - 1) / ppu;
     return dispatch(pool, p, static_cast<cudaStream_t>(stream));
 }
 
@@ -237,7 +250,7 @@ namespace kvc {
 // Launch the split merge on its own (partials already written by the decode kernel).
 kvc_status launch_split_merge(const DecodeParams &p, int D, cudaStream_t stream)
 {
-    merge_kernel<<<dim3(p.H_Q, p.B), 128, 0, stream>>>(p, D);
+    merge_kernel<<<dim3(p.H_Q, p.n_pos), 128, 0, stream>>>(p, D);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);

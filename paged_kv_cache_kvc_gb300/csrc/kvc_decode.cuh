@@ -76,11 +76,13 @@ __device__ __forceinline__ uint32_t swz(int row, int ch)
     return static_cast<uint32_t>((band * 2 * kBS + row) * 128 + ((c ^ (row & 7)) << 4));
 }
 
-// Positions attended by sequence b: lens[b] (+1 when the step's token is appended
-// in the same launch), or len_base + b + 1 for a prefill chunk's query b.
+// Positions attended by unit b: lens[b] (+1 when the step's token is appended
+// in the same launch); for a prefill chunk, whose unit b holds query positions
+// b*ppu .. b*ppu+ppu-1 and query i reads len_base + i + 1 positions, the
+// longest of its queries.
 __device__ __forceinline__ int seq_len(const DecodeParams &p, int b)
 {
-    if (!p.lens) return p.len_base + b + 1;
+    if (!p.lens) return p.len_base + min(p.n_pos, (b + 1) * p.ppu);
     return __ldg(p.lens + b) + (p.k_new ? 1 : 0);
 }
 
@@ -133,6 +135,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, tg = lane & 3;
     const int hq0 = h * p.g;
+    // query columns of the unit: ppu consecutive positions x the g heads of KV head h
+    const int rows = p.ppu * p.g;
+    auto col_pos = [&](int qi) { return b * p.ppu + qi / p.g; };
+    auto col_real = [&](int qi) { return qi < rows && col_pos(qi) < p.n_pos; };
+    auto col_orow = [&](int qi) {   // row of the column in q / out ([position][H_Q])
+        return static_cast<size_t>(col_pos(qi)) * p.H_Q + hq0 + qi % p.g;
+    };
 
     int len = seq_len(p, b);
     if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) {
@@ -142,9 +151,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int nblk = (len + kBS - 1) / kBS;
     if (nblk == 0) {   // empty sequence: zero output, lse = -inf
         if (split == 0) {
-            for (int i = threadIdx.x; i < p.g * D; i += kThreads)
-                p.out[(static_cast<size_t>(b) * p.H_Q + hq0) * D + i] = 0.f;
-            if (p.lse && threadIdx.x < p.g) p.lse[static_cast<size_t>(b) * p.H_Q + hq0 + threadIdx.x] = -INFINITY;
+            for (int i = threadIdx.x; i < rows * D; i += kThreads)
+                if (col_real(i / D)) p.out[col_orow(i / D) * D + i % D] = 0.f;
+            if (p.lse && threadIdx.x < rows && col_real(threadIdx.x)) p.lse[col_orow(threadIdx.x)] = -INFINITY;
         }
         return;
     }
@@ -197,8 +206,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         const int qi = 8 * j + gq;
-        const bool real = qi < p.g;
-        const uint16_t *qrow = p.q + (static_cast<size_t>(b) * p.H_Q + hq0 + (real ? qi : 0)) * D;
+        const bool real = col_real(qi);
+        const uint16_t *qrow = p.q + (real ? col_orow(qi) : static_cast<size_t>(0)) * D;
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
             if constexpr (!FP8) {
@@ -214,6 +223,16 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             }
         }
     }
+
+    // positions each of this thread's two columns per n-tile may read (0 for padding columns)
+    int clen[NT][2];
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int qi = 8 * jn + 2 * tg + c;
+            clen[jn][c] = !col_real(qi) ? 0 : (p.lens ? len : p.len_base + col_pos(qi) + 1);
+        }
 
     float m_run[NT][2], l_run[NT][2];
     float oacc[C::MT][NT][4];
@@ -291,12 +310,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 
             // ---- online softmax (log2 domain); column = query head, rows = tokens gq, gq+8
             uint32_t pb[NT][2], pl[NT][2];
+            const int tok0 = (blk0 + warp + kWarps * j) * kBS;
 #pragma unroll
             for (int jn = 0; jn < NT; ++jn) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const int tok = gq + ((c >> 1) << 3);
-                    sc[jn][c] = tok < valid ? sc[jn][c] * p.scale_log2 : -INFINITY;
+                    const int tok = tok0 + gq + ((c >> 1) << 3);
+                    sc[jn][c] = tok < clen[jn][c & 1] ? sc[jn][c] * p.scale_log2 : -INFINITY;
                 }
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -304,9 +324,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
                     bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
                     bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
-                    const float mn = fmaxf(m_run[jn][c], bm);    // finite: every block has a valid token
-                    const float alpha = fast_exp2(m_run[jn][c] - mn);
-                    const float p0 = fast_exp2(sc[jn][c] - mn), p1 = fast_exp2(sc[jn][c + 2] - mn);
+                    const float mn = fmaxf(m_run[jn][c], bm);
+                    const float mref = mn == -INFINITY ? 0.f : mn;   // a column with nothing visible yet
+                    const float alpha = fast_exp2(m_run[jn][c] - mref);
+                    const float p0 = fast_exp2(sc[jn][c] - mref), p1 = fast_exp2(sc[jn][c + 2] - mref);
                     m_run[jn][c] = mn;
                     l_run[jn][c] = l_run[jn][c] * alpha + p0 + p1;
                     sc[jn][c] = p0;
@@ -428,20 +449,22 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     __syncthreads();
 
     const int ns = (nblk + p.chunk - 1) / p.chunk;
-    for (int i = threadIdx.x; i < p.g * D; i += kThreads) {
+    for (int i = threadIdx.x; i < rows * D; i += kThreads) {
         const int qi = i / D, d = i - qi * D;
+        if (!col_real(qi)) continue;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * QW + qi]);
+        const float Mref = M == -INFINITY ? 0.f : M;     // no visible position in this CTA's blocks
         float L = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float e = fast_exp2(cm[w * QW + qi] - M);   // warps without blocks: exp2(-inf) = 0
+            const float e = fast_exp2(cm[w * QW + qi] - Mref);   // warps without blocks: exp2(-inf) = 0
             L += e * cl[w * QW + qi];
             O += e * co[(w * QW + qi) * D + d];
         }
         if constexpr (FP8) O *= __ldg(p.s_v + static_cast<size_t>(h) * D + d);
-        const size_t bq = static_cast<size_t>(b) * p.H_Q + hq0 + qi;
+        const size_t bq = col_orow(qi);
         if (ns == 1) {
             p.out[bq * D + d] = O / L;
             if (d == 0 && p.lse) p.lse[bq] = (M + log2f(L)) * kLn2;
@@ -466,9 +489,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     __syncthreads();
     if (!last_flag) return;
     __threadfence();
-    for (int i = threadIdx.x; i < p.g * D; i += kThreads) {
+    for (int i = threadIdx.x; i < rows * D; i += kThreads) {
         const int qi = i / D, d = i - qi * D;
-        const size_t bq = static_cast<size_t>(b) * p.H_Q + hq0 + qi;
+        if (!col_real(qi)) continue;
+        const size_t bq = col_orow(qi);
         const float2 *ml = p.part_ml + bq * p.max_splits;
         const float *po = p.part_o + bq * p.max_splits * D + d;
         float M = -INFINITY;

@@ -21,7 +21,7 @@ kvc_status launch_decode_bf16(const kvc_pool *pool, DecodeParams &p, cudaStream_
         const char *e = std::getenv("KVC_PSPLIT");
         return !(e && e[0] == '0');
     }();
-    const int NT = p.g <= 8 ? 1 : (p.g <= 16 ? 2 : 4);
+    const int NT = n_tiles(p.ppu * p.g);
     DecodeKernel k;
     switch (pool->D) {
     case 64: k = pick_bf16<64>(NT, psplit); break;

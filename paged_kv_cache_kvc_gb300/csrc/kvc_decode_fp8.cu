@@ -5,7 +5,7 @@ namespace kvc {
 
 kvc_status launch_decode_fp8(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream)
 {
-    const int NT = p.g <= 8 ? 1 : (p.g <= 16 ? 2 : 4);
+    const int NT = n_tiles(p.ppu * p.g);
     if (pool->D != 128) return KVC_ERR_UNSUPPORTED;
     DecodeKernel k = NT == 1 ? decode_instance<128, 1, true, false>()
                    : NT == 2 ? decode_instance<128, 2, true, false>()

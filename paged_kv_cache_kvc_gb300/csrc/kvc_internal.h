@@ -39,7 +39,9 @@ struct DecodeParams {
     int64_t bt_stride;       // elements between table rows (0: every row is the same row)
     int32_t max_blocks;
     int32_t len_base;
-    int32_t B, H_Q, H_KV, g;
+    int32_t B, H_Q, H_KV, g;  // B = units (grid z)
+    int32_t ppu;             // query positions per unit: 1 for decode, a tile of a prefill chunk
+    int32_t n_pos;           // query positions in all (decode: B; prefill: n_q)
     int32_t layer;
     int32_t chunk;           // logical blocks per split (multiple of 4)
     int32_t max_splits;

@@ -74,6 +74,8 @@ extern "C" kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, con
     p.max_blocks = max_blocks;
     p.len_base = 0;
     p.B = B;
+    p.ppu = 1;
+    p.n_pos = B;
     p.H_Q = num_q_heads;
     p.H_KV = pool->H_KV;
     p.g = num_q_heads / pool->H_KV;

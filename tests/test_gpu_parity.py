@@ -535,3 +535,39 @@ def test_allocator_copy_on_write_decode(kvc, dtype):
     finally:
         pool.close()
         alloc.close()
+
+
+@pytest.mark.parametrize("ppu", ["1", "3", "4", "8"])
+@pytest.mark.parametrize("H_KV,dtype", [(8, "bf16"), (2, "bf16"), (32, "bf16"), (8, "fp8")])
+def test_prefill_tiles(kvc, ppu, H_KV, dtype):
+    """Causal prefill chunks whose CTAs serve several query positions (tail tile
+    shorter, chunks starting inside a block) against the oracle."""
+    H_Q, d = 32, 128
+    if int(ppu) * (H_Q // H_KV) > 32:
+        pytest.skip("more than 32 query columns per unit")
+    os.environ["KVC_PREFILL_PPU"] = ppu
+    try:
+        for q_start, n_q in ((0, 37), (45, 23), (200, 61)):
+            total = q_start + n_q
+            w = _custom(B=1, H_Q=H_Q, H_KV=H_KV, d_h=d, lens=[total], dtype=dtype, seed=q_start + n_q)
+            ld = layer_data(w, 0, with_step=False)
+            g = GpuCase(kvc, w)
+            try:
+                g.load_context(0, ld)
+                qc = synth.normal_bf16(7, n_q, n_q * H_Q * d).reshape(n_q, H_Q, d)
+                out = torch.empty((n_q, H_Q, d), device="cuda")
+                lse = torch.empty((n_q, H_Q), device="cuda")
+                kvc.kvc_prefill_attn(g.pool, 0, dev_bits(qc), g.bt[0], q_start, out, lse, scale=w.scale)
+                torch.cuda.synchronize()
+                assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+                sc = None
+                K, V = ld.k_ctx, ld.v_ctx
+                if dtype == "fp8":
+                    sc = g.pool.scales_view()[0].cpu().numpy()
+                    K, V = oracle.quantize_e4m3(K, sc[0]), oracle.quantize_e4m3(V, sc[1])
+                ro, rl = oracle.prefill(qc, K, V, q_start, H_KV, scales=sc, scale=w.scale)
+                check_attention(out, lse, ro, rl, dtype, f"prefill ppu={ppu} q_start={q_start} n_q={n_q}")
+            finally:
+                g.close()
+    finally:
+        os.environ.pop("KVC_PREFILL_PPU", None)
