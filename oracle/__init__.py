@@ -34,6 +34,7 @@ _SRC = os.path.join(_HERE, "kvc_oracle.c")
 LIB_PATH = os.path.join(_HERE, "_build", "libkvc_oracle.so")
 
 OK, ERR_ARG, ERR_BAD_BLOCK, ERR_RANGE = 0, 1, 3, 4
+KIND_E4M3, KIND_BF16, KIND_INT4 = 1, 2, 3       # stored-scalar kinds (same codes as the C file)
 
 _lib = None
 
@@ -71,6 +72,14 @@ def lib():
         L.orc_fp8_scales.argtypes = [vp, i64, i32, i32, vp]
         L.orc_quantize_e4m3.restype = None
         L.orc_quantize_e4m3.argtypes = [vp, i64, i32, i32, vp, vp]
+        L.orc_quantize_int4.restype = None
+        L.orc_quantize_int4.argtypes = [vp, i64, i32, i32, vp, vp]
+        L.orc_int4_encode.restype = ctypes.c_uint8
+        L.orc_int4_encode.argtypes = [ctypes.c_float]
+        L.orc_int4_decode.restype = dbl
+        L.orc_int4_decode.argtypes = [ctypes.c_uint8]
+        L.orc_int4_scales.restype = None
+        L.orc_int4_scales.argtypes = [vp, i64, i32, i32, vp]
         L.orc_locate.restype = ctypes.c_int
         L.orc_locate.argtypes = [vp, i32, i64, i32, i64, vp, vp]
         L.orc_pool_offset.restype = u64
@@ -141,6 +150,39 @@ def quantize_e4m3(x_bits: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return out
 
 
+def int4_encode(y: float) -> int:
+    return int(lib().orc_int4_encode(float(y)))
+
+
+def int4_decode(nibble: int) -> float:
+    return float(lib().orc_int4_decode(int(nibble)))
+
+
+def int4_scales(x_bits: np.ndarray) -> np.ndarray:
+    """x_bits: bf16 [n_tokens][H_KV][d_h] -> fp32 [H_KV][d_h] = absmax / 7."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    n, H, d = x_bits.shape
+    out = np.empty((H, d), dtype=np.float32)
+    lib().orc_int4_scales(_p(x_bits), n, H, d, _p(out))
+    return out
+
+
+def quantize_int4(x_bits: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """bf16 [n][H_KV][d_h] -> int4 nibbles (one per byte) under fp32 scales [H_KV][d_h]."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    n, H, d = x_bits.shape
+    sc = np.ascontiguousarray(scales, dtype=np.float32).reshape(H, d)
+    out = np.empty((n, H, d), dtype=np.uint8)
+    lib().orc_quantize_int4(_p(x_bits), n, H, d, _p(sc), _p(out))
+    return out
+
+
+def kind_of(elem) -> int:
+    """2 / 'bf16' -> bf16, 1 / 'fp8' -> e4m3, 'int4' -> int4."""
+    return {2: KIND_BF16, "bf16": KIND_BF16, 1: KIND_E4M3, "fp8": KIND_E4M3, "e4m3": KIND_E4M3,
+            "int4": KIND_INT4, KIND_INT4: KIND_INT4}[elem]
+
+
 # ------------------------------------------------------------------ tables
 def locate(bt_row: np.ndarray, t: int, bs: int, num_blocks: int):
     """(status, physical block, slot) of logical position t."""
@@ -155,13 +197,16 @@ class PoolImage:
     """The oracle's own model of the pool bytes (same documented layout)."""
 
     def __init__(self, num_blocks, block_size, L, H_KV, d_h, elem_bytes, fill: int = 0):
-        self.N, self.bs, self.L, self.H_KV, self.d_h, self.s = num_blocks, block_size, L, H_KV, d_h, elem_bytes
-        nbytes = L * num_blocks * 2 * H_KV * block_size * d_h * elem_bytes
-        self.bytes = np.full(nbytes, fill, dtype=np.uint8)
+        """elem_bytes: 2 (bf16), 1 (e4m3) or 'int4' (two elements per byte)."""
+        self.kind = kind_of(elem_bytes)
+        self.N, self.bs, self.L, self.H_KV, self.d_h = num_blocks, block_size, L, H_KV, d_h
+        self.s = 2 if self.kind == KIND_BF16 else 1             # bytes per element in logical lists
+        elems = L * num_blocks * 2 * H_KV * block_size * d_h
+        self.bytes = np.full(elems // 2 if self.kind == KIND_INT4 else elems * self.s, fill, dtype=np.uint8)
         self.scales = np.ones((L, 2, H_KV, d_h), dtype=np.float32)   # e4m3 pools only
 
     def layer_view(self, layer: int) -> np.ndarray:
-        n = self.N * 2 * self.H_KV * self.bs * self.d_h * self.s
+        n = self.bytes.size // self.L
         return self.bytes[layer * n:(layer + 1) * n]
 
     def offset(self, layer, phys, kv, h, slot, c) -> int:
@@ -175,7 +220,7 @@ class PoolImage:
         k = np.ascontiguousarray(k_bits, dtype=np.uint16)
         v = np.ascontiguousarray(v_bits, dtype=np.uint16)
         sc = np.ascontiguousarray(self.scales[layer])
-        return int(lib().orc_write_tokens(_p(self.bytes), self.N, self.bs, self.H_KV, self.d_h, self.s,
+        return int(lib().orc_write_tokens(_p(self.bytes), self.N, self.bs, self.H_KV, self.d_h, self.kind,
                                           layer, _p(bt), mb, B, _p(sp), _p(cu), _p(k), _p(v), _p(sc)))
 
     def append(self, layer, block_tables, lens_pre, k_new, v_new) -> int:
@@ -192,13 +237,13 @@ class PoolImage:
         dt = np.uint16 if self.s == 2 else np.uint8
         k = np.empty((length, self.H_KV, self.d_h), dtype=dt)
         v = np.empty_like(k)
-        st = lib().orc_gather(_p(self.bytes), self.N, self.bs, self.H_KV, self.d_h, self.s, layer,
+        st = lib().orc_gather(_p(self.bytes), self.N, self.bs, self.H_KV, self.d_h, self.kind, layer,
                               _p(bt_row), len(bt_row), length, _p(k), _p(v))
         return int(st), k, v
 
 
 # ------------------------------------------------------------------ attention
-def decode(q_bits, K, V, cu, n, H_KV, scales=None, scale=None):
+def decode(q_bits, K, V, cu, n, H_KV, scales=None, scale=None, kind=None):
     """Decode attention over logical lists.
 
     q_bits: bf16 [B][H_Q][d_h]; K, V: stored scalars (uint16 bf16 or uint8 e4m3)
@@ -209,7 +254,7 @@ def decode(q_bits, K, V, cu, n, H_KV, scales=None, scale=None):
     B, H_Q, d = q.shape
     K = np.ascontiguousarray(K)
     V = np.ascontiguousarray(V)
-    s = K.dtype.itemsize
+    kind = kind_of(kind if kind is not None else K.dtype.itemsize)
     cu = np.ascontiguousarray(cu, dtype=np.int64)
     n = np.ascontiguousarray(n, dtype=np.int64)
     sc = None if scales is None else np.ascontiguousarray(scales, dtype=np.float32)
@@ -217,14 +262,14 @@ def decode(q_bits, K, V, cu, n, H_KV, scales=None, scale=None):
         scale = float(np.float32(1.0 / np.sqrt(d)))
     out = np.empty((B, H_Q, d), dtype=np.float64)
     lse = np.empty((B, H_Q), dtype=np.float64)
-    st = lib().orc_decode(_p(q), _p(K), _p(V), _p(cu), _p(n), B, H_Q, H_KV, d, s, _p(sc),
+    st = lib().orc_decode(_p(q), _p(K), _p(V), _p(cu), _p(n), B, H_Q, H_KV, d, kind, _p(sc),
                           float(scale), _p(out), _p(lse))
     if st != OK:
         raise ValueError(f"oracle decode status {st}")
     return out, lse
 
 
-def prefill(q_bits, K, V, q_start, H_KV, scales=None, scale=None):
+def prefill(q_bits, K, V, q_start, H_KV, scales=None, scale=None, kind=None):
     """Causal chunk: query i (position q_start+i) reads positions 0..q_start+i of K/V [len][H_KV][d_h]."""
     q = np.ascontiguousarray(q_bits, dtype=np.uint16)
     n_q, H_Q, d = q.shape
@@ -236,7 +281,8 @@ def prefill(q_bits, K, V, q_start, H_KV, scales=None, scale=None):
         scale = float(np.float32(1.0 / np.sqrt(d)))
     out = np.empty((n_q, H_Q, d), dtype=np.float64)
     lse = np.empty((n_q, H_Q), dtype=np.float64)
-    st = lib().orc_prefill(_p(q), n_q, _p(K), _p(V), q_start, H_Q, H_KV, d, K.dtype.itemsize, _p(sc),
+    st = lib().orc_prefill(_p(q), n_q, _p(K), _p(V), q_start, H_Q, H_KV, d,
+                           kind_of(kind if kind is not None else K.dtype.itemsize), _p(sc),
                            float(scale), _p(out), _p(lse))
     if st != OK:
         raise ValueError(f"oracle prefill status {st}")

@@ -29,6 +29,14 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* stored-scalar kinds: bf16 (2 bytes), OCP E4M3 (1 byte), int4 (half a byte in
+ * the pool; one byte per element in logical lists) */
+#define ORC_KIND_E4M3 1
+#define ORC_KIND_BF16 2
+#define ORC_KIND_INT4 3
+
+static int logical_bytes(int kind) { return kind == ORC_KIND_BF16 ? 2 : 1; }
+
 /* status codes (the oracle's own; the tests compare them by meaning) */
 #define ORC_OK 0
 #define ORC_ERR_ARG 1
@@ -108,6 +116,34 @@ uint8_t orc_e4m3_from_float(float x)
     return sign | (uint8_t)code;
 }
 
+/* int4 ([P3] "The architecture: every piece explained": int4 with per-channel
+ * scales; the pages fix nothing more, so the plainest symmetric reading):
+ * q = round-half-even(y), clamped to [-7, 7], stored as the nibble q + 8;
+ * NaN stores 0 (nibble 8). */
+uint8_t orc_int4_encode(float y)
+{
+    if (isnan(y)) return 8;
+    double r = rint((double)y);
+    if (r > 7.0) r = 7.0;
+    if (r < -7.0) r = -7.0;
+    return (uint8_t)(r + 8.0);
+}
+
+double orc_int4_decode(uint8_t nibble) { return (double)nibble - 8.0; }
+
+/* int4 scale for one channel: absmax over positions / 7 in fp32 (1 if 0). */
+void orc_int4_scales(const uint16_t *x, int64_t n_tokens, int32_t H_KV, int32_t d_h, float *scale_out)
+{
+    for (int64_t hc = 0; hc < (int64_t)H_KV * d_h; ++hc) {
+        float amax = 0.0f;
+        for (int64_t t = 0; t < n_tokens; ++t) {
+            const float v = fabsf((float)orc_bf16_to_double(x[t * H_KV * d_h + hc]));
+            if (v > amax) amax = v;
+        }
+        scale_out[hc] = (amax > 0.0f) ? amax / 7.0f : 1.0f;
+    }
+}
+
 /* fp8 scale for one channel, per the configuration: absmax over positions
  * divided by 448, in fp32; an all-zero channel gets scale 1. */
 void orc_fp8_scales(const uint16_t *x, int64_t n_tokens, int32_t H_KV, int32_t d_h, float *scale_out)
@@ -132,6 +168,18 @@ void orc_quantize_e4m3(const uint16_t *x, int64_t n_tokens, int32_t H_KV, int32_
         for (int64_t hc = 0; hc < (int64_t)H_KV * d_h; ++hc) {
             const float xf = (float)orc_bf16_to_double(x[t * H_KV * d_h + hc]);
             out[t * H_KV * d_h + hc] = orc_e4m3_from_float(xf / scale[hc]);
+        }
+}
+
+/* Stored int4 nibbles (one per byte) of bf16 tokens under scales [H_KV][d_h]. */
+void orc_quantize_int4(const uint16_t *x, int64_t n_tokens, int32_t H_KV, int32_t d_h, const float *scale,
+                       uint8_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n_tokens; ++t)
+        for (int64_t hc = 0; hc < (int64_t)H_KV * d_h; ++hc) {
+            const float xf = (float)orc_bf16_to_double(x[t * H_KV * d_h + hc]);
+            out[t * H_KV * d_h + hc] = orc_int4_encode(xf / scale[hc]);
         }
 }
 
@@ -166,13 +214,14 @@ uint64_t orc_pool_offset(int64_t num_blocks, int32_t bs, int32_t H_KV, int32_t d
  * at a time, logical order preserved across nonconsecutive blocks
  * ([P1] Table 21.1 steps 1-2).  Sequence b receives tokens
  * k[cu[b] .. cu[b+1]) at positions start_pos[b], start_pos[b]+1, ...;
- * each lands at (block_table[b][t / bs], t mod bs).  Stored bytes: the bf16
- * bit pattern unchanged (elem_bytes 2) or the e4m3 code of
- * float(x) / scale[h][c] computed in fp32 (elem_bytes 1; scales are the
- * layer's [2][H_KV][d_h] array, keys first).
+ * each lands at (block_table[b][t / bs], t mod bs).  Stored scalars (kind):
+ * the bf16 bit pattern unchanged, or the e4m3 code / int4 nibble of
+ * float(x) / scale[h][c] computed in fp32 (scales are the layer's
+ * [2][H_KV][d_h] array, keys first).  int4 element e of the pool image is
+ * nibble e mod 2 (0 = low) of byte e / 2.
  * A token whose slot cannot be located is skipped; the first such error is
  * returned and every other token is still written. */
-int orc_write_tokens(uint8_t *img, int64_t num_blocks, int32_t bs, int32_t H_KV, int32_t d_h, int32_t elem_bytes,
+int orc_write_tokens(uint8_t *img, int64_t num_blocks, int32_t bs, int32_t H_KV, int32_t d_h, int32_t kind,
                      int32_t layer, const int32_t *bt, int32_t max_blocks, int32_t B,
                      const int32_t *start_pos, const int64_t *cu, const uint16_t *k, const uint16_t *v,
                      const float *scales)
@@ -194,13 +243,17 @@ int orc_write_tokens(uint8_t *img, int64_t num_blocks, int32_t bs, int32_t H_KV,
                     for (int32_t c = 0; c < d_h; ++c) {
                         const uint64_t off = orc_pool_offset(num_blocks, bs, H_KV, d_h, layer, phys, kv, h, slot, c);
                         const uint16_t x = src[h * d_h + c];
-                        if (elem_bytes == 2) {
+                        const float xf = (float)orc_bf16_to_double(x);
+                        const float sc = scales ? scales[((int64_t)kv * H_KV + h) * d_h + c] : 1.0f;
+                        if (kind == ORC_KIND_BF16) {
                             img[2 * off] = (uint8_t)(x & 0xFF);      /* little-endian bf16 */
                             img[2 * off + 1] = (uint8_t)(x >> 8);
-                        } else {
-                            const float xf = (float)orc_bf16_to_double(x);
-                            const float sc = scales[((int64_t)kv * H_KV + h) * d_h + c];
+                        } else if (kind == ORC_KIND_E4M3) {
                             img[off] = orc_e4m3_from_float(xf / sc);
+                        } else {
+                            const uint8_t nib = orc_int4_encode(xf / sc);
+                            const int shift = (off % 2) ? 4 : 0;
+                            img[off / 2] = (uint8_t)((img[off / 2] & ~(0x0F << shift)) | (nib << shift));
                         }
                     }
             }
@@ -211,7 +264,7 @@ int orc_write_tokens(uint8_t *img, int64_t num_blocks, int32_t bs, int32_t H_KV,
 
 /* Read sequence b's first len positions back through its table: stored
  * scalars [len][H_KV][d_h] (keys to k_out, values to v_out). */
-int orc_gather(const uint8_t *img, int64_t num_blocks, int32_t bs, int32_t H_KV, int32_t d_h, int32_t elem_bytes,
+int orc_gather(const uint8_t *img, int64_t num_blocks, int32_t bs, int32_t H_KV, int32_t d_h, int32_t kind,
                int32_t layer, const int32_t *bt_row, int32_t max_blocks, int64_t len,
                uint8_t *k_out, uint8_t *v_out)
 {
@@ -224,23 +277,29 @@ int orc_gather(const uint8_t *img, int64_t num_blocks, int32_t bs, int32_t H_KV,
             for (int32_t h = 0; h < H_KV; ++h)
                 for (int32_t c = 0; c < d_h; ++c) {
                     const uint64_t off = orc_pool_offset(num_blocks, bs, H_KV, d_h, layer, phys, kv, h, slot, c);
-                    uint8_t *dst = (kv == 0 ? k_out : v_out) + ((t * H_KV + h) * d_h + c) * elem_bytes;
-                    memcpy(dst, img + off * elem_bytes, (size_t)elem_bytes);
+                    const int lb = logical_bytes(kind);
+                    uint8_t *dst = (kv == 0 ? k_out : v_out) + ((t * H_KV + h) * d_h + c) * lb;
+                    if (kind == ORC_KIND_INT4)
+                        *dst = (uint8_t)((img[off / 2] >> ((off % 2) ? 4 : 0)) & 0x0F);
+                    else
+                        memcpy(dst, img + off * lb, (size_t)lb);
                 }
     }
     return ORC_OK;
 }
 
 /* ---------------------------------------------------------------- attention
- * Value of one stored scalar: bf16 widened exactly, or e4m3 decoded times the
- * channel's scale ([P2] FP8: quantized values need scales). */
-static double stored_value(const uint8_t *base, int64_t idx, int32_t elem_bytes, const float *scale_hc)
+ * Value of one stored scalar of a logical list: bf16 widened exactly, or the
+ * e4m3 code / int4 nibble decoded times the channel's scale ([P2] FP8 and
+ * [P3]: quantized values need scales). */
+static double stored_value(const uint8_t *base, int64_t idx, int32_t kind, const float *scale_hc)
 {
-    if (elem_bytes == 2) {
+    if (kind == ORC_KIND_BF16) {
         const uint16_t bits = (uint16_t)(base[2 * idx] | (base[2 * idx + 1] << 8));
         return orc_bf16_to_double(bits);
     }
-    return orc_e4m3_to_double(base[idx]) * (double)(*scale_hc);
+    if (kind == ORC_KIND_E4M3) return orc_e4m3_to_double(base[idx]) * (double)(*scale_hc);
+    return orc_int4_decode(base[idx]) * (double)(*scale_hc);
 }
 
 /* One query head against one sequence's first n positions ([P1] 21.1: the new
@@ -251,7 +310,7 @@ static double stored_value(const uint8_t *base, int64_t idx, int32_t elem_bytes,
  *   out_c = sum_t exp(x_t - m) V[t][h][c] / Z,   lse = m + ln Z
  * n = 0 gives out = 0 and lse = -inf.  x is caller scratch of n doubles. */
 static void attend_one(const double *q, const uint8_t *K, const uint8_t *V, int64_t n,
-                       int32_t H_KV, int32_t d_h, int32_t h, int32_t elem_bytes,
+                       int32_t H_KV, int32_t d_h, int32_t h, int32_t kind,
                        const float *sk, const float *sv, double scale, double *x, double *out, double *lse)
 {
     if (n == 0) {
@@ -264,7 +323,7 @@ static void attend_one(const double *q, const uint8_t *K, const uint8_t *V, int6
         double dot = 0.0;
         for (int32_t c = 0; c < d_h; ++c) {
             const int64_t idx = (t * H_KV + h) * d_h + c;
-            dot += q[c] * stored_value(K, idx, elem_bytes, sk ? &sk[h * d_h + c] : NULL);
+            dot += q[c] * stored_value(K, idx, kind, sk ? &sk[h * d_h + c] : NULL);
         }
         x[t] = scale * dot;
         if (x[t] > m) m = x[t];
@@ -278,7 +337,7 @@ static void attend_one(const double *q, const uint8_t *K, const uint8_t *V, int6
     for (int64_t t = 0; t < n; ++t)
         for (int32_t c = 0; c < d_h; ++c) {
             const int64_t idx = (t * H_KV + h) * d_h + c;
-            out[c] += x[t] * stored_value(V, idx, elem_bytes, sv ? &sv[h * d_h + c] : NULL);
+            out[c] += x[t] * stored_value(V, idx, kind, sv ? &sv[h * d_h + c] : NULL);
         }
     for (int32_t c = 0; c < d_h; ++c) out[c] /= Z;
     *lse = m + log(Z);
@@ -292,7 +351,7 @@ static void attend_one(const double *q, const uint8_t *K, const uint8_t *V, int6
  * own scores and value mixture.  scales: [2][H_KV][d_h] for e4m3, else NULL.
  * out: [B][H_Q][d_h], lse: [B][H_Q] (natural log of the scaled-score sum). */
 int orc_decode(const uint16_t *q, const uint8_t *K, const uint8_t *V, const int64_t *cu, const int64_t *n,
-               int32_t B, int32_t H_Q, int32_t H_KV, int32_t d_h, int32_t elem_bytes, const float *scales,
+               int32_t B, int32_t H_Q, int32_t H_KV, int32_t d_h, int32_t kind, const float *scales,
                double scale, double *out, double *lse)
 {
     if (H_KV <= 0 || H_Q % H_KV != 0) return ORC_ERR_ARG;
@@ -312,8 +371,8 @@ int orc_decode(const uint16_t *q, const uint8_t *K, const uint8_t *V, const int6
             continue;
         }
         for (int32_t c = 0; c < d_h; ++c) qd[c] = orc_bf16_to_double(q[bh * d_h + c]);
-        const int64_t row0 = cu[b] * H_KV * d_h * elem_bytes;
-        attend_one(qd, K + row0, V + row0, n[b], H_KV, d_h, h, elem_bytes, sk, sv, scale, x,
+        const int64_t row0 = cu[b] * H_KV * d_h * logical_bytes(kind);
+        attend_one(qd, K + row0, V + row0, n[b], H_KV, d_h, h, kind, sk, sv, scale, x,
                    out + bh * d_h, lse + bh);
         free(x);
     }
@@ -326,7 +385,7 @@ int orc_decode(const uint16_t *q, const uint8_t *K, const uint8_t *V, const int6
  * position q_start + i and, by causal visibility ([P1] 21.1), reads positions
  * 0 .. q_start + i.  q: [n_q][H_Q][d_h]; out/lse like orc_decode with B = n_q. */
 int orc_prefill(const uint16_t *q, int64_t n_q, const uint8_t *K, const uint8_t *V, int64_t q_start,
-                int32_t H_Q, int32_t H_KV, int32_t d_h, int32_t elem_bytes, const float *scales,
+                int32_t H_Q, int32_t H_KV, int32_t d_h, int32_t kind, const float *scales,
                 double scale, double *out, double *lse)
 {
     int64_t *cu = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n_q + 1));
@@ -334,7 +393,7 @@ int orc_prefill(const uint16_t *q, int64_t n_q, const uint8_t *K, const uint8_t 
     if (!cu || !n) { free(cu); free(n); return ORC_ERR_ARG; }
     for (int64_t i = 0; i <= n_q; ++i) cu[i] = 0;        /* every query reads the same list */
     for (int64_t i = 0; i < n_q; ++i) n[i] = q_start + i + 1;
-    const int st = orc_decode(q, K, V, cu, n, (int32_t)n_q, H_Q, H_KV, d_h, elem_bytes, scales, scale, out, lse);
+    const int st = orc_decode(q, K, V, cu, n, (int32_t)n_q, H_Q, H_KV, d_h, kind, scales, scale, out, lse);
     free(cu);
     free(n);
     return st;

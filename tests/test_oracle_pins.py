@@ -433,3 +433,64 @@ def test_prefill_rows_are_decodes():
                                     _dequant(K), _dequant(V), H_Q, float(np.float32(1 / math.sqrt(d))), rng)
     np.testing.assert_allclose(out[-1], ro, atol=1e-12)
     np.testing.assert_allclose(lse[-1], rl, atol=1e-12)
+
+
+# ---------------------------------------------------------------- int4
+def test_int4_codec_nearest_even_and_clamped():
+    ys = list(np.arange(-9.0, 9.0, 0.25)) + [0.5, 1.5, 2.5, -0.5, -2.5, 6.5, -6.5, 7.5, -7.5, 1e9, -1e9, 3.4999998]
+    ys += list(synth.normal_f64(4, 1, 2000) * 4)
+    for y in ys:
+        y = float(np.float32(y))
+        cand = np.arange(-7, 8)
+        dist = np.abs(cand - y)
+        best = cand[dist == dist.min()]
+        want = int(best[0]) if len(best) == 1 else int(best[best % 2 == 0][0])
+        assert oracle.int4_encode(y) == want + 8, y
+        assert oracle.int4_encode(y) == int(np.clip(np.rint(np.float32(y)), -7, 7)) + 8     # numpy's rint: ties to even
+    assert oracle.int4_encode(float("nan")) == 8
+    for q in range(-7, 8):
+        assert oracle.int4_decode(q + 8) == q and oracle.int4_encode(float(q)) == q + 8
+
+
+def test_int4_scales_definition():
+    x = synth.normal_bf16(6, 2, 50 * 3 * 8).reshape(50, 3, 8)
+    assert np.array_equal(oracle.int4_scales(x), (np.abs(synth.bf16_bits_to_f32(x)).max(axis=0) / np.float32(7)))
+    assert np.array_equal(oracle.int4_scales(np.zeros((2, 1, 4), np.uint16)), np.ones((1, 4), np.float32))
+
+
+def test_int4_pool_image_packs_two_channels_per_byte():
+    H, d, bs, N = 2, 8, 4, 6
+    img = oracle.PoolImage(N, bs, 1, H, d, "int4", fill=0x00)
+    assert img.bytes.size == N * 2 * H * bs * d // 2
+    x = synth.normal_bf16(8, 1, 9 * H * d).reshape(9, H, d)
+    sc = oracle.int4_scales(x)
+    img.scales[0] = np.stack([sc, sc])
+    bt = np.array([[3, 0, 5]], np.int32)
+    assert img.write_tokens(0, bt, np.array([0], np.int32), np.array([0, 9], np.int64), x, x) == oracle.OK
+    st, k, v = img.gather(0, bt[0], 9)
+    q = oracle.quantize_int4(x, sc)
+    assert st == oracle.OK and np.array_equal(k, q) and np.array_equal(v, q)
+    # channel 2j of a row sits in the low nibble of a byte, 2j+1 in the high nibble
+    off = img.offset(0, 3, 0, 1, 2, 4)          # block 3, keys, head 1, slot 2, channel 4
+    assert off % 2 == 0
+    byte = int(img.bytes[off // 2])
+    assert byte & 0x0F == q[2, 1, 4] and byte >> 4 == q[2, 1, 5]
+
+
+def test_decode_equals_full_recompute_int4():
+    rng = np.random.default_rng(8)
+    H_Q, H_KV, d, lens = 8, 2, 16, [1, 9, 30]
+    B = len(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    Kb = synth.normal_bf16(31, 1, int(cu[-1]) * H_KV * d).reshape(-1, H_KV, d)
+    Vb = synth.normal_bf16(31, 2, int(cu[-1]) * H_KV * d).reshape(-1, H_KV, d)
+    sc = np.stack([oracle.int4_scales(Kb), oracle.int4_scales(Vb)])
+    K, V = oracle.quantize_int4(Kb, sc[0]), oracle.quantize_int4(Vb, sc[1])
+    q = synth.normal_bf16(32, 1, B * H_Q * d).reshape(B, H_Q, d)
+    out, lse = oracle.decode(q, K, V, cu, np.array(lens), H_KV, scales=sc, scale=0.25, kind="int4")
+    for b in range(B):
+        Kd = (K[cu[b]:cu[b + 1]].astype(np.float64) - 8) * sc[0].astype(np.float64)[None]
+        Vd = (V[cu[b]:cu[b + 1]].astype(np.float64) - 8) * sc[1].astype(np.float64)[None]
+        ro, rl = _torch_causal_last_row(synth.bf16_bits_to_f32(q[b]).astype(np.float64), Kd, Vd, H_Q, 0.25, rng)
+        np.testing.assert_allclose(out[b], ro, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[b], rl, rtol=0, atol=1e-12)
