@@ -45,11 +45,11 @@ def step_bytes(w) -> dict:
     """Algorithmic bytes of one decode step of workload w (one layer)."""
     s = w.elem_bytes
     lens = w.lens_post.astype(np.int64)
-    kv = int(lens.sum()) * 2 * w.H_KV * w.d_h * s
+    kv = int(lens.sum()) * 2 * w.H_KV * w.d_h * w.elem_bits // 8
     table = int(((lens + w.bs - 1) // w.bs).sum()) * 4
     q = w.B * w.H_Q * w.d_h * 2
     out = w.B * w.H_Q * w.d_h * 4 + w.B * w.H_Q * 4
-    append = 2 * w.B * w.H_KV * w.d_h * (2 + s)
+    append = int(2 * w.B * w.H_KV * w.d_h * (2 + s))
     lens_b = w.B * 4 * 2
     return {"kv": kv, "table": table, "q": q, "out": out, "append": append, "lens": lens_b,
             "attn_kernel": kv + table + q + out + w.B * 4,
@@ -180,7 +180,7 @@ def oracle_sample(w, ld, budget_s: float, units_max=None):
             img.write_tokens(0, np.zeros((1, 1), np.int32), np.array([nb[i] - 1], np.int32),
                              np.array([0, 1], np.int64), ld.k_new[b:b + 1, h:h + 1], ld.v_new[b:b + 1, h:h + 1])
         oracle.decode(qb, kb, vb, cub, nb, 1, scale=w.scale)
-        return int(nb.sum()) * 2 * w.d_h * w.elem_bytes, time.perf_counter() - t0
+        return int(nb.sum()) * 2 * w.d_h * w.elem_bits // 8, time.perf_counter() - t0
 
     _, t1 = run(units[:1])
     k = max(1, min(len(units), int(budget_s / max(t1, 1e-6))))

@@ -55,7 +55,10 @@ typedef void *kvc_stream_t;         /* a cudaStream_t */
 
 typedef enum {
     KVC_BF16 = 0,       /* 2-byte bfloat16 elements, stored bit for bit */
-    KVC_FP8_E4M3 = 1    /* 1-byte OCP E4M3 ("FN") elements with fp32 per-(head, channel) scales */
+    KVC_FP8_E4M3 = 1,   /* 1-byte OCP E4M3 ("FN") elements with fp32 per-(head, channel) scales */
+    KVC_INT4 = 2        /* 4-bit elements, q = rint(x / scale) in [-7, 7] stored as q + 8, two per byte
+                         * (even channel in the low nibble), fp32 per-(head, channel) scales
+                         * (the xf_kv_cache page: "int4 with per-channel scales") */
 } kvc_dtype;
 
 typedef enum {
@@ -79,7 +82,7 @@ typedef struct {
     int32_t num_kv_heads;           /* H_KV */
     int32_t head_dim;               /* d_h */
     int32_t dtype;                  /* kvc_dtype */
-    int32_t elem_bytes;             /* s: 2 (bf16) or 1 (e4m3) */
+    int32_t elem_bytes;             /* s: 2 (bf16), 1 (e4m3), 0 (int4: half a byte, see elem_bits) */
     int32_t device;                 /* CUDA ordinal the pool lives on */
     int64_t num_blocks;             /* N */
     uint64_t block_bytes_per_layer; /* 2 * H_KV * bs * d_h * s */
@@ -88,7 +91,9 @@ typedef struct {
     uint64_t capacity_tokens;       /* N * bs */
     uint64_t pool_bytes;            /* L * layer_bytes */
     void *base;                     /* device pointer of element 0 */
-    float *scales;                  /* device fp32 [L][2][H_KV][d_h] (keys first) for e4m3 pools, else NULL */
+    float *scales;                  /* device fp32 [L][2][H_KV][d_h] (keys first) for e4m3 / int4 pools, else NULL */
+    int32_t elem_bits;              /* 16, 8 or 4 */
+    int32_t reserved;
 } kvc_pool_desc;
 
 /* ------------------------------------------------------------------ pool */
@@ -98,10 +103,10 @@ typedef struct {
  * ("KV cache: Generation state, latency, and allocation" 21.5: fixed-size
  * blocks allocated as sequences grow; "KV Cache Explained", "Why
  * PagedAttention allocates KV in blocks": the pool is initialised up front).
- * Bytes: L * N * 2 * H_KV * bs * d_h * s, plus for e4m3 the scale array
+ * Bytes: L * N * 2 * H_KV * bs * d_h * s (s = 1/2 for int4), plus for e4m3 / int4 the scale array
  * (initialised to 1.0).  Pool contents are uninitialised.
- * Limits: 1 <= block_size <= 128, head_dim in {64, 128, 256} for bf16 and
- * {128, 256} for e4m3, 1 <= H_KV <= 256, num_blocks >= 1, the pool's total
+ * Limits: 1 <= block_size <= 128, head_dim in {64, 128, 256} for bf16,
+ * {128, 256} for e4m3 and 128 for int4, 1 <= H_KV <= 256, num_blocks >= 1, the pool's total
  * row count L*N*H_KV*2*bs < 2^31.  Errors: KVC_ERR_ARG, KVC_ERR_OOM,
  * KVC_ERR_CUDA; *out is NULL on error. */
 KVC_API kvc_status kvc_pool_create(int64_t num_blocks, int32_t block_size, int32_t num_layers,
@@ -115,19 +120,23 @@ KVC_API kvc_status kvc_pool_info(const kvc_pool *pool, kvc_pool_desc *desc);
 
 /* Set layer `layer`'s e4m3 scales: s_k, s_v are device fp32 [H_KV][d_h]
  * ("KV Cache Explained", "What changes when you use FP8 KV": quantized values
- * need scales; per-(KV head, channel) granularity).  Stored as given; a
- * scale must be a positive finite float.  Errors: KVC_ERR_ARG (bf16 pool,
+ * need scales; per-(KV head, channel) granularity), e4m3 or int4 pools.
+ * Stored as given; a scale must be a positive finite float.  Errors: KVC_ERR_ARG (bf16 pool,
  * layer out of range, NULL), KVC_ERR_CUDA. */
 KVC_API kvc_status kvc_pool_set_scales(kvc_pool *pool, int32_t layer, const float *s_k, const float *s_v,
                                kvc_stream_t stream);
 
-/* Calibrate layer `layer`'s e4m3 scales from bf16 tokens: absmax over the
- * given positions per (KV head, channel), divided by 448 (the largest finite
- * E4M3 value), in fp32; a channel whose absmax is 0 gets scale 1.
+/* Calibrate layer `layer`'s scales from bf16 tokens: absmax over the given
+ * positions per (KV head, channel), divided by 448 (the largest finite E4M3
+ * value) for e4m3 pools or by 7 (the int4 range) for int4 pools, in fp32; a
+ * channel whose absmax is 0 gets scale 1.
  * k, v: device bf16 [n_tokens][H_KV][d_h].  With accumulate = 0 the running
  * absmax is reset first; with accumulate = 1 it extends the previous calls',
  * so a context uploaded in pieces calibrates like one array.  The scales are
  * rewritten after every call.  Errors: KVC_ERR_ARG, KVC_ERR_CUDA. */
+KVC_API kvc_status kvc_calibrate_scales(kvc_pool *pool, int32_t layer, const void *k, const void *v,
+                                        int64_t n_tokens, int32_t accumulate, kvc_stream_t stream);
+/* The same call under its first name (e4m3 pools). */
 KVC_API kvc_status kvc_calibrate_fp8(kvc_pool *pool, int32_t layer, const void *k, const void *v,
                              int64_t n_tokens, int32_t accumulate, kvc_stream_t stream);
 

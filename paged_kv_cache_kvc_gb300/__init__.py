@@ -20,7 +20,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libkvc.so")
 
-KVC_BF16, KVC_FP8_E4M3 = 0, 1
+KVC_BF16, KVC_FP8_E4M3, KVC_INT4 = 0, 1, 2
 (KVC_OK, KVC_ERR_ARG, KVC_ERR_OOM, KVC_ERR_BAD_BLOCK, KVC_ERR_RANGE, KVC_ERR_ALIAS, KVC_ERR_STALE,
  KVC_ERR_TIMEOUT, KVC_ERR_CUDA, KVC_ERR_UNSUPPORTED) = range(10)
 
@@ -39,10 +39,12 @@ class kvc_pool_desc(ctypes.Structure):
                 ("elem_bytes", ctypes.c_int32), ("device", ctypes.c_int32), ("num_blocks", ctypes.c_int64),
                 ("block_bytes_per_layer", ctypes.c_uint64), ("layer_bytes", ctypes.c_uint64),
                 ("bytes_per_token", ctypes.c_uint64), ("capacity_tokens", ctypes.c_uint64),
-                ("pool_bytes", ctypes.c_uint64), ("base", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+                ("pool_bytes", ctypes.c_uint64), ("base", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("elem_bits", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 EXPORTS = ["kvc_pool_create", "kvc_pool_destroy", "kvc_pool_info", "kvc_pool_set_scales", "kvc_calibrate_fp8",
+           "kvc_calibrate_scales",
            "kvc_append", "kvc_write_tokens", "kvc_decode_attn", "kvc_prefill_attn", "kvc_pool_reserve",
            "kvc_bytes", "kvc_pool_sync_status", "kvc_status_str", "kvc_launch_count", "kvc_decode_attn_noalloc", "kvc_decode_step",
            "kvc_alloc_create", "kvc_alloc_destroy", "kvc_alloc_new_seq", "kvc_alloc_fork", "kvc_alloc_reserve",
@@ -65,6 +67,7 @@ def load(path: str = LIB_PATH):
     L.kvc_pool_info.restype, L.kvc_pool_info.argtypes = st, [vp, ctypes.POINTER(kvc_pool_desc)]
     L.kvc_pool_set_scales.restype, L.kvc_pool_set_scales.argtypes = st, [vp, i32, vp, vp, vp]
     L.kvc_calibrate_fp8.restype, L.kvc_calibrate_fp8.argtypes = st, [vp, i32, vp, vp, i64, i32, vp]
+    L.kvc_calibrate_scales.restype, L.kvc_calibrate_scales.argtypes = st, [vp, i32, vp, vp, i64, i32, vp]
     L.kvc_append.restype, L.kvc_append.argtypes = st, [vp, i32, vp, i32, vp, i32, vp, vp, vp]
     L.kvc_write_tokens.restype, L.kvc_write_tokens.argtypes = st, [vp, i32, vp, i32, vp, vp, i32, i32, vp, vp, vp]
     L.kvc_decode_attn.restype = st
@@ -134,6 +137,7 @@ class Pool:
         d = kvc_pool_info(self)
         self.num_blocks, self.block_size, self.num_layers = d.num_blocks, d.block_size, d.num_layers
         self.num_kv_heads, self.head_dim, self.dtype, self.elem_bytes = d.num_kv_heads, d.head_dim, d.dtype, d.elem_bytes
+        self.elem_bits = d.elem_bits
         self.device = d.device
 
     def close(self):
@@ -198,6 +202,13 @@ def kvc_pool_info(pool) -> kvc_pool_desc:
 def kvc_pool_set_scales(pool, layer, s_k, s_v, stream=None):
     _check(load().kvc_pool_set_scales(_h(pool), layer, _dev(s_k, torch.float32, "s_k"), _dev(s_v, torch.float32, "s_v"),
                                       _stream(stream)), "kvc_pool_set_scales")
+
+
+def kvc_calibrate_scales(pool, layer, k, v, accumulate=False, stream=None):
+    """absmax / 448 (e4m3) or / 7 (int4) per (KV head, channel) over bf16 tokens [n][H_KV][d_h]."""
+    n = k.shape[0]
+    _check(load().kvc_calibrate_scales(_h(pool), layer, _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"), n,
+                                       int(bool(accumulate)), _stream(stream)), "kvc_calibrate_scales")
 
 
 def kvc_calibrate_fp8(pool, layer, k, v, accumulate=False, stream=None):

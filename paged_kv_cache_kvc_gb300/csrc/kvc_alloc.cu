@@ -399,7 +399,7 @@ extern "C" kvc_status kvc_copy_blocks(kvc_pool *pool, const int32_t *pairs, int3
     if ((reinterpret_cast<uintptr_t>(pairs) & 3) != 0) return KVC_ERR_ARG;
     kvc_status st = check_device(pool);
     if (st != KVC_OK) return st;
-    const int64_t block_bytes = 2ll * pool->H_KV * pool->bs * pool->D * pool->s;
+    const int64_t block_bytes = 2ll * pool->H_KV * pool->bs * pool->D * pool->bits / 8;
     copy_blocks_kernel<<<dim3(n, pool->L), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         pool->base, pairs, pool->N, static_cast<int64_t>(pool->layer_bytes), block_bytes, pool->err);
     const cudaError_t e = cudaGetLastError();

@@ -157,7 +157,9 @@ static void fill_common(DecodeParams &p, const kvc_pool *pool, int32_t layer, co
 
 static kvc_status dispatch(kvc_pool *pool, DecodeParams &p, cudaStream_t stream)
 {
-    return pool->dtype == KVC_FP8_E4M3 ? launch_decode_fp8(pool, p, stream) : launch_decode_bf16(pool, p, stream);
+    if (pool->dtype == KVC_FP8_E4M3) return launch_decode_fp8(pool, p, stream);
+    if (pool->dtype == KVC_INT4) return launch_decode_int4(pool, p, stream);
+    return launch_decode_bf16(pool, p, stream);
 }
 
 }  // namespace kvc

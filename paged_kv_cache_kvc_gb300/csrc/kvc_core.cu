@@ -54,7 +54,8 @@ struct ScatterParams {
     const int32_t *start;   // [B] first position written
     const int32_t *cu;      // [B+1] token offsets, or nullptr: one token per sequence at row b
     const uint16_t *k, *v;  // bf16 [rows][H_KV][D]
-    const float *scales;    // this layer's [2][H_KV][D] for e4m3, else nullptr
+    const float *scales;    // this layer's [2][H_KV][D] for e4m3 / int4, else nullptr
+    int32_t bits;           // stored bits per element: 16, 8, 4
     uint32_t *err;
     int32_t tok_per_cta;
 };
@@ -95,8 +96,21 @@ __global__ void __launch_bounds__(256) scatter_kernel(const ScatterParams p)
         const uint4 x = *reinterpret_cast<const uint4 *>(src);
         const int64_t e =
             ((((static_cast<int64_t>(p.layer) * p.N + phys) * p.H_KV + h) * 2 + kv) * p.bs + slot) * p.D + ch * 8;
-        if (p.s == 2) {
+        if (p.bits == 16) {
             *reinterpret_cast<uint4 *>(p.base + e * 2) = x;
+        } else if (p.bits == 4) {   // rint(x / s) clamped to [-7, 7], nibble q + 8; channel 2j in the low nibble
+            const float *sc = p.scales + (static_cast<int64_t>(kv) * p.H_KV + h) * p.D + ch * 8;
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+            uint32_t packed = 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float f = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+                const float y = __fdiv_rn(f, __ldg(sc + i));
+                const uint32_t q = isnan(y) ? 8u
+                                            : static_cast<uint32_t>(static_cast<int>(fminf(fmaxf(rintf(y), -7.f), 7.f)) + 8);
+                packed |= q << (4 * i);
+            }
+            *reinterpret_cast<uint32_t *>(p.base + e / 2) = packed;
         } else {
             const float *sc = p.scales + (static_cast<int64_t>(kv) * p.H_KV + h) * p.D + ch * 8;
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -142,6 +156,7 @@ static kvc_status scatter(kvc_pool *pool, int32_t layer, const int32_t *bt, int3
     p.v = static_cast<const uint16_t *>(v);
     p.scales = pool->scales ? pool->scales + static_cast<size_t>(layer) * 2 * pool->H_KV * pool->D : nullptr;
     p.err = pool->err;
+    p.bits = pool->bits;
     const int per_tok = 2 * pool->H_KV * (pool->D / 8);
     p.tok_per_cta = per_tok >= 4096 ? 1 : 4096 / per_tok;
     const int gx = (max_tokens + p.tok_per_cta - 1) / p.tok_per_cta;
@@ -164,10 +179,11 @@ __global__ void absmax_kernel(const uint16_t *x, int64_t n_tokens, int HD, int t
     }
 }
 
-__global__ void scales_from_absmax_kernel(const float *amax, float *scales, int n)
+// scale = absmax / qmax (448: largest finite e4m3; 7: int4 range), 1 for an all-zero channel
+__global__ void scales_from_absmax_kernel(const float *amax, float *scales, int n, float qmax)
 {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n) scales[i] = amax[i] > 0.f ? __fdiv_rn(amax[i], 448.f) : 1.f;
+    if (i < n) scales[i] = amax[i] > 0.f ? __fdiv_rn(amax[i], qmax) : 1.f;
 }
 
 __global__ void fill_kernel(float *x, float v, int n)
@@ -237,15 +253,16 @@ extern "C" kvc_status kvc_pool_create(int64_t num_blocks, int32_t block_size, in
     if (num_blocks < 1 || block_size < 1 || block_size > 128 || num_layers < 1 || num_kv_heads < 1 ||
         num_kv_heads > 256)
         return KVC_ERR_ARG;
-    if (dtype != KVC_BF16 && dtype != KVC_FP8_E4M3) return KVC_ERR_ARG;
-    const int s = dtype == KVC_BF16 ? 2 : 1;
+    if (dtype != KVC_BF16 && dtype != KVC_FP8_E4M3 && dtype != KVC_INT4) return KVC_ERR_ARG;
+    const int bits = dtype == KVC_BF16 ? 16 : (dtype == KVC_FP8_E4M3 ? 8 : 4);
+    const int s = bits / 8;
     const bool dim_ok = dtype == KVC_BF16 ? (head_dim == 64 || head_dim == 128 || head_dim == 256)
-                                          : (head_dim == 128 || head_dim == 256);
+                        : dtype == KVC_FP8_E4M3 ? (head_dim == 128 || head_dim == 256) : head_dim == 128;
     if (!dim_ok) return KVC_ERR_ARG;
     const uint64_t rows = static_cast<uint64_t>(num_layers) * static_cast<uint64_t>(num_blocks) *
                           static_cast<uint64_t>(num_kv_heads) * 2u * static_cast<uint64_t>(block_size);
     if (rows >= (1ull << 31)) return KVC_ERR_ARG;
-    const uint64_t pool_bytes = rows * static_cast<uint64_t>(head_dim) * s;
+    const uint64_t pool_bytes = rows * static_cast<uint64_t>(head_dim) * bits / 8;
 
     kvc_pool *pool = new (std::nothrow) kvc_pool();
     if (!pool) return KVC_ERR_OOM;
@@ -256,6 +273,7 @@ extern "C" kvc_status kvc_pool_create(int64_t num_blocks, int32_t block_size, in
     pool->D = head_dim;
     pool->dtype = dtype;
     pool->s = s;
+    pool->bits = bits;
     pool->layer_bytes = pool_bytes / num_layers;
     pool->pool_bytes = pool_bytes;
     if (cudaGetDevice(&pool->device) != cudaSuccess ||
@@ -268,7 +286,7 @@ extern "C" kvc_status kvc_pool_create(int64_t num_blocks, int32_t block_size, in
         cudaMemset(pool->err, 0, sizeof(uint32_t)) != cudaSuccess)
         st = KVC_ERR_OOM;
     const int nsc = num_layers * 2 * num_kv_heads * head_dim;
-    if (st == KVC_OK && dtype == KVC_FP8_E4M3) {
+    if (st == KVC_OK && dtype != KVC_BF16) {
         if (cudaMalloc(&pool->scales, sizeof(float) * nsc) != cudaSuccess ||
             cudaMalloc(&pool->absmax, sizeof(float) * nsc) != cudaSuccess ||
             cudaMemset(pool->absmax, 0, sizeof(float) * nsc) != cudaSuccess)
@@ -286,13 +304,18 @@ extern "C" kvc_status kvc_pool_create(int64_t num_blocks, int32_t block_size, in
     }
     // Tensor map: the pool as rows of D elements; a box is one 128-byte
     // column band of one block's 2*bs key+value rows, with 128-byte swizzle.
+    // int4 rows are 64 bytes: the map's rows are 128-byte lines (two token
+    // rows) and a box is one block-head's bs lines.
     pool->tmap_ok = false;
     if (PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder()) {
-        cuuint64_t gdim[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-        cuuint64_t gstride[1] = {static_cast<cuuint64_t>(head_dim) * s};
-        cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / s), static_cast<cuuint32_t>(2 * block_size)};
+        const bool lines = bits == 4;
+        cuuint64_t gdim[2] = {lines ? 128u : static_cast<cuuint64_t>(head_dim),
+                              lines ? static_cast<cuuint64_t>(pool_bytes / 128) : static_cast<cuuint64_t>(rows)};
+        cuuint64_t gstride[1] = {lines ? 128u : static_cast<cuuint64_t>(head_dim) * s};
+        cuuint32_t box[2] = {lines ? 128u : static_cast<cuuint32_t>(128 / s),
+                             static_cast<cuuint32_t>(lines ? block_size : 2 * block_size)};
         cuuint32_t estride[2] = {1, 1};
-        const CUresult r = enc(&pool->tmap, s == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+        const CUresult r = enc(&pool->tmap, bits == 16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                                2, pool->base, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -313,11 +336,12 @@ extern "C" kvc_status kvc_pool_info(const kvc_pool *pool, kvc_pool_desc *d)
     d->head_dim = pool->D;
     d->dtype = pool->dtype;
     d->elem_bytes = pool->s;
+    d->elem_bits = pool->bits;
     d->device = pool->device;
     d->num_blocks = pool->N;
-    d->block_bytes_per_layer = 2ull * pool->H_KV * pool->bs * pool->D * pool->s;
+    d->block_bytes_per_layer = 2ull * pool->H_KV * pool->bs * pool->D * pool->bits / 8;
     d->layer_bytes = pool->layer_bytes;
-    d->bytes_per_token = kvc_bytes(pool->L, 1, pool->H_KV, 1, pool->D, pool->s);
+    d->bytes_per_token = 2ull * pool->L * pool->H_KV * pool->D * pool->bits / 8;
     d->capacity_tokens = static_cast<uint64_t>(pool->N) * pool->bs;
     d->pool_bytes = pool->pool_bytes;
     d->base = pool->base;
@@ -328,7 +352,7 @@ extern "C" kvc_status kvc_pool_info(const kvc_pool *pool, kvc_pool_desc *d)
 extern "C" kvc_status kvc_pool_set_scales(kvc_pool *pool, int32_t layer, const float *s_k, const float *s_v,
                                           kvc_stream_t stream)
 {
-    if (!pool || !s_k || !s_v || pool->dtype != KVC_FP8_E4M3 || layer < 0 || layer >= pool->L) return KVC_ERR_ARG;
+    if (!pool || !s_k || !s_v || pool->dtype == KVC_BF16 || layer < 0 || layer >= pool->L) return KVC_ERR_ARG;
     kvc_status st = check_device(pool);
     if (st != KVC_OK) return st;
     const size_t n = static_cast<size_t>(pool->H_KV) * pool->D;
@@ -339,10 +363,10 @@ extern "C" kvc_status kvc_pool_set_scales(kvc_pool *pool, int32_t layer, const f
     return cuda_status(e);
 }
 
-extern "C" kvc_status kvc_calibrate_fp8(kvc_pool *pool, int32_t layer, const void *k, const void *v,
-                                        int64_t n_tokens, int32_t accumulate, kvc_stream_t stream)
+extern "C" kvc_status kvc_calibrate_scales(kvc_pool *pool, int32_t layer, const void *k, const void *v,
+                                           int64_t n_tokens, int32_t accumulate, kvc_stream_t stream)
 {
-    if (!pool || pool->dtype != KVC_FP8_E4M3 || layer < 0 || layer >= pool->L || n_tokens < 0) return KVC_ERR_ARG;
+    if (!pool || pool->dtype == KVC_BF16 || layer < 0 || layer >= pool->L || n_tokens < 0) return KVC_ERR_ARG;
     if (n_tokens > 0 && (!k || !v || !aligned(k, 2) || !aligned(v, 2))) return KVC_ERR_ARG;
     kvc_status st = check_device(pool);
     if (st != KVC_OK) return st;
@@ -365,10 +389,16 @@ extern "C" kvc_status kvc_calibrate_fp8(kvc_pool *pool, int32_t layer, const voi
         }
     }
     scales_from_absmax_kernel<<<(2 * HD + 255) / 256, 256, 0, s>>>(
-        amax, pool->scales + static_cast<size_t>(layer) * 2 * HD, 2 * HD);
+        amax, pool->scales + static_cast<size_t>(layer) * 2 * HD, 2 * HD, pool->dtype == KVC_INT4 ? 7.f : 448.f);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return KVC_OK;
+}
+
+extern "C" kvc_status kvc_calibrate_fp8(kvc_pool *pool, int32_t layer, const void *k, const void *v,
+                                        int64_t n_tokens, int32_t accumulate, kvc_stream_t stream)
+{
+    return kvc_calibrate_scales(pool, layer, k, v, n_tokens, accumulate, stream);
 }
 
 extern "C" kvc_status kvc_append(kvc_pool *pool, int32_t layer, const int32_t *block_tables, int32_t max_blocks,

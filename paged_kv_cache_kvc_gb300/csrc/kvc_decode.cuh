@@ -22,9 +22,9 @@
 //   online softmax over the tokens (warp shuffles across the 8 lanes of a column)
 //   O^T[D x 8q]     += V^T[D x 16] * P^T[16 x 8q]     (P^T by movmatrix from S^T)
 // bf16 pools feed bf16 operands; P is split into a bf16 high and low part
-// (two mma) so the value mixture keeps ~16 bits of each weight.  e4m3 pools
-// convert codes to f16 in registers (exact) and fold the key scales into q
-// (f16) and the value scales into the output.
+// (two mma) so the value mixture keeps ~16 bits of each weight.  e4m3 and
+// int4 pools convert codes / nibbles to f16 in registers (exact) and fold the
+// key scales into q (f16) and the value scales into the output.
 //
 // TMA writes the tiles with the 128-byte swizzle: within each 128-byte row of
 // a band, 16-byte chunk c sits at c ^ (row mod 8), so the ldmatrix and 16-byte
@@ -44,25 +44,34 @@ constexpr int kBS = 16;                 // positions per block = mma M tile
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D, bool FP8>
+// stored element kinds of a pool
+constexpr int KV_BF16 = 0, KV_E4M3 = 1, KV_INT4 = 2;
+
+template <int D, int KIND>
 struct DecodeCfg {
-    static constexpr int ELEM = FP8 ? 1 : 2;
-    static constexpr int ROW_BYTES = D * ELEM;
-    static constexpr int BANDS = ROW_BYTES / 128;          // 128-byte column bands (one TMA box each)
-    static constexpr int BAND_BYTES = 2 * kBS * 128;       // 32 rows (keys then values) x 128 B
-    static constexpr int STAGE = BANDS * BAND_BYTES;
+    static constexpr int BITS = KIND == KV_BF16 ? 16 : (KIND == KV_E4M3 ? 8 : 4);
+    static constexpr int ROW_BYTES = D * BITS / 8;         // one token row of one head
+    static constexpr int STAGE = 2 * kBS * ROW_BYTES;      // keys then values of one (block, head)
+    // bf16 / e4m3: the tensor map's rows are token rows and a box is one 128-byte
+    // column band of 32 rows; int4 (64-byte rows): rows are 128-byte lines
+    // holding two token rows and one box is the whole stage.
+    static constexpr bool LINES = ROW_BYTES < 128;
+    static constexpr int BANDS = LINES ? 1 : ROW_BYTES / 128;
+    static constexpr int BOX_BYTES = LINES ? STAGE : 2 * kBS * 128;
+    static constexpr int BOX_ROWS = LINES ? STAGE / 128 : 2 * kBS;
+    static constexpr int BOX_X = LINES ? 0 : 128 * 8 / BITS;   // elements per band row
+    static constexpr int CHUNKS = ROW_BYTES / 16;             // 16-byte chunks per token row
     static constexpr int R0 = 98304 / (kWarps * STAGE);
     static constexpr int R = R0 < 2 ? 2 : (R0 > 4 ? 4 : R0);   // ring depth per warp
     static constexpr int KSTEPS = D / 16;
     static constexpr int MT = D / 16;
-    static constexpr int BOX_X = 128 / ELEM;               // elements per band row
-    static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte bands");
+    static_assert(LINES ? (ROW_BYTES == 64) : (ROW_BYTES % 128 == 0), "rows: 64 bytes or whole 128-byte bands");
 };
 
-template <int D, int NT, bool FP8>
+template <int D, int NT, int KIND>
 __host__ __device__ constexpr int decode_smem_bytes()
 {
-    using C = DecodeCfg<D, FP8>;
+    using C = DecodeCfg<D, KIND>;
     constexpr int stages = kWarps * C::R * C::STAGE;
     constexpr int combine = (kWarps * NT * 8 * 2 + kWarps * NT * 8 * D) * 4;
     constexpr int region = stages > combine ? stages : combine;
@@ -74,6 +83,39 @@ __device__ __forceinline__ uint32_t swz(int row, int ch)
 {
     const int band = ch >> 3, c = ch & 7;
     return static_cast<uint32_t>((band * 2 * kBS + row) * 128 + ((c ^ (row & 7)) << 4));
+}
+
+// same for 64-byte token rows packed two per 128-byte line (int4, d_h 128):
+// row r is half r & 1 of line r >> 1
+__device__ __forceinline__ uint32_t swz64(int row, int ch)
+{
+    const int line = row >> 1, c = ((row & 1) << 2) + ch;
+    return static_cast<uint32_t>(line * 128 + ((c ^ (line & 7)) << 4));
+}
+
+template <int D, int KIND>
+__device__ __forceinline__ uint32_t row_chunk(int row, int ch)
+{
+    if constexpr (DecodeCfg<D, KIND>::LINES) return swz64(row, ch);
+    else return swz(row, ch);
+}
+
+// int4: two nibbles at bits 0..3 and 16..19 of x (stored q + 8) -> f16x2 of q, exact
+__device__ __forceinline__ uint32_t nibbles_to_f16x2(uint32_t x)
+{
+    const uint32_t biased = (x & 0x000F000Fu) | 0x64006400u;      // f16 1024 + u
+    uint32_t r;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x64086408u));   // - (1024 + 8)
+    return r;
+}
+
+// int4 quantisation of one value: rint(x / s) clamped to [-7, 7], stored + 8; NaN stores 0
+__device__ __forceinline__ uint32_t int4_code(float x, float s)
+{
+    const float y = __fdiv_rn(x, s);
+    if (isnan(y)) return 8u;
+    const float r = fminf(fmaxf(rintf(y), -7.f), 7.f);
+    return static_cast<uint32_t>(static_cast<int>(r) + 8);
 }
 
 // Positions attended by unit b: lens[b] (+1 when the step's token is appended
@@ -91,19 +133,33 @@ __device__ __forceinline__ int seq_len(const DecodeParams &p, int b)
 // pool, and put the same stored bytes into the landed stage, so attention uses
 // exactly what the pool now holds.  Lanes [0, CH) take the key row, [CH, 2CH)
 // the value row, one 16-byte chunk each.
-template <int D, bool FP8>
+template <int D, int KIND>
 __device__ __forceinline__ void append_row(const DecodeParams &p, uint32_t st, int b, int h, int64_t phys, int slot,
                                            int lane)
 {
-    using C = DecodeCfg<D, FP8>;
-    constexpr int CH = C::ROW_BYTES / 16;
+    using C = DecodeCfg<D, KIND>;
+    constexpr int CH = C::CHUNKS;
     static_assert(2 * CH <= 32, "one warp covers both rows");
     if (lane >= 2 * CH) return;
     const int kv = lane / CH, ch = lane - kv * CH;
     const uint16_t *src = (kv ? p.v_new : p.k_new) + (static_cast<size_t>(b) * p.H_KV + h) * D;
     uint4 val;
-    if constexpr (!FP8) {
+    if constexpr (KIND == KV_BF16) {
         val = *reinterpret_cast<const uint4 *>(src + ch * 8);
+    } else if constexpr (KIND == KV_INT4) {   // 32 channels -> 16 bytes, channel 2j in the low nibble
+        const float *sc = (kv ? p.s_v : p.s_k) + static_cast<size_t>(h) * D + ch * 32;
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(src + ch * 32 + part * 8);
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float f = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+                o[part] |= int4_code(f, __ldg(sc + part * 8 + i)) << (4 * i);
+            }
+        }
+        val = make_uint4(o[0], o[1], o[2], o[3]);
     } else {
         const uint4 x0 = *reinterpret_cast<const uint4 *>(src + ch * 16);
         const uint4 x1 = *reinterpret_cast<const uint4 *>(src + ch * 16 + 8);
@@ -119,15 +175,19 @@ __device__ __forceinline__ void append_row(const DecodeParams &p, uint32_t st, i
         val = make_uint4(o[0], o[1], o[2], o[3]);
     }
     const int64_t e = ((((static_cast<int64_t>(p.layer) * p.N + phys) * p.H_KV + h) * 2 + kv) * kBS + slot) * D;
-    *reinterpret_cast<uint4 *>(p.pool + e * C::ELEM + ch * 16) = val;
-    sts128(st + swz(kv * kBS + slot, ch), val);
+    *reinterpret_cast<uint4 *>(p.pool + e * C::BITS / 8 + ch * 16) = val;
+    sts128(st + row_chunk<D, KIND>(kv * kBS + slot, ch), val);
 }
 
-template <int D, int NT, bool FP8, bool PSPLIT>
+// CAUSAL: columns may see different numbers of positions (prefill tiles), so
+// the mask is per column and a column may see nothing in a block; decode
+// instances (every column sees the unit's whole length) skip both.
+template <int D, int NT, int KIND, bool PSPLIT, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmap,
                                                           const DecodeParams p)
 {
-    using C = DecodeCfg<D, FP8>;
+    using C = DecodeCfg<D, KIND>;
+    constexpr bool FP8 = KIND == KV_E4M3, INT4 = KIND == KV_INT4, QUANT = KIND != KV_BF16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -136,11 +196,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int gq = lane >> 2, tg = lane & 3;
     const int hq0 = h * p.g;
     // query columns of the unit: ppu consecutive positions x the g heads of KV head h
-    const int rows = p.ppu * p.g;
-    auto col_pos = [&](int qi) { return b * p.ppu + qi / p.g; };
-    auto col_real = [&](int qi) { return qi < rows && col_pos(qi) < p.n_pos; };
+    // (decode instances have one position per unit: no divisions)
+    const int rows = CAUSAL ? p.ppu * p.g : p.g;
+    auto col_pos = [&](int qi) { return CAUSAL ? b * p.ppu + qi / p.g : b; };
+    auto col_real = [&](int qi) { return CAUSAL ? (qi < rows && col_pos(qi) < p.n_pos) : qi < rows; };
     auto col_orow = [&](int qi) {   // row of the column in q / out ([position][H_Q])
-        return static_cast<size_t>(col_pos(qi)) * p.H_Q + hq0 + qi % p.g;
+        return CAUSAL ? static_cast<size_t>(col_pos(qi)) * p.H_Q + hq0 + qi % p.g
+                      : static_cast<size_t>(b) * p.H_Q + hq0 + qi;
     };
 
     int len = seq_len(p, b);
@@ -162,7 +224,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int nloc = min(nblk, blk0 + p.chunk) - blk0;
     const int32_t *bt_row = p.bt + static_cast<int64_t>(b) * p.bt_stride + blk0 + warp;
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (decode_smem_bytes<D, NT, FP8>() - 1024 - kWarps * C::R * 8));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (decode_smem_bytes<D, NT, KIND>() - 1024 - kWarps * C::R * 8));
     if (lane == 0) {
         for (int s = 0; s < C::R; ++s) mbar_init(smem_u32(&bars[warp * C::R + s]), 1);
         fence_barrier_init();
@@ -191,12 +253,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
                 mbar_arrive(bar);   // complete the phase without data; the consumer skips it
             } else {
-                const int32_t y = static_cast<int32_t>(((row_layer + phys) * p.H_KV + h) * (2 * kBS));
+                const int32_t y = static_cast<int32_t>(((row_layer + phys) * p.H_KV + h) * C::BOX_ROWS);
                 const uint32_t dst = st_base + static_cast<uint32_t>((jj % C::R) * C::STAGE);
                 mbar_arrive_expect_tx(bar, C::STAGE);
 #pragma unroll
                 for (int band = 0; band < C::BANDS; ++band)
-                    tma_load_2d(dst + band * C::BAND_BYTES, &tmap, bar, band * C::BOX_X, y);
+                    tma_load_2d(dst + band * C::BOX_BYTES, &tmap, bar, band * C::BOX_X, y);
             }
         }
     };
@@ -210,9 +272,20 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         const uint16_t *qrow = p.q + (real ? col_orow(qi) : static_cast<size_t>(0)) * D;
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            if constexpr (!FP8) {
+            if constexpr (!QUANT) {
                 qf[j][kk][0] = real ? *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 2 * tg) : 0u;
                 qf[j][kk][1] = real ? *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 8 + 2 * tg) : 0u;
+            } else if constexpr (INT4) {
+                // slots of k-step kk: channels base, base+4 (b0) and base+1, base+5 (b1) of the
+                // thread's 32-channel chunk, matching the nibble pairs the key fragments hold
+                const int base = 32 * tg + 8 * (kk >> 1) + 2 * (kk & 1);
+                const float *sk = p.s_k + static_cast<size_t>(h) * D;
+                auto qv = [&](int c) {
+                    const uint16_t raw = real ? qrow[c] : uint16_t(0);
+                    return __uint_as_float(static_cast<uint32_t>(raw) << 16) * __ldg(sk + c);
+                };
+                qf[j][kk][0] = pack_f16(qv(base), qv(base + 4));
+                qf[j][kk][1] = pack_f16(qv(base + 1), qv(base + 5));
             } else {
                 // channel slots permuted: thread tg owns channels [tg*D/4, (tg+1)*D/4), four per k-step
                 const int c0 = (D / 4) * tg + 4 * kk;
@@ -231,7 +304,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int qi = 8 * jn + 2 * tg + c;
-            clen[jn][c] = !col_real(qi) ? 0 : (p.lens ? len : p.len_base + col_pos(qi) + 1);
+            clen[jn][c] = !CAUSAL ? len : (!col_real(qi) ? 0 : p.len_base + col_pos(qi) + 1);
         }
 
     float m_run[NT][2], l_run[NT][2];
@@ -266,25 +339,47 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             const int valid = min(kBS, len - (blk0 + warp + kWarps * j) * kBS);
 
             // value rows past the sequence end may hold anything (NaN included): zero them
-            if (valid < kBS) {
+            // (every int4 nibble is a finite value, and its weight there is 0)
+            if (!INT4 && valid < kBS) {
                 const int nz = (kBS - valid) * C::BANDS * 8;
                 for (int i = lane; i < nz; i += 32) sts128_zero(st + swz(kBS + valid + i / (C::BANDS * 8), i % (C::BANDS * 8)));
             }
             // the step's own token (fused append) is the last valid slot of the last block
-            if (p.k_new && blk0 + warp + kWarps * j == nblk - 1) append_row<D, FP8>(p, st, b, h, phys, valid - 1, lane);
+            if (p.k_new && blk0 + warp + kWarps * j == nblk - 1) append_row<D, KIND>(p, st, b, h, phys, valid - 1, lane);
             __syncwarp();
 
             // ---- S^T = K Q^T
             float sc[NT][4];
 #pragma unroll
             for (int jn = 0; jn < NT; ++jn) sc[jn][0] = sc[jn][1] = sc[jn][2] = sc[jn][3] = 0.f;
-            if constexpr (!FP8) {
+            if constexpr (!QUANT) {
 #pragma unroll
                 for (int kk = 0; kk < C::KSTEPS; ++kk) {
                     uint32_t a[4];
                     ldsm_x4(a, st + swz((lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)));
 #pragma unroll
                     for (int jn = 0; jn < NT; ++jn) mma_bf16(sc[jn], a, qf[jn][kk]);
+                }
+            } else if constexpr (INT4) {
+                uint32_t kw[2][4];   // rows gq, gq+8: this thread's 32-channel chunk tg (8 nibbles a word)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint4 v = lds128(st + swz64(gq + 8 * r, tg));
+                    kw[r][0] = v.x;
+                    kw[r][1] = v.y;
+                    kw[r][2] = v.z;
+                    kw[r][3] = v.w;
+                }
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    const int sh = 8 * (kk & 1);   // nibbles (2e, 2e+4) and (2e+1, 2e+5) of word kk / 2
+                    uint32_t a[4];
+                    a[0] = nibbles_to_f16x2(kw[0][kk >> 1] >> sh);
+                    a[2] = nibbles_to_f16x2(kw[0][kk >> 1] >> (sh + 4));
+                    a[1] = nibbles_to_f16x2(kw[1][kk >> 1] >> sh);
+                    a[3] = nibbles_to_f16x2(kw[1][kk >> 1] >> (sh + 4));
+#pragma unroll
+                    for (int jn = 0; jn < NT; ++jn) mma_f16(sc[jn], a, qf[jn][kk]);
                 }
             } else {
                 uint32_t kw[2][D / 16];   // rows gq, gq+8: this thread's D/4 code bytes each
@@ -315,8 +410,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             for (int jn = 0; jn < NT; ++jn) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const int tok = tok0 + gq + ((c >> 1) << 3);
-                    sc[jn][c] = tok < clen[jn][c & 1] ? sc[jn][c] * p.scale_log2 : -INFINITY;
+                    if constexpr (CAUSAL) {
+                        const int tok = tok0 + gq + ((c >> 1) << 3);
+                        sc[jn][c] = tok < clen[jn][c & 1] ? sc[jn][c] * p.scale_log2 : -INFINITY;
+                    } else {   // every column sees the same positions; padding columns hold q = 0
+                        sc[jn][c] = gq + ((c >> 1) << 3) < valid ? sc[jn][c] * p.scale_log2 : -INFINITY;
+                    }
                 }
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -324,8 +423,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
                     bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
                     bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
-                    const float mn = fmaxf(m_run[jn][c], bm);
-                    const float mref = mn == -INFINITY ? 0.f : mn;   // a column with nothing visible yet
+                    const float mn = fmaxf(m_run[jn][c], bm);   // without CAUSAL finite: a block has a valid token
+                    const float mref = (CAUSAL && mn == -INFINITY) ? 0.f : mn;   // a column with nothing visible yet
                     const float alpha = fast_exp2(m_run[jn][c] - mref);
                     const float p0 = fast_exp2(sc[jn][c] - mref), p1 = fast_exp2(sc[jn][c + 2] - mref);
                     m_run[jn][c] = mn;
@@ -338,7 +437,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                         oacc[mt][jn][c + 2] *= alpha;
                     }
                 }
-                if constexpr (!FP8) {
+                if constexpr (!QUANT) {
                     const uint32_t h0 = pack_bf16(sc[jn][0], sc[jn][1]), h1 = pack_bf16(sc[jn][2], sc[jn][3]);
                     pb[jn][0] = movmatrix_trans(h0);
                     pb[jn][1] = movmatrix_trans(h1);
@@ -353,7 +452,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             }
 
             // ---- O^T += V^T P^T
-            if constexpr (!FP8) {
+            if constexpr (!QUANT) {
 #pragma unroll
                 for (int mt = 0; mt < C::MT; ++mt) {
                     uint32_t a[4];
@@ -364,6 +463,27 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                         if constexpr (PSPLIT) mma_bf16(oacc[mt][jn], a, pl[jn]);
                     }
                 }
+            } else if constexpr (INT4) {
+                // output channels permuted as for e4m3: m-row gq of tile mt is channel 16*gq + 2*mt,
+                // m-row gq+8 the next one; the thread's 16 channels are 8 bytes of each value row
+                uint32_t vw[4][2];   // value rows 2tg, 2tg+1, 2tg+8, 2tg+9
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const uint32_t a = st + swz64(kBS + 2 * tg + (r & 1) + (r >> 1) * 8, gq >> 1) + 8 * (gq & 1);
+                    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(vw[r][0]), "=r"(vw[r][1]) : "r"(a));
+                }
+#pragma unroll
+                for (int w = 0; w < 2; ++w)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        constexpr uint32_t kSel[4] = {0x4400u, 0x5511u, 0x6622u, 0x7733u};   // [A.b_k, A.b_k, B.b_k, B.b_k]
+                        const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], kSel[k]);
+                        const uint32_t x89 = __byte_perm(vw[2][w], vw[3][w], kSel[k]);
+                        const uint32_t a[4] = {nibbles_to_f16x2(x01), nibbles_to_f16x2(x01 >> 4),
+                                               nibbles_to_f16x2(x89), nibbles_to_f16x2(x89 >> 4)};
+#pragma unroll
+                        for (int jn = 0; jn < NT; ++jn) mma_f16(oacc[4 * w + k][jn], a, pb[jn]);
+                    }
             } else {
                 // output channels permuted: m-row r of tile mt is channel gq*D/8 + 2*mt (+1 for r >= 8)
                 uint32_t vw[4][D / 32];   // value rows 2tg, 2tg+1, 2tg+8, 2tg+9; D/8 code bytes each
@@ -442,7 +562,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int qi = 8 * jn + 2 * tg + (c & 1);
-                const int dim = FP8 ? gq * (D / 8) + 2 * mt + (c >> 1) : 16 * mt + gq + 8 * (c >> 1);
+                const int dim = QUANT ? gq * (D / 8) + 2 * mt + (c >> 1) : 16 * mt + gq + 8 * (c >> 1);
                 co[(warp * QW + qi) * D + dim] = oacc[mt][jn][c];
             }
     }
@@ -463,7 +583,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             L += e * cl[w * QW + qi];
             O += e * co[(w * QW + qi) * D + d];
         }
-        if constexpr (FP8) O *= __ldg(p.s_v + static_cast<size_t>(h) * D + d);
+        if constexpr (QUANT) O *= __ldg(p.s_v + static_cast<size_t>(h) * D + d);
         const size_t bq = col_orow(qi);
         if (ns == 1) {
             p.out[bq * D + d] = O / L;
@@ -517,19 +637,19 @@ struct DecodeKernel {
     int ctas_per_sm;
 };
 
-template <int D, int NT, bool FP8, bool PSPLIT>
+template <int D, int NT, int KIND, bool PSPLIT, bool CAUSAL = false>
 DecodeKernel decode_instance()
 {
     static DecodeKernel k = [] {
         DecodeKernel r;
-        r.fn = reinterpret_cast<const void *>(&decode_kernel<D, NT, FP8, PSPLIT>);
-        r.smem = decode_smem_bytes<D, NT, FP8>();
+        r.fn = reinterpret_cast<const void *>(&decode_kernel<D, NT, KIND, PSPLIT, CAUSAL>);
+        r.smem = decode_smem_bytes<D, NT, KIND>();
         r.ctas_per_sm = 0;
-        if (cudaFuncSetAttribute(&decode_kernel<D, NT, FP8, PSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 r.smem) == cudaSuccess) {
+        if (cudaFuncSetAttribute(&decode_kernel<D, NT, KIND, PSPLIT, CAUSAL>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem) == cudaSuccess) {
             int n = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_kernel<D, NT, FP8, PSPLIT>, kThreads,
-                                                              r.smem) == cudaSuccess)
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_kernel<D, NT, KIND, PSPLIT, CAUSAL>,
+                                                              kThreads, r.smem) == cudaSuccess)
                 r.ctas_per_sm = n;
         }
         return r;
@@ -542,6 +662,7 @@ kvc_status run_decode(const kvc_pool *pool, DecodeParams &p, const DecodeKernel 
 // Kernel instance selection without launching (used by the allocation-free entry point).
 DecodeKernel select_decode_bf16(int D, int g);
 DecodeKernel select_decode_fp8(int D, int g);
+DecodeKernel select_decode_int4(int D, int g);
 kvc_status launch_split_merge(const DecodeParams &p, int D, cudaStream_t stream);
 
 }  // namespace kvc

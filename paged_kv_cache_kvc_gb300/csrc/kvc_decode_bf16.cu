@@ -8,21 +8,26 @@ namespace kvc {
 template <int D>
 static DecodeKernel pick_bf16(int NT, bool psplit)
 {
-    if (NT == 1) return psplit ? decode_instance<D, 1, false, true>() : decode_instance<D, 1, false, false>();
-    if (NT == 2) return psplit ? decode_instance<D, 2, false, true>() : decode_instance<D, 2, false, false>();
-    return psplit ? decode_instance<D, 4, false, true>() : decode_instance<D, 4, false, false>();
+    if (NT == 1) return psplit ? decode_instance<D, 1, KV_BF16, true>() : decode_instance<D, 1, KV_BF16, false>();
+    if (NT == 2) return psplit ? decode_instance<D, 2, KV_BF16, true>() : decode_instance<D, 2, KV_BF16, false>();
+    return psplit ? decode_instance<D, 4, KV_BF16, true>() : decode_instance<D, 4, KV_BF16, false>();
 }
 
 kvc_status launch_decode_bf16(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream)
 {
-    // KVC_PSPLIT=0 feeds the softmax weights to the value mixture as one bf16
-    // operand instead of a high/low pair (faster, ~8 fewer bits per weight).
-    static const bool psplit = [] {
-        const char *e = std::getenv("KVC_PSPLIT");
-        return !(e && e[0] == '0');
-    }();
+    // The softmax weights enter the value mixture as a bf16 high/low pair for up
+    // to 16 query columns; 32-column units (MQA, prefill tiles) take one bf16
+    // operand so their registers fit.  KVC_PSPLIT=0 / 1 forces either.
     const int NT = n_tiles(p.ppu * p.g);
+    const char *e = std::getenv("KVC_PSPLIT");
+    const bool psplit = e ? e[0] != '0' : NT <= 2;
     DecodeKernel k;
+    if (!p.lens) {   // prefill tiles: per-column causal lengths, 32 columns
+        if (pool->D == 64) k = decode_instance<64, 4, KV_BF16, false, true>();
+        else if (pool->D == 128) k = decode_instance<128, 4, KV_BF16, false, true>();
+        else return KVC_ERR_UNSUPPORTED;
+        return run_decode(pool, p, k, stream);
+    }
     switch (pool->D) {
     case 64: k = pick_bf16<64>(NT, psplit); break;
     case 128: k = pick_bf16<128>(NT, psplit); break;
@@ -38,9 +43,9 @@ namespace kvc {
 // The bf16 kernel instance kvc_decode_attn would launch for head width D and group size g.
 DecodeKernel select_decode_bf16(int D, int g)
 {
+    const int NT = n_tiles(g);
     const char *e = std::getenv("KVC_PSPLIT");
-    const bool psplit = !(e && e[0] == '0');
-    const int NT = g <= 8 ? 1 : (g <= 16 ? 2 : 4);
+    const bool psplit = e ? e[0] != '0' : NT <= 2;
     if (D == 64) return pick_bf16<64>(NT, psplit);
     if (D == 128) return pick_bf16<128>(NT, psplit);
     return DecodeKernel{nullptr, 0, 0};

@@ -7,9 +7,10 @@ kvc_status launch_decode_fp8(const kvc_pool *pool, DecodeParams &p, cudaStream_t
 {
     const int NT = n_tiles(p.ppu * p.g);
     if (pool->D != 128) return KVC_ERR_UNSUPPORTED;
-    DecodeKernel k = NT == 1 ? decode_instance<128, 1, true, false>()
-                   : NT == 2 ? decode_instance<128, 2, true, false>()
-                             : decode_instance<128, 4, true, false>();
+    if (!p.lens) return run_decode(pool, p, decode_instance<128, 4, KV_E4M3, false, true>(), stream);
+    DecodeKernel k = NT == 1 ? decode_instance<128, 1, KV_E4M3, false>()
+                   : NT == 2 ? decode_instance<128, 2, KV_E4M3, false>()
+                             : decode_instance<128, 4, KV_E4M3, false>();
     return run_decode(pool, p, k, stream);
 }
 
@@ -22,9 +23,9 @@ DecodeKernel select_decode_fp8(int D, int g)
 {
     const int NT = g <= 8 ? 1 : (g <= 16 ? 2 : 4);
     if (D != 128) return DecodeKernel{nullptr, 0, 0};
-    return NT == 1 ? decode_instance<128, 1, true, false>()
-         : NT == 2 ? decode_instance<128, 2, true, false>()
-                   : decode_instance<128, 4, true, false>();
+    return NT == 1 ? decode_instance<128, 1, KV_E4M3, false>()
+         : NT == 2 ? decode_instance<128, 2, KV_E4M3, false>()
+                   : decode_instance<128, 4, KV_E4M3, false>();
 }
 
 }  // namespace kvc

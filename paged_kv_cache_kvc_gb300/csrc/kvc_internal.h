@@ -14,7 +14,8 @@
 
 struct kvc_pool {
     int64_t N;            // physical blocks
-    int32_t bs, L, H_KV, D, dtype, s, device;
+    int32_t bs, L, H_KV, D, dtype, s, device;   // s: bytes per element (0 for int4)
+    int32_t bits;         // bits per stored element: 16, 8 or 4
     uint8_t *base;        // pool bytes
     size_t layer_bytes, pool_bytes;
     float *scales;        // [L][2][H_KV][D] (e4m3 pools)
@@ -69,6 +70,7 @@ kvc_status check_device(const kvc_pool *pool);
 // Launchers implemented per element type.
 kvc_status launch_decode_bf16(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream);
 kvc_status launch_decode_fp8(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream);
+kvc_status launch_decode_int4(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream);
 
 // Split-K sizing: blocks per split and the split count for a batch.
 void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits,

@@ -89,7 +89,9 @@ extern "C" kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, con
     p.err = pool->err;
 
     const DecodeKernel k =
-        pool->dtype == KVC_FP8_E4M3 ? select_decode_fp8(pool->D, p.g) : select_decode_bf16(pool->D, p.g);
+        pool->dtype == KVC_FP8_E4M3 ? select_decode_fp8(pool->D, p.g)
+        : pool->dtype == KVC_INT4   ? select_decode_int4(pool->D, p.g)
+                                    : select_decode_bf16(pool->D, p.g);
     if (!k.fn) return KVC_ERR_UNSUPPORTED;
     if (k.ctas_per_sm <= 0) return KVC_ERR_CUDA;
     choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits, n_tiles(p.g));

@@ -63,8 +63,12 @@ class Workload:
         return int(self.block_tables.shape[1])
 
     @property
-    def elem_bytes(self) -> int:
-        return 1 if self.dtype == "fp8" else 2
+    def elem_bits(self) -> int:
+        return {"bf16": 16, "fp8": 8, "int4": 4}[self.dtype]
+
+    @property
+    def elem_bytes(self) -> float:
+        return self.elem_bits / 8
 
     @property
     def scale(self) -> float:
@@ -114,7 +118,7 @@ class Workload:
     # ------------------------------------------------------------ bytes
     def kv_bytes_read(self) -> int:
         """Valid cached K+V bytes one decode-attention pass reads per layer."""
-        return int(self.lens_post.astype(np.int64).sum()) * 2 * self.H_KV * self.d_h * self.elem_bytes
+        return int(self.lens_post.astype(np.int64).sum()) * 2 * self.H_KV * self.d_h * self.elem_bits // 8
 
 
 def _tables(lens_need: np.ndarray, perm: np.ndarray, bs: int, max_blocks: int,
@@ -152,7 +156,7 @@ def make_workload(name: str, seed: int = 0, **kw) -> Workload:
     if name == "llama_gqa":     # B=32, context 8192, one layer
         return _uniform(name, seed, B=32, H_Q=32, H_KV=8, d=128, ctx=8192, L=1, dtype="bf16")
 
-    if name.startswith("sweep_"):   # sweep_hkv{32,8,1}_{bf16,fp8}: B=8, context 32768
+    if name.startswith("sweep_"):   # sweep_hkv{32,8,1}_{bf16,fp8,int4}: B=8, context 32768
         _, hk, dt = name.split("_")
         return _uniform(name, seed, B=8, H_Q=32, H_KV=int(hk[3:]), d=128, ctx=32768, L=1, dtype=dt)
 
@@ -208,4 +212,5 @@ def _ragged_prefix(seed, B=64, shared=1200, chunk=600, lo=128, hi=32768) -> Work
 
 WORKLOADS = ["tiny", "llama_gqa", "ragged_prefix",
              "sweep_hkv32_bf16", "sweep_hkv8_bf16", "sweep_hkv1_bf16",
-             "sweep_hkv32_fp8", "sweep_hkv8_fp8", "sweep_hkv1_fp8", "full_pool"]
+             "sweep_hkv32_fp8", "sweep_hkv8_fp8", "sweep_hkv1_fp8", "full_pool",
+             "sweep_hkv32_int4", "sweep_hkv8_int4", "sweep_hkv1_int4"]

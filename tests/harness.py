@@ -16,7 +16,7 @@ import synth
 from synth.workloads import K_KIND, V_KIND, Workload
 
 # tolerances on attention outputs (fp32 accumulation on the GPU vs fp64 oracle)
-TOL_OUT = {"bf16": 1e-2, "fp8": 3e-2}
+TOL_OUT = {"bf16": 1e-2, "fp8": 3e-2, "int4": 3e-2}
 TOL_LSE_REL = 2e-3
 
 
@@ -90,7 +90,7 @@ class GpuCase:
 
     def __init__(self, kvc, w: Workload, fill_byte: int = 0xFF, device="cuda"):
         self.kvc, self.w, self.device = kvc, w, device
-        dt = kvc.KVC_FP8_E4M3 if w.dtype == "fp8" else kvc.KVC_BF16
+        dt = {"bf16": kvc.KVC_BF16, "fp8": kvc.KVC_FP8_E4M3, "int4": kvc.KVC_INT4}[w.dtype]
         self.pool = kvc.kvc_pool_create(w.num_blocks, w.bs, w.L, w.H_KV, w.d_h, dt)
         self.pool.bytes_view().fill_(fill_byte)
         self.bt = dev_i32(w.block_tables, device)
@@ -103,8 +103,8 @@ class GpuCase:
         if len(ld.k_ctx) == 0:
             return
         k, v = dev_bits(ld.k_ctx, self.device), dev_bits(ld.v_ctx, self.device)
-        if w.dtype == "fp8" and calibrate:
-            kvc.kvc_calibrate_fp8(self.pool, layer, k, v)
+        if w.dtype != "bf16" and calibrate:
+            kvc.kvc_calibrate_scales(self.pool, layer, k, v)
         unit_bt = dev_i32(w.block_tables[ld.rows], self.device)
         max_tok = int(np.max(ld.cu[1:] - ld.cu[:-1]))
         kvc.kvc_write_tokens(self.pool, layer, unit_bt, dev_i32(ld.start, self.device),
@@ -146,10 +146,12 @@ class OracleCase:
 
     def run_layer(self, ld: LayerData, decode: bool = True, image: bool = True):
         o, w = self.oracle, self.w
-        s = 1 if w.dtype == "fp8" else 2
+        s = {"bf16": 2, "fp8": 1, "int4": "int4"}[w.dtype]
         scales = None
         if w.dtype == "fp8":
             scales = np.stack([o.fp8_scales(ld.k_ctx), o.fp8_scales(ld.v_ctx)]).astype(np.float32)
+        elif w.dtype == "int4":
+            scales = np.stack([o.int4_scales(ld.k_ctx), o.int4_scales(ld.v_ctx)]).astype(np.float32)
         img = None
         if image:
             img = o.PoolImage(w.num_blocks, w.bs, 1, w.H_KV, w.d_h, s, fill=self.fill)
@@ -164,10 +166,12 @@ class OracleCase:
             if scales is None:
                 sk, sv, nk, nv = ld.k_ctx, ld.v_ctx, ld.k_new, ld.v_new
             else:
-                sk, sv = o.quantize_e4m3(ld.k_ctx, scales[0]), o.quantize_e4m3(ld.v_ctx, scales[1])
-                nk, nv = o.quantize_e4m3(ld.k_new, scales[0]), o.quantize_e4m3(ld.v_new, scales[1])
+                qz = o.quantize_e4m3 if w.dtype == "fp8" else o.quantize_int4
+                sk, sv = qz(ld.k_ctx, scales[0]), qz(ld.v_ctx, scales[1])
+                nk, nv = qz(ld.k_new, scales[0]), qz(ld.v_new, scales[1])
             K, V, cu = logical_lists(w, ld, sk, sv, nk, nv)
-            out, lse = o.decode(ld.q, K, V, cu, w.lens_post.astype(np.int64), w.H_KV, scales=scales, scale=w.scale)
+            out, lse = o.decode(ld.q, K, V, cu, w.lens_post.astype(np.int64), w.H_KV, scales=scales, scale=w.scale,
+                                kind=w.dtype)
             res.update(out=out, lse=lse, K=K, V=V, cu=cu)
         return res
 

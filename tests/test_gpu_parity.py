@@ -34,7 +34,7 @@ def _run(kvc, w, layers=(0,), fill=0xFF, bytes_check=True, decode_layers=None):
             assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
             dec = decode_layers is None or layer in decode_layers
             ref = orc.run_layer(ld, decode=dec, image=bytes_check)
-            if w.dtype == "fp8":
+            if w.dtype != "bf16":
                 got_sc = g.pool.scales_view()[layer].cpu().numpy()
                 assert np.array_equal(got_sc.view(np.uint32), ref["scales"].view(np.uint32)), "scales differ"
             if bytes_check:
@@ -58,7 +58,8 @@ def test_llama_gqa(kvc):
 
 
 @pytest.mark.parametrize("name", ["sweep_hkv8_bf16", "sweep_hkv8_fp8", "sweep_hkv32_bf16", "sweep_hkv32_fp8",
-                                  "sweep_hkv1_bf16", "sweep_hkv1_fp8"])
+                                  "sweep_hkv1_bf16", "sweep_hkv1_fp8", "sweep_hkv8_int4", "sweep_hkv1_int4",
+                                  "sweep_hkv32_int4"])
 def test_sweep(kvc, name):
     _run(kvc, synth.make_workload(name, seed=0))
 
@@ -165,7 +166,7 @@ def test_short_and_boundary_lengths(kvc, d_h):
             os.environ.pop("KVC_SPLIT_CHUNK", None)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "int4"])
 @pytest.mark.parametrize("H_KV", [32, 16, 8, 4, 2, 1])
 def test_group_sizes(kvc, H_KV, dtype):
     """GQA group sizes 1 (MHA) .. 32 (MQA) with ragged lengths."""
@@ -401,7 +402,8 @@ def test_launches_are_counted(kvc):
         g.close()
 
 
-@pytest.mark.parametrize("case", ["tiny", "boundary", "boundary_split4", "fp8_gqa", "mqa", "mha_fp8"])
+@pytest.mark.parametrize("case", ["tiny", "boundary", "boundary_split4", "fp8_gqa", "mqa", "mha_fp8", "int4_gqa",
+                                  "int4_mqa"])
 def test_fused_step_equals_append_then_decode(kvc, case):
     """kvc_decode_step (append + attention in one launch) leaves the same pool
     bytes and gives bit-identical outputs to kvc_append then kvc_decode_attn."""
@@ -411,7 +413,9 @@ def test_fused_step_equals_append_then_decode(kvc, case):
          "boundary_split4": lambda: _custom(B=len(lens), H_Q=32, H_KV=8, d_h=128, lens=lens),
          "fp8_gqa": lambda: _custom(B=3, H_Q=32, H_KV=8, d_h=128, lens=[7, 500, 2047], dtype="fp8"),
          "mqa": lambda: _custom(B=2, H_Q=32, H_KV=1, d_h=128, lens=[300, 65]),
-         "mha_fp8": lambda: _custom(B=2, H_Q=16, H_KV=16, d_h=128, lens=[48, 17], dtype="fp8")}[case]()
+         "mha_fp8": lambda: _custom(B=2, H_Q=16, H_KV=16, d_h=128, lens=[48, 17], dtype="fp8"),
+         "int4_gqa": lambda: _custom(B=3, H_Q=32, H_KV=8, d_h=128, lens=[0, 300, 1025], dtype="int4"),
+         "int4_mqa": lambda: _custom(B=2, H_Q=32, H_KV=1, d_h=128, lens=[77, 15], dtype="int4")}[case]()
     if case == "boundary_split4":
         os.environ["KVC_SPLIT_CHUNK"] = "4"
     try:
@@ -538,7 +542,7 @@ def test_allocator_copy_on_write_decode(kvc, dtype):
 
 
 @pytest.mark.parametrize("ppu", ["1", "3", "4", "8"])
-@pytest.mark.parametrize("H_KV,dtype", [(8, "bf16"), (2, "bf16"), (32, "bf16"), (8, "fp8")])
+@pytest.mark.parametrize("H_KV,dtype", [(8, "bf16"), (2, "bf16"), (32, "bf16"), (8, "fp8"), (8, "int4")])
 def test_prefill_tiles(kvc, ppu, H_KV, dtype):
     """Causal prefill chunks whose CTAs serve several query positions (tail tile
     shorter, chunks starting inside a block) against the oracle."""
@@ -562,12 +566,40 @@ def test_prefill_tiles(kvc, ppu, H_KV, dtype):
                 assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
                 sc = None
                 K, V = ld.k_ctx, ld.v_ctx
-                if dtype == "fp8":
+                if dtype != "bf16":
                     sc = g.pool.scales_view()[0].cpu().numpy()
-                    K, V = oracle.quantize_e4m3(K, sc[0]), oracle.quantize_e4m3(V, sc[1])
-                ro, rl = oracle.prefill(qc, K, V, q_start, H_KV, scales=sc, scale=w.scale)
+                    qz = oracle.quantize_e4m3 if dtype == "fp8" else oracle.quantize_int4
+                    K, V = qz(K, sc[0]), qz(V, sc[1])
+                ro, rl = oracle.prefill(qc, K, V, q_start, H_KV, scales=sc, scale=w.scale, kind=dtype)
                 check_attention(out, lse, ro, rl, dtype, f"prefill ppu={ppu} q_start={q_start} n_q={n_q}")
             finally:
                 g.close()
     finally:
         os.environ.pop("KVC_PREFILL_PPU", None)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.37, 2.0 ** -6])
+def test_int4_append_matches_codec_for_every_bf16(kvc, scale):
+    """Every bf16 bit pattern written through an int4 pool: the stored nibble is
+    the oracle's rint(fp32(x) / scale) clamped to [-7, 7] (+8), NaN -> 8, and the
+    two channels of a byte land in its low and high nibble."""
+    H, d = 1, 128
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    n_tok = 65536 // (H * d)
+    N = n_tok // 16
+    pool = kvc.kvc_pool_create(N, 16, 1, H, d, kvc.KVC_INT4)
+    try:
+        pool.bytes_view().fill_(0)
+        s = torch.full((H, d), scale, dtype=torch.float32, device="cuda")
+        kvc.kvc_pool_set_scales(pool, 0, s, s)
+        x = bits.reshape(n_tok, H, d)
+        bt = np.arange(N, dtype=np.int32).reshape(1, N)
+        kvc.kvc_write_tokens(pool, 0, dev_i32(bt), dev_i32([0]), dev_i32([0, n_tok]), dev_bits(x), dev_bits(x))
+        torch.cuda.synchronize()
+        img = oracle.PoolImage(N, 16, 1, H, d, "int4")
+        img.scales[0] = np.float32(scale)
+        img.write_tokens(0, bt, np.array([0], np.int32), np.array([0, n_tok], np.int64), x, x)
+        n, first = first_mismatch(pool.bytes_view().cpu().numpy(), img.bytes)
+        assert n == 0, f"{n} bytes differ, first at {first}"
+    finally:
+        pool.close()
