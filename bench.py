@@ -345,31 +345,69 @@ def main():
     clocks = clk.summary()
     assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
 
-    # ---- end to end through the public API: pinned host inputs in, results out, every step
+    # ---- end to end through the public API: every step copies its inputs from
+    # pinned host memory and its results back.  Copies run on their own streams,
+    # double-buffered, so step i's inputs arrive while step i-1 computes and its
+    # results leave while step i+1 computes (a serving loop's overlap).
     pin = lambda t: t.cpu().pin_memory()
     q_h, k_h, v_h = [pin(t) for t in q], [pin(t) for t in k_new], [pin(t) for t in v_new]
     bt_h, lp_h = pin(g.bt_dec), pin(g.lens_pre)
-    out_h = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
-    lse_h = [torch.empty_like(t, device="cpu").pin_memory() for t in lses]
+    sets = []          # two device buffer sets: inputs and results of alternate steps
+    for _ in range(2):
+        sets.append({"q": [torch.empty_like(t) for t in q], "k": [torch.empty_like(t) for t in k_new],
+                     "v": [torch.empty_like(t) for t in v_new], "bt": torch.empty_like(g.bt_dec),
+                     "lp": torch.empty_like(g.lens_pre), "out": [torch.empty_like(t) for t in outs],
+                     "lse": [torch.empty_like(t) for t in lses],
+                     "out_h": [torch.empty_like(t, device="cpu").pin_memory() for t in outs],
+                     "lse_h": [torch.empty_like(t, device="cpu").pin_memory() for t in lses]})
     h2d = sum(t.numel() * t.element_size() for t in q_h + k_h + v_h + [bt_h, lp_h])
-    d2h = sum(t.numel() * 4 for t in out_h + lse_h)
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    e_start.record(stream)
-    for i in range(K):
-        g.bt_dec.copy_(bt_h, non_blocking=True)
-        g.lens_pre.copy_(lp_h, non_blocking=True)
+    d2h = sum(t.numel() * 4 for t in sets[0]["out_h"] + sets[0]["lse_h"])
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    computed, drained = [ev(), ev()], [ev(), ev()]
+    for e in computed + drained:
+        e.record(stream)
+
+    def e2e_step(i):
+        b = sets[i % 2]
+        loaded = ev()
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(computed[i % 2])          # step i-2 has finished reading this set's inputs
+            b["bt"].copy_(bt_h, non_blocking=True)
+            b["lp"].copy_(lp_h, non_blocking=True)
+            for layer in range(L):
+                b["q"][layer].copy_(q_h[layer], non_blocking=True)
+                b["k"][layer].copy_(k_h[layer], non_blocking=True)
+                b["v"][layer].copy_(v_h[layer], non_blocking=True)
+            loaded.record(s_in)
+        stream.wait_event(loaded)
+        stream.wait_event(drained[i % 2])             # step i-2's results have left this set
         for layer in range(L):
-            q[layer].copy_(q_h[layer], non_blocking=True)
-            k_new[layer].copy_(k_h[layer], non_blocking=True)
-            v_new[layer].copy_(v_h[layer], non_blocking=True)
-            kvc.kvc_decode_step(g.pool, layer, q[layer], g.bt_dec, g.lens_pre, k_new[layer], v_new[layer],
-                                outs[layer], lses[layer], scale=w.scale)
-            out_h[layer].copy_(outs[layer], non_blocking=True)
-            lse_h[layer].copy_(lses[layer], non_blocking=True)
+            kvc.kvc_decode_step(g.pool, layer, b["q"][layer], b["bt"], b["lp"], b["k"][layer], b["v"][layer],
+                                b["out"][layer], b["lse"][layer], scale=w.scale, stream=stream)
+        computed[i % 2].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(computed[i % 2])
+            for layer in range(L):
+                b["out_h"][layer].copy_(b["out"][layer], non_blocking=True)
+                b["lse_h"][layer].copy_(b["lse"][layer], non_blocking=True)
+            drained[i % 2].record(s_out)
+
+    for i in range(min(4, K)):                        # warm the copy path
+        e2e_step(i)
+    barrier()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    s_in.wait_event(e_start)
+    for i in range(K):
+        e2e_step(i)
+    stream.wait_event(drained[(K - 1) % 2])           # the last results are on the host
     e_end.record(stream)
     barrier()
     e2e_ms = e_start.elapsed_time(e_end) / K
+    torch.cuda.synchronize()
+    for layer in range(L):                            # the copied-back results are the kernel's
+        assert torch.equal(sets[(K - 1) % 2]["out_h"][layer], sets[(K - 1) % 2]["out"][layer].cpu())
 
     # ---- max over ranks
     ms, e2e_ms, attn_ms = max_over_ranks([ms, e2e_ms, attn_ms], dist, "cuda")

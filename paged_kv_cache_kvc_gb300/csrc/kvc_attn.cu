@@ -61,29 +61,52 @@ void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_
     *max_splits = (max_blocks + ch - 1) / ch;
 }
 
-static kvc_status ensure_workspace(kvc_pool *pool, size_t bytes)
+// The workspace holds the arrival counters at its front, at a fixed place
+// whatever the batch (every launch leaves them at zero, so a later launch of
+// another shape may use them), then the partials.  It grows by reallocation
+// (zeroed); nothing in it outlives a launch except the zeroed counters.
+static size_t counter_region(size_t n) { return (n * sizeof(uint32_t) + 255) & ~size_t(255); }
+
+static kvc_status ensure_workspace(kvc_pool *pool, size_t counters, size_t bytes)
 {
-    if (bytes <= pool->ws_bytes) return KVC_OK;
+    if (counters <= pool->ws_counters && bytes <= pool->ws_bytes) return KVC_OK;
+    counters = std::max(counters, pool->ws_counters);
+    bytes = std::max(bytes, pool->ws_bytes);
     if (pool->ws) {
         cudaError_t e = cudaFree(pool->ws);
         pool->ws = nullptr;
-        pool->ws_bytes = 0;
+        pool->ws_bytes = pool->ws_counters = 0;
         if (e != cudaSuccess) return cuda_status(e);
     }
-    if (cudaMalloc(&pool->ws, bytes) != cudaSuccess) {
+    const size_t total = counter_region(counters) + bytes;
+    if (cudaMalloc(&pool->ws, total) != cudaSuccess) {
         (void)cudaGetLastError();
         pool->ws = nullptr;
         return KVC_ERR_OOM;
     }
     pool->ws_bytes = bytes;
-    return cuda_status(cudaMemset(pool->ws, 0, bytes));   // the arrival counters start at zero
+    pool->ws_counters = counters;
+    return cuda_status(cudaMemset(pool->ws, 0, total));   // the arrival counters start at zero
 }
 
-// partials o [B][H_Q][splits][D], (max, sum) [B][H_Q][splits], then arrival counters [B][H_KV]
+static uint32_t *ws_counters(const kvc_pool *pool) { return static_cast<uint32_t *>(pool->ws); }
+static float *ws_data(const kvc_pool *pool)
+{
+    return reinterpret_cast<float *>(static_cast<uint8_t *>(pool->ws) + counter_region(pool->ws_counters));
+}
+
+// split partials: o [units'][H_Q][splits][D], then (max, sum) [units'][H_Q][splits]
 static size_t workspace_bytes(int B, int H_Q, int max_splits, int D)
 {
     const size_t n = static_cast<size_t>(B) * H_Q * max_splits;
-    return n * D * sizeof(float) + n * sizeof(float2) + static_cast<size_t>(B) * H_Q * sizeof(uint32_t) + 256;
+    return n * D * sizeof(float) + n * sizeof(float2);
+}
+
+// persistent records: o [workers + units][g][D], then (max, sum) [workers + units][g]
+static size_t record_bytes(int workers, int units, int g, int D)
+{
+    const size_t n = (static_cast<size_t>(workers) + units) * g;
+    return n * D * sizeof(float) + n * sizeof(float2);
 }
 
 kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream)
@@ -93,14 +116,15 @@ kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel
     choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits, n_tiles(p.ppu * p.g));
     if (p.max_splits > 65535) return KVC_ERR_UNSUPPORTED;
     if (p.max_splits > 1) {
-        kvc_status st = ensure_workspace(pool, workspace_bytes(p.n_pos, p.H_Q, p.max_splits, pool->D));
+        kvc_status st = ensure_workspace(pool, static_cast<size_t>(p.B) * p.H_KV,
+                                         workspace_bytes(p.n_pos, p.H_Q, p.max_splits, pool->D));
         if (st != KVC_OK) return st;
         const size_t n = static_cast<size_t>(p.n_pos) * p.H_Q * p.max_splits;
-        p.part_o = static_cast<float *>(pool->ws);
-        p.part_ml = reinterpret_cast<float2 *>(static_cast<float *>(pool->ws) + n * pool->D);
+        p.part_o = ws_data(pool);
+        p.part_ml = reinterpret_cast<float2 *>(p.part_o + n * pool->D);
         // the last split CTA merges its group in the kernel when that is a small job (g * splits
         // partial rows); otherwise one merge CTA per (sequence, query head) does it afterwards
-        p.counters = (p.ppu * p.g * p.max_splits <= 64) ? reinterpret_cast<uint32_t *>(p.part_ml + n) : nullptr;
+        p.counters = (p.ppu * p.g * p.max_splits <= 64) ? ws_counters(pool) : nullptr;
     } else {
         p.part_o = nullptr;
         p.part_ml = nullptr;
@@ -117,6 +141,42 @@ kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel
         if (e != cudaSuccess) return cuda_status(e);
         g_launches.fetch_add(1, std::memory_order_relaxed);
     }
+    return KVC_OK;
+}
+
+kvc_status run_decode_persistent(kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream)
+{
+    // Opt-in (KVC_PERSISTENT=1): its static ranges finish with the slowest SM (on GB300
+    // the SMs of one launch stream at rates up to ~25 % apart), so the split kernel,
+    // whose CTAs the hardware hands to whichever SM frees first, stays the default.
+    // A split size forced by KVC_SPLIT_CHUNK selects the split kernel.
+    const char *opt = std::getenv("KVC_PERSISTENT");
+    if (!opt || opt[0] != '1') return KVC_ERR_UNSUPPORTED;
+    if (std::getenv("KVC_SPLIT_CHUNK")) return KVC_ERR_UNSUPPORTED;
+    if (!p.lens || p.B > kMaxSeqPersistent || !k.fn || k.ctas_per_sm <= 0) return KVC_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(p.B) * p.max_blocks >= (int64_t(1) << 31)) return KVC_ERR_UNSUPPORTED;
+    const int units = p.B * p.H_KV;
+    // ranges of the flattened blocks, each served by H_KV workers: every resident warp
+    // takes part, but no range is shorter than kMinBlocksPerWorker blocks at full tables
+    int64_t ranges = static_cast<int64_t>(pool->num_sms) * k.ctas_per_sm * kWarps / p.H_KV;
+    ranges = std::max<int64_t>(1, std::min(ranges, static_cast<int64_t>(p.B) * p.max_blocks / kMinBlocksPerWorker));
+    // a unit's merge reads (ranges per sequence + 2) records of g rows: keep it a small job
+    if (static_cast<double>(p.g) * (static_cast<double>(ranges) / p.B + 2.0) > 256.0) return KVC_ERR_UNSUPPORTED;
+    const int64_t workers = ranges * p.H_KV;
+    if (workers > static_cast<int64_t>(pool->num_sms) * k.ctas_per_sm * kWarps * 4) return KVC_ERR_UNSUPPORTED;
+    const int grid = static_cast<int>((workers + kWarps - 1) / kWarps);
+    const int nw = grid * kWarps;
+    kvc_status st = ensure_workspace(pool, static_cast<size_t>(units), record_bytes(nw, units, p.g, pool->D));
+    if (st != KVC_OK) return st;
+    p.part_o = ws_data(pool);
+    p.part_ml = reinterpret_cast<float2 *>(p.part_o + (static_cast<size_t>(nw) + units) * p.g * pool->D);
+    p.counters = ws_counters(pool);
+    p.chunk = 0;
+    p.max_splits = 0;
+    void *args[] = {const_cast<CUtensorMap *>(&pool->tmap), &p};
+    const cudaError_t e = cudaLaunchKernel(k.fn, dim3(grid), dim3(kThreads), args, k.smem, stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return KVC_OK;
 }
 
@@ -244,7 +304,12 @@ extern "C" kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_
     if (st != KVC_OK) return st;
     // the largest split count any batch of this size can get is the 16-block floor
     const int max_splits = (max_blocks + 15) / 16;
-    return ensure_workspace(pool, workspace_bytes(max_batch, num_q_heads, max_splits, pool->D));
+    const int g = num_q_heads / pool->H_KV;
+    const int workers = pool->num_sms * 8 * kWarps;   // the persistent kernel's records: at most 8 CTAs per SM
+    const size_t units = static_cast<size_t>(max_batch) * pool->H_KV;
+    return ensure_workspace(pool, units,
+                            std::max(workspace_bytes(max_batch, num_q_heads, max_splits, pool->D),
+                                     record_bytes(workers, static_cast<int>(units), g, pool->D)));
 }
 
 namespace kvc {

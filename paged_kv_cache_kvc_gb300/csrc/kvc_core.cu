@@ -430,7 +430,7 @@ extern "C" kvc_status kvc_pool_sync_status(kvc_pool *pool, kvc_stream_t stream)
         return KVC_ERR_CUDA;
     if ((bits & KVC_EBIT_TIMEOUT) && pool->ws) {
         // an expired wait may have left split arrival counters short of their count: restart them at zero
-        if (cudaMemset(pool->ws, 0, pool->ws_bytes) != cudaSuccess) return KVC_ERR_CUDA;
+        if (cudaMemset(pool->ws, 0, pool->ws_counters * sizeof(uint32_t)) != cudaSuccess) return KVC_ERR_CUDA;
     }
     if (bits & KVC_EBIT_BAD_BLOCK) return KVC_ERR_BAD_BLOCK;
     if (bits & KVC_EBIT_RANGE) return KVC_ERR_RANGE;

@@ -179,6 +179,187 @@ __device__ __forceinline__ void append_row(const DecodeParams &p, uint32_t st, i
     sts128(st + row_chunk<D, KIND>(kv * kBS + slot, ch), val);
 }
 
+// One 16-token block's update of a warp's running softmax state: scores of the
+// block's keys against the warp's query columns, masking (positions at or past
+// `valid` in the block; CAUSAL: per column, positions at or past clen), the
+// online rescale, and the value mixture.  `st` is the landed stage (keys in
+// rows 0..15, values in rows 16..31); tok0 is the block's first position.
+template <int D, int NT, int KIND, bool PSPLIT, bool CAUSAL>
+__device__ __forceinline__ void block_update(uint32_t st, const uint32_t (&qf)[NT][D / 16][2], float (&m_run)[NT][2],
+                                             float (&l_run)[NT][2], float (&oacc)[D / 16][NT][4], int valid, int tok0,
+                                             const int (&clen)[NT][2], float scale_log2, int lane)
+{
+    using C = DecodeCfg<D, KIND>;
+    constexpr bool INT4 = KIND == KV_INT4, QUANT = KIND != KV_BF16;
+    const int gq = lane >> 2, tg = lane & 3;
+    // ---- S^T = K Q^T
+    float sc[NT][4];
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn) sc[jn][0] = sc[jn][1] = sc[jn][2] = sc[jn][3] = 0.f;
+    if constexpr (!QUANT) {
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(a, st + swz((lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)));
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn) mma_bf16(sc[jn], a, qf[jn][kk]);
+        }
+    } else if constexpr (INT4) {
+        uint32_t kw[2][4];   // rows gq, gq+8: this thread's 32-channel chunk tg (8 nibbles a word)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const uint4 v = lds128(st + swz64(gq + 8 * r, tg));
+            kw[r][0] = v.x;
+            kw[r][1] = v.y;
+            kw[r][2] = v.z;
+            kw[r][3] = v.w;
+        }
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            const int sh = 8 * (kk & 1);   // nibbles (2e, 2e+4) and (2e+1, 2e+5) of word kk / 2
+            uint32_t a[4];
+            a[0] = nibbles_to_f16x2(kw[0][kk >> 1] >> sh);
+            a[2] = nibbles_to_f16x2(kw[0][kk >> 1] >> (sh + 4));
+            a[1] = nibbles_to_f16x2(kw[1][kk >> 1] >> sh);
+            a[3] = nibbles_to_f16x2(kw[1][kk >> 1] >> (sh + 4));
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn) mma_f16(sc[jn], a, qf[jn][kk]);
+        }
+    } else {
+        uint32_t kw[2][D / 16];   // rows gq, gq+8: this thread's D/4 code bytes each
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int u = 0; u < D / 64; ++u) {
+                const uint4 v = lds128(st + swz(gq + 8 * r, (D / 64) * tg + u));
+                kw[r][4 * u + 0] = v.x;
+                kw[r][4 * u + 1] = v.y;
+                kw[r][4 * u + 2] = v.z;
+                kw[r][4 * u + 3] = v.w;
+            }
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            uint32_t a[4];
+            e4m3x4_to_f16x2x2(kw[0][kk], a[0], a[2]);
+            e4m3x4_to_f16x2x2(kw[1][kk], a[1], a[3]);
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn) mma_f16(sc[jn], a, qf[jn][kk]);
+        }
+    }
+
+    // ---- online softmax (log2 domain); column = query head, rows = tokens gq, gq+8
+    uint32_t pb[NT][2], pl[NT][2];
+    #pragma unroll
+    for (int jn = 0; jn < NT; ++jn) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if constexpr (CAUSAL) {
+                const int tok = tok0 + gq + ((c >> 1) << 3);
+                sc[jn][c] = tok < clen[jn][c & 1] ? sc[jn][c] * scale_log2 : -INFINITY;
+            } else {   // every column sees the same positions; padding columns hold q = 0
+                sc[jn][c] = gq + ((c >> 1) << 3) < valid ? sc[jn][c] * scale_log2 : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float bm = fmaxf(sc[jn][c], sc[jn][c + 2]);
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
+            const float mn = fmaxf(m_run[jn][c], bm);   // without CAUSAL finite: a block has a valid token
+            const float mref = (CAUSAL && mn == -INFINITY) ? 0.f : mn;   // a column with nothing visible yet
+            const float alpha = fast_exp2(m_run[jn][c] - mref);
+            const float p0 = fast_exp2(sc[jn][c] - mref), p1 = fast_exp2(sc[jn][c + 2] - mref);
+            m_run[jn][c] = mn;
+            l_run[jn][c] = l_run[jn][c] * alpha + p0 + p1;
+            sc[jn][c] = p0;
+            sc[jn][c + 2] = p1;
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                oacc[mt][jn][c] *= alpha;
+                oacc[mt][jn][c + 2] *= alpha;
+            }
+        }
+        if constexpr (!QUANT) {
+            const uint32_t h0 = pack_bf16(sc[jn][0], sc[jn][1]), h1 = pack_bf16(sc[jn][2], sc[jn][3]);
+            pb[jn][0] = movmatrix_trans(h0);
+            pb[jn][1] = movmatrix_trans(h1);
+            if constexpr (PSPLIT) {
+                pl[jn][0] = movmatrix_trans(pack_bf16(sc[jn][0] - bf16_lo(h0), sc[jn][1] - bf16_hi(h0)));
+                pl[jn][1] = movmatrix_trans(pack_bf16(sc[jn][2] - bf16_lo(h1), sc[jn][3] - bf16_hi(h1)));
+            }
+        } else {
+            pb[jn][0] = movmatrix_trans(pack_f16(sc[jn][0], sc[jn][1]));
+            pb[jn][1] = movmatrix_trans(pack_f16(sc[jn][2], sc[jn][3]));
+        }
+    }
+
+    // ---- O^T += V^T P^T
+    if constexpr (!QUANT) {
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_trans(a, st + swz(kBS + (lane & 7) + ((lane >> 4) & 1) * 8, 2 * mt + ((lane >> 3) & 1)));
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn) {
+                mma_bf16(oacc[mt][jn], a, pb[jn]);
+                if constexpr (PSPLIT) mma_bf16(oacc[mt][jn], a, pl[jn]);
+            }
+        }
+    } else if constexpr (INT4) {
+        // output channels permuted as for e4m3: m-row gq of tile mt is channel 16*gq + 2*mt,
+        // m-row gq+8 the next one; the thread's 16 channels are 8 bytes of each value row
+        uint32_t vw[4][2];   // value rows 2tg, 2tg+1, 2tg+8, 2tg+9
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t a = st + swz64(kBS + 2 * tg + (r & 1) + (r >> 1) * 8, gq >> 1) + 8 * (gq & 1);
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(vw[r][0]), "=r"(vw[r][1]) : "r"(a));
+        }
+#pragma unroll
+        for (int w = 0; w < 2; ++w)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                constexpr uint32_t kSel[4] = {0x4400u, 0x5511u, 0x6622u, 0x7733u};   // [A.b_k, A.b_k, B.b_k, B.b_k]
+                const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], kSel[k]);
+                const uint32_t x89 = __byte_perm(vw[2][w], vw[3][w], kSel[k]);
+                const uint32_t a[4] = {nibbles_to_f16x2(x01), nibbles_to_f16x2(x01 >> 4),
+                                       nibbles_to_f16x2(x89), nibbles_to_f16x2(x89 >> 4)};
+#pragma unroll
+                for (int jn = 0; jn < NT; ++jn) mma_f16(oacc[4 * w + k][jn], a, pb[jn]);
+            }
+    } else {
+        // output channels permuted: m-row r of tile mt is channel gq*D/8 + 2*mt (+1 for r >= 8)
+        uint32_t vw[4][D / 32];   // value rows 2tg, 2tg+1, 2tg+8, 2tg+9; D/8 code bytes each
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int u = 0; u < D / 128; ++u) {
+                const uint4 v = lds128(st + swz(kBS + 2 * tg + (r & 1) + (r >> 1) * 8, (D / 128) * gq + u));
+                vw[r][4 * u + 0] = v.x;
+                vw[r][4 * u + 1] = v.y;
+                vw[r][4 * u + 2] = v.z;
+                vw[r][4 * u + 3] = v.w;
+            }
+#pragma unroll
+        for (int w = 0; w < D / 32; ++w) {
+            const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], 0x5140);
+            const uint32_t y01 = __byte_perm(vw[0][w], vw[1][w], 0x7362);
+            const uint32_t x89 = __byte_perm(vw[2][w], vw[3][w], 0x5140);
+            const uint32_t y89 = __byte_perm(vw[2][w], vw[3][w], 0x7362);
+            uint32_t a0[4], a1[4];
+            e4m3x4_to_f16x2x2(x01, a0[0], a0[1]);
+            e4m3x4_to_f16x2x2(x89, a0[2], a0[3]);
+            e4m3x4_to_f16x2x2(y01, a1[0], a1[1]);
+            e4m3x4_to_f16x2x2(y89, a1[2], a1[3]);
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn) {
+                mma_f16(oacc[2 * w][jn], a0, pb[jn]);
+                mma_f16(oacc[2 * w + 1][jn], a1, pb[jn]);
+            }
+        }
+    }
+}
+
 // CAUSAL: columns may see different numbers of positions (prefill tiles), so
 // the mask is per column and a column may see nothing in a block; decode
 // instances (every column sees the unit's whole length) skip both.
@@ -348,173 +529,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             if (p.k_new && blk0 + warp + kWarps * j == nblk - 1) append_row<D, KIND>(p, st, b, h, phys, valid - 1, lane);
             __syncwarp();
 
-            // ---- S^T = K Q^T
-            float sc[NT][4];
-#pragma unroll
-            for (int jn = 0; jn < NT; ++jn) sc[jn][0] = sc[jn][1] = sc[jn][2] = sc[jn][3] = 0.f;
-            if constexpr (!QUANT) {
-#pragma unroll
-                for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                    uint32_t a[4];
-                    ldsm_x4(a, st + swz((lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)));
-#pragma unroll
-                    for (int jn = 0; jn < NT; ++jn) mma_bf16(sc[jn], a, qf[jn][kk]);
-                }
-            } else if constexpr (INT4) {
-                uint32_t kw[2][4];   // rows gq, gq+8: this thread's 32-channel chunk tg (8 nibbles a word)
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const uint4 v = lds128(st + swz64(gq + 8 * r, tg));
-                    kw[r][0] = v.x;
-                    kw[r][1] = v.y;
-                    kw[r][2] = v.z;
-                    kw[r][3] = v.w;
-                }
-#pragma unroll
-                for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                    const int sh = 8 * (kk & 1);   // nibbles (2e, 2e+4) and (2e+1, 2e+5) of word kk / 2
-                    uint32_t a[4];
-                    a[0] = nibbles_to_f16x2(kw[0][kk >> 1] >> sh);
-                    a[2] = nibbles_to_f16x2(kw[0][kk >> 1] >> (sh + 4));
-                    a[1] = nibbles_to_f16x2(kw[1][kk >> 1] >> sh);
-                    a[3] = nibbles_to_f16x2(kw[1][kk >> 1] >> (sh + 4));
-#pragma unroll
-                    for (int jn = 0; jn < NT; ++jn) mma_f16(sc[jn], a, qf[jn][kk]);
-                }
-            } else {
-                uint32_t kw[2][D / 16];   // rows gq, gq+8: this thread's D/4 code bytes each
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-#pragma unroll
-                    for (int u = 0; u < D / 64; ++u) {
-                        const uint4 v = lds128(st + swz(gq + 8 * r, (D / 64) * tg + u));
-                        kw[r][4 * u + 0] = v.x;
-                        kw[r][4 * u + 1] = v.y;
-                        kw[r][4 * u + 2] = v.z;
-                        kw[r][4 * u + 3] = v.w;
-                    }
-#pragma unroll
-                for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                    uint32_t a[4];
-                    e4m3x4_to_f16x2x2(kw[0][kk], a[0], a[2]);
-                    e4m3x4_to_f16x2x2(kw[1][kk], a[1], a[3]);
-#pragma unroll
-                    for (int jn = 0; jn < NT; ++jn) mma_f16(sc[jn], a, qf[jn][kk]);
-                }
-            }
-
-            // ---- online softmax (log2 domain); column = query head, rows = tokens gq, gq+8
-            uint32_t pb[NT][2], pl[NT][2];
-            const int tok0 = (blk0 + warp + kWarps * j) * kBS;
-#pragma unroll
-            for (int jn = 0; jn < NT; ++jn) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if constexpr (CAUSAL) {
-                        const int tok = tok0 + gq + ((c >> 1) << 3);
-                        sc[jn][c] = tok < clen[jn][c & 1] ? sc[jn][c] * p.scale_log2 : -INFINITY;
-                    } else {   // every column sees the same positions; padding columns hold q = 0
-                        sc[jn][c] = gq + ((c >> 1) << 3) < valid ? sc[jn][c] * p.scale_log2 : -INFINITY;
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float bm = fmaxf(sc[jn][c], sc[jn][c + 2]);
-                    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
-                    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
-                    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
-                    const float mn = fmaxf(m_run[jn][c], bm);   // without CAUSAL finite: a block has a valid token
-                    const float mref = (CAUSAL && mn == -INFINITY) ? 0.f : mn;   // a column with nothing visible yet
-                    const float alpha = fast_exp2(m_run[jn][c] - mref);
-                    const float p0 = fast_exp2(sc[jn][c] - mref), p1 = fast_exp2(sc[jn][c + 2] - mref);
-                    m_run[jn][c] = mn;
-                    l_run[jn][c] = l_run[jn][c] * alpha + p0 + p1;
-                    sc[jn][c] = p0;
-                    sc[jn][c + 2] = p1;
-#pragma unroll
-                    for (int mt = 0; mt < C::MT; ++mt) {
-                        oacc[mt][jn][c] *= alpha;
-                        oacc[mt][jn][c + 2] *= alpha;
-                    }
-                }
-                if constexpr (!QUANT) {
-                    const uint32_t h0 = pack_bf16(sc[jn][0], sc[jn][1]), h1 = pack_bf16(sc[jn][2], sc[jn][3]);
-                    pb[jn][0] = movmatrix_trans(h0);
-                    pb[jn][1] = movmatrix_trans(h1);
-                    if constexpr (PSPLIT) {
-                        pl[jn][0] = movmatrix_trans(pack_bf16(sc[jn][0] - bf16_lo(h0), sc[jn][1] - bf16_hi(h0)));
-                        pl[jn][1] = movmatrix_trans(pack_bf16(sc[jn][2] - bf16_lo(h1), sc[jn][3] - bf16_hi(h1)));
-                    }
-                } else {
-                    pb[jn][0] = movmatrix_trans(pack_f16(sc[jn][0], sc[jn][1]));
-                    pb[jn][1] = movmatrix_trans(pack_f16(sc[jn][2], sc[jn][3]));
-                }
-            }
-
-            // ---- O^T += V^T P^T
-            if constexpr (!QUANT) {
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-                    uint32_t a[4];
-                    ldsm_x4_trans(a, st + swz(kBS + (lane & 7) + ((lane >> 4) & 1) * 8, 2 * mt + ((lane >> 3) & 1)));
-#pragma unroll
-                    for (int jn = 0; jn < NT; ++jn) {
-                        mma_bf16(oacc[mt][jn], a, pb[jn]);
-                        if constexpr (PSPLIT) mma_bf16(oacc[mt][jn], a, pl[jn]);
-                    }
-                }
-            } else if constexpr (INT4) {
-                // output channels permuted as for e4m3: m-row gq of tile mt is channel 16*gq + 2*mt,
-                // m-row gq+8 the next one; the thread's 16 channels are 8 bytes of each value row
-                uint32_t vw[4][2];   // value rows 2tg, 2tg+1, 2tg+8, 2tg+9
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const uint32_t a = st + swz64(kBS + 2 * tg + (r & 1) + (r >> 1) * 8, gq >> 1) + 8 * (gq & 1);
-                    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(vw[r][0]), "=r"(vw[r][1]) : "r"(a));
-                }
-#pragma unroll
-                for (int w = 0; w < 2; ++w)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        constexpr uint32_t kSel[4] = {0x4400u, 0x5511u, 0x6622u, 0x7733u};   // [A.b_k, A.b_k, B.b_k, B.b_k]
-                        const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], kSel[k]);
-                        const uint32_t x89 = __byte_perm(vw[2][w], vw[3][w], kSel[k]);
-                        const uint32_t a[4] = {nibbles_to_f16x2(x01), nibbles_to_f16x2(x01 >> 4),
-                                               nibbles_to_f16x2(x89), nibbles_to_f16x2(x89 >> 4)};
-#pragma unroll
-                        for (int jn = 0; jn < NT; ++jn) mma_f16(oacc[4 * w + k][jn], a, pb[jn]);
-                    }
-            } else {
-                // output channels permuted: m-row r of tile mt is channel gq*D/8 + 2*mt (+1 for r >= 8)
-                uint32_t vw[4][D / 32];   // value rows 2tg, 2tg+1, 2tg+8, 2tg+9; D/8 code bytes each
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int u = 0; u < D / 128; ++u) {
-                        const uint4 v = lds128(st + swz(kBS + 2 * tg + (r & 1) + (r >> 1) * 8, (D / 128) * gq + u));
-                        vw[r][4 * u + 0] = v.x;
-                        vw[r][4 * u + 1] = v.y;
-                        vw[r][4 * u + 2] = v.z;
-                        vw[r][4 * u + 3] = v.w;
-                    }
-#pragma unroll
-                for (int w = 0; w < D / 32; ++w) {
-                    const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], 0x5140);
-                    const uint32_t y01 = __byte_perm(vw[0][w], vw[1][w], 0x7362);
-                    const uint32_t x89 = __byte_perm(vw[2][w], vw[3][w], 0x5140);
-                    const uint32_t y89 = __byte_perm(vw[2][w], vw[3][w], 0x7362);
-                    uint32_t a0[4], a1[4];
-                    e4m3x4_to_f16x2x2(x01, a0[0], a0[1]);
-                    e4m3x4_to_f16x2x2(x89, a0[2], a0[3]);
-                    e4m3x4_to_f16x2x2(y01, a1[0], a1[1]);
-                    e4m3x4_to_f16x2x2(y89, a1[2], a1[3]);
-#pragma unroll
-                    for (int jn = 0; jn < NT; ++jn) {
-                        mma_f16(oacc[2 * w][jn], a0, pb[jn]);
-                        mma_f16(oacc[2 * w + 1][jn], a1, pb[jn]);
-                    }
-                }
-            }
+            block_update<D, NT, KIND, PSPLIT, CAUSAL>(st, qf, m_run, l_run, oacc, valid,
+                                                      (blk0 + warp + kWarps * j) * kBS, clen, p.scale_log2, lane);
         }
         __syncwarp();
         if (j + C::R < nmine) {
@@ -630,6 +646,400 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     if (threadIdx.x == 0) p.counters[static_cast<size_t>(b) * p.H_KV + h] = 0u;   // ready for the next launch
 }
 
+// ---------------------------------------------------------------------------
+// Balanced persistent decode.
+//
+// One launch of (SMs x resident CTAs) CTAs whose warps are independent
+// workers.  The batch's logical blocks are flattened sequence by sequence
+// into T positions; they are cut into NG equal contiguous ranges, and each
+// range is served by a group of H_KV workers, worker (r, h) reading KV head
+// h of range r's blocks.  Every worker streams the same number of blocks, so
+// the launch has no wave tail and each warp pays its prologue once; the
+// H_KV workers of a range read the H_KV adjacent head tiles of each physical
+// block at about the same time (as the split kernel's CTAs of one sequence
+// do).  A warp keeps its TMA ring running across sequence boundaries; on
+// entering a sequence it loads that unit's query fragments and clears its
+// running state.
+//
+// A unit u = (b, h) covered by one worker is written out by it directly.
+// Otherwise each covering worker writes a partial (m, l, o) record for its
+// share -- record (r + b) * H_KV + h, unique because the ranges and the
+// sequences are both contiguous and increasing -- and counts itself on the
+// unit's arrival counter; the worker that completes the count merges the
+// unit's records (the log-sum-exp merge of the split path) after its CTA's
+// warps have all finished their ranges, with the whole CTA.  Only a range's
+// first and last sequence can be shared, so a warp has at most two merges to
+// do.  The merge order is fixed, so results are the same from run to run.
+constexpr int kMaxSeqPersistent = 1024;   // sequences per launch (prefix sums held in shared memory)
+constexpr int kMinBlocksPerWorker = 8;
+
+template <int D, int KIND>
+__host__ __device__ constexpr int persistent_smem_bytes()
+{
+    using C = DecodeCfg<D, KIND>;
+    return 1024 /* alignment slack */ + kWarps * C::R * C::STAGE + kWarps * C::R * 8 /* mbarriers */ +
+           (kMaxSeqPersistent + 1) * 4 /* block prefix sums */ + (2 * kWarps + kWarps) * 4 /* merges, scan */;
+}
+
+// range holding flattened position P when T positions are cut into ng ranges
+__device__ __forceinline__ int range_of(int64_t P, int64_t T, int ng)
+{
+    return static_cast<int>(((P + 1) * ng - 1) / T);
+}
+
+template <int D, int NT, int KIND, bool PSPLIT>
+__global__ void __launch_bounds__(kThreads) decode_persistent_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                     const DecodeParams p)
+{
+    using C = DecodeCfg<D, KIND>;
+    constexpr bool QUANT = KIND != KV_BF16;
+    constexpr int PER = (kMaxSeqPersistent + kThreads - 1) / kThreads;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWarps * C::R * C::STAGE);
+    int *cum = reinterpret_cast<int *>(bars + kWarps * C::R);   // [B + 1] blocks of the sequences before b
+    int *pend = cum + kMaxSeqPersistent + 1;                     // [kWarps][2] units to merge, -1 = none
+    int *wsum = pend + 2 * kWarps;                               // [kWarps] scan carries
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tg = lane & 3;
+    const int B = p.B, H = p.H_KV, g = p.g;
+
+    // ---- prologue: block prefix sums over the sequences (a length out of range counts as empty)
+    int nb_loc[PER];
+    int tot = 0;
+    const int b0 = threadIdx.x * PER;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int b = b0 + i;
+        int nb = 0;
+        if (b < B) {
+            const int len = seq_len(p, b);
+            if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) {
+                if (blockIdx.x == 0) atomicOr(p.err, KVC_EBIT_RANGE);
+            } else {
+                nb = (len + kBS - 1) / kBS;
+            }
+        }
+        nb_loc[i] = nb;
+        tot += nb;
+    }
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    if (lane == 0) {
+        for (int s = 0; s < C::R; ++s) mbar_init(smem_u32(&bars[warp * C::R + s]), 1);
+        fence_barrier_init();
+    }
+    if (lane < 2) pend[2 * warp + lane] = -1;
+    if (threadIdx.x == 0) prefetch_tensormap(&tmap);
+    __syncthreads();
+    {
+        int run = incl - tot;
+        for (int w = 0; w < warp; ++w) run += wsum[w];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            if (b0 + i < B) cum[b0 + i] = run;
+            run += nb_loc[i];
+        }
+        if (threadIdx.x == kThreads - 1) cum[B] = run;
+    }
+    __syncthreads();
+
+    // empty sequences: zero output, lse = -inf
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        if (cum[b + 1] != cum[b]) continue;
+        for (int i = threadIdx.x; i < p.H_Q * D; i += kThreads) p.out[static_cast<size_t>(b) * p.H_Q * D + i] = 0.f;
+        if (p.lse)
+            for (int i = threadIdx.x; i < p.H_Q; i += kThreads) p.lse[static_cast<size_t>(b) * p.H_Q + i] = -INFINITY;
+    }
+
+    const int64_t T = cum[B];
+    if (T == 0) return;   // uniform across the CTA
+    const int NG = static_cast<int>(min(static_cast<int64_t>(gridDim.x) * kWarps / H,
+                                        max(static_cast<int64_t>(1), T / kMinBlocksPerWorker)));
+    const int W = warp * gridDim.x + blockIdx.x;   // consecutive workers sit on different SMs
+    const int r = W / H, h = W - r * H;            // range r, KV head h
+    const int64_t lo = r < NG ? (static_cast<int64_t>(r) * T) / NG : 0;
+    const int n = r < NG ? static_cast<int>((static_cast<int64_t>(r + 1) * T) / NG - lo) : 0;
+
+    const uint32_t st_base = smem_u32(smem + warp * C::R * C::STAGE);
+    const uint32_t bar_base = smem_u32(&bars[warp * C::R]);
+    const int64_t row_head = (static_cast<int64_t>(p.layer) * p.N) * H + h;
+
+    // Where local position jj of this worker lies: sequence, block, table entry.
+    // Lanes hold 32 consecutive positions per batch (current and next batch).
+    auto lookup = [&](int jj, int32_t &b, int32_t &blk, int32_t &phys) {
+        if (jj >= n) {
+            b = -1;
+            blk = 0;
+            phys = -1;
+            return;
+        }
+        const int64_t P = lo + jj;
+        int a = 0, z = B;   // largest b with cum[b] <= P (a sequence with blocks)
+        while (z - a > 1) {
+            const int m = (a + z) >> 1;
+            if (cum[m] <= P) a = m;
+            else z = m;
+        }
+        b = a;
+        blk = static_cast<int>(P - cum[a]);
+        phys = __ldg(p.bt + static_cast<int64_t>(a) * p.bt_stride + blk);
+    };
+    int32_t c_b, c_blk, c_ph, n_b, n_blk, n_ph;
+    lookup(lane, c_b, c_blk, c_ph);
+    lookup(32 + lane, n_b, n_blk, n_ph);
+    auto pick = [&](int32_t cur, int32_t nxt, int jj, int jbase) {
+        return __shfl_sync(kFull, (jj - jbase < 32) ? cur : nxt, (jj - jbase) & 31);
+    };
+    auto issue = [&](int jj, int jbase) {   // warp-collective; lane 0 issues
+        const int32_t phys = pick(c_ph, n_ph, jj, jbase);
+        if (lane == 0) {
+            const uint32_t bar = bar_base + 8u * static_cast<uint32_t>(jj % C::R);
+            if (phys < 0 || static_cast<int64_t>(phys) >= p.N) {
+                atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
+                mbar_arrive(bar);   // complete the phase without data; the consumer skips it
+            } else {
+                const int32_t y = static_cast<int32_t>((row_head + static_cast<int64_t>(phys) * H) * C::BOX_ROWS);
+                const uint32_t dst = st_base + static_cast<uint32_t>((jj % C::R) * C::STAGE);
+                mbar_arrive_expect_tx(bar, C::STAGE);
+#pragma unroll
+                for (int band = 0; band < C::BANDS; ++band)
+                    tma_load_2d(dst + band * C::BOX_BYTES, &tmap, bar, band * C::BOX_X, y);
+            }
+        }
+    };
+    for (int jj = 0; jj < min(C::R, n); ++jj) issue(jj, 0);
+
+    uint32_t qf[NT][C::KSTEPS][2];
+    float m_run[NT][2], l_run[NT][2];
+    float oacc[C::MT][NT][4];
+    int clen[NT][2];   // unused by non-causal blocks
+#pragma unroll
+    for (int jn = 0; jn < NT; ++jn) clen[jn][0] = clen[jn][1] = 0;
+
+    int ub = -1, ulen = 0, unblk = 0, u_nr = 0;   // the unit (ub, h) in progress
+    int npend = 0;
+    const int uh = h;
+
+    auto start_unit = [&](int32_t b) {
+        ub = b;
+        ulen = seq_len(p, ub);
+        unblk = cum[ub + 1] - cum[ub];
+        const int r0 = range_of(cum[ub], T, NG);
+        u_nr = range_of(cum[ub + 1] - 1, T, NG) - r0 + 1;
+        const int hq0 = uh * g;
+#pragma unroll
+        for (int jn = 0; jn < NT; ++jn) {
+            const int qi = 8 * jn + gq;
+            const bool real = qi < g;
+            const uint16_t *qrow = p.q + (real ? static_cast<size_t>(ub) * p.H_Q + hq0 + qi : static_cast<size_t>(0)) * D;
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                if constexpr (!QUANT) {
+                    qf[jn][kk][0] = real ? *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 2 * tg) : 0u;
+                    qf[jn][kk][1] = real ? *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 8 + 2 * tg) : 0u;
+                } else if constexpr (KIND == KV_INT4) {
+                    const int base = 32 * tg + 8 * (kk >> 1) + 2 * (kk & 1);
+                    const float *sk = p.s_k + static_cast<size_t>(uh) * D;
+                    auto qv = [&](int c) {
+                        const uint16_t raw = real ? qrow[c] : uint16_t(0);
+                        return __uint_as_float(static_cast<uint32_t>(raw) << 16) * __ldg(sk + c);
+                    };
+                    qf[jn][kk][0] = pack_f16(qv(base), qv(base + 4));
+                    qf[jn][kk][1] = pack_f16(qv(base + 1), qv(base + 5));
+                } else {
+                    const int c0 = (D / 4) * tg + 4 * kk;
+                    const uint2 raw = real ? *reinterpret_cast<const uint2 *>(qrow + c0) : make_uint2(0u, 0u);
+                    const float *sk = p.s_k + static_cast<size_t>(uh) * D + c0;
+                    qf[jn][kk][0] = pack_f16(bf16_lo(raw.x) * __ldg(sk + 0), bf16_hi(raw.x) * __ldg(sk + 1));
+                    qf[jn][kk][1] = pack_f16(bf16_lo(raw.y) * __ldg(sk + 2), bf16_hi(raw.y) * __ldg(sk + 3));
+                }
+            }
+        }
+#pragma unroll
+        for (int jn = 0; jn < NT; ++jn) {
+            m_run[jn][0] = m_run[jn][1] = -INFINITY;
+            l_run[jn][0] = l_run[jn][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) oacc[mt][jn][0] = oacc[mt][jn][1] = oacc[mt][jn][2] = oacc[mt][jn][3] = 0.f;
+        }
+    };
+
+    // Output channel of accumulator element (mt, c) for this thread (e4m3 / int4 permute channels).
+    auto dim_of = [&](int mt, int c) { return QUANT ? gq * (D / 8) + 2 * mt + (c >> 1) : 16 * mt + gq + 8 * (c >> 1); };
+
+    auto finish_unit = [&]() {
+#pragma unroll
+        for (int jn = 0; jn < NT; ++jn)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float l = l_run[jn][c];
+                l += __shfl_xor_sync(kFull, l, 4);
+                l += __shfl_xor_sync(kFull, l, 8);
+                l += __shfl_xor_sync(kFull, l, 16);
+                l_run[jn][c] = l;
+            }
+        const size_t row0 = static_cast<size_t>(ub) * p.H_Q + static_cast<size_t>(uh) * g;   // first out row
+        if (u_nr == 1) {
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn)
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int qi = 8 * jn + 2 * tg + (c & 1);
+                        if (qi >= g) continue;
+                        const int dim = dim_of(mt, c);
+                        float o = oacc[mt][jn][c] / l_run[jn][c & 1];
+                        if constexpr (QUANT) o *= __ldg(p.s_v + static_cast<size_t>(uh) * D + dim);
+                        p.out[(row0 + qi) * D + dim] = o;
+                    }
+            if (p.lse && gq == 0)
+#pragma unroll
+                for (int jn = 0; jn < NT; ++jn)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int qi = 8 * jn + 2 * tg + c;
+                        if (qi < g) p.lse[row0 + qi] = (m_run[jn][c] + log2f(l_run[jn][c])) * kLn2;
+                    }
+            return;
+        }
+        const int u = ub * H + uh;
+        const size_t rec = (static_cast<size_t>(r + ub) * H + uh) * g;   // this worker's record of unit u
+#pragma unroll
+        for (int jn = 0; jn < NT; ++jn)
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int qi = 8 * jn + 2 * tg + (c & 1);
+                    if (qi < g) p.part_o[(rec + qi) * D + dim_of(mt, c)] = oacc[mt][jn][c];
+                }
+        if (gq == 0)
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int qi = 8 * jn + 2 * tg + c;
+                    if (qi < g) p.part_ml[rec + qi] = make_float2(m_run[jn][c], l_run[jn][c]);
+                }
+        __threadfence();   // release the record before counting it
+        __syncwarp();
+        uint32_t prev = 0;
+        if (lane == 0) prev = atomicAdd(p.counters + u, 1u);
+        prev = __shfl_sync(kFull, prev, 0);
+        if (prev == static_cast<uint32_t>(u_nr - 1)) {   // the unit's last share: merge it at the end
+            if (lane == 0 && npend < 2) pend[2 * warp + npend] = u;
+            ++npend;
+        }
+    };
+
+    int j = 0;
+    bool timed_out = false;
+    for (; j < n; ++j) {
+        const int jbase = j & ~31;
+        if (j > 0 && (j & 31) == 0) {
+            c_b = n_b;
+            c_blk = n_blk;
+            c_ph = n_ph;
+            lookup(j + 32 + lane, n_b, n_blk, n_ph);
+        }
+        const int s = j % C::R;
+        const bool ok = mbar_wait_bounded(bar_base + 8u * s, static_cast<uint32_t>((j / C::R) & 1));
+        if (!__all_sync(kFull, ok)) {
+            timed_out = true;
+            break;
+        }
+        const int32_t b = pick(c_b, n_b, j, jbase);
+        const int32_t blk = pick(c_blk, n_blk, j, jbase);
+        const int32_t phys = pick(c_ph, n_ph, j, jbase);
+        if (b != ub) {
+            if (ub >= 0) finish_unit();
+            start_unit(b);
+        }
+        if (phys >= 0 && static_cast<int64_t>(phys) < p.N) {
+            const uint32_t st = st_base + static_cast<uint32_t>(s * C::STAGE);
+            const int valid = min(kBS, ulen - blk * kBS);
+            if (KIND != KV_INT4 && valid < kBS) {   // value rows past the sequence end may hold NaN
+                const int nz = (kBS - valid) * C::BANDS * 8;
+                for (int i = lane; i < nz; i += 32) sts128_zero(st + swz(kBS + valid + i / (C::BANDS * 8), i % (C::BANDS * 8)));
+            }
+            if (p.k_new && blk == unblk - 1) append_row<D, KIND>(p, st, ub, uh, phys, valid - 1, lane);
+            __syncwarp();
+            block_update<D, NT, KIND, PSPLIT, false>(st, qf, m_run, l_run, oacc, valid, blk * kBS, clen,
+                                                     p.scale_log2, lane);
+        }
+        __syncwarp();
+        if (j + C::R < n) {
+            if (lane == 0) fence_proxy_async_smem();
+            issue(j + C::R, jbase);
+        }
+    }
+
+    if (timed_out) {   // record, then let copies already in flight land before the CTA exits
+        if (lane == 0) {
+            atomicOr(p.err, KVC_EBIT_TIMEOUT);
+            for (int jj = j; jj < min(n, j + C::R); ++jj)
+                (void)mbar_wait_bounded(bar_base + 8u * (jj % C::R), static_cast<uint32_t>((jj / C::R) & 1), 100000000ull);
+        }
+        __syncwarp();
+    } else if (ub >= 0) {
+        finish_unit();
+    }
+    if (npend > 2 && lane == 0) atomicOr(p.err, KVC_EBIT_RANGE);   // cannot happen: only first and last units are shared
+
+    // ---- merges of the units whose last share finished in this CTA (whole CTA, after every warp's range)
+    __syncthreads();
+    __threadfence();
+    for (int k = 0; k < 2 * kWarps; ++k) {
+        const int u = pend[k];
+        if (u < 0) continue;
+        const int b = u / H, hu = u - b * H;
+        const int r0 = range_of(cum[b], T, NG);
+        const int nr = range_of(cum[b + 1] - 1, T, NG) - r0 + 1;
+        const size_t row0 = static_cast<size_t>(b) * p.H_Q + static_cast<size_t>(hu) * g;
+        auto rec_of = [&](int i) { return (static_cast<size_t>(r0 + i + b) * H + hu) * g; };
+        for (int i = threadIdx.x; i < g * (D / 4); i += kThreads) {
+            const int qi = i / (D / 4), d = 4 * (i - qi * (D / 4));
+            float M = -INFINITY;
+            for (int k2 = 0; k2 < nr; ++k2) M = fmaxf(M, __ldcg(&p.part_ml[rec_of(k2) + qi].x));
+            const float Mref = M == -INFINITY ? 0.f : M;
+            float L = 0.f;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int k2 = 0; k2 < nr; ++k2) {
+                const size_t rec = rec_of(k2) + qi;
+                const float2 ml = __ldcg(p.part_ml + rec);
+                const float4 o = __ldcg(reinterpret_cast<const float4 *>(p.part_o + rec * D + d));
+                const float e = fast_exp2(ml.x - Mref);
+                L += e * ml.y;
+                O.x += e * o.x;
+                O.y += e * o.y;
+                O.z += e * o.z;
+                O.w += e * o.w;
+            }
+            const float inv = 1.f / L;
+            float4 res = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+            if constexpr (QUANT) {
+                const float4 sv = __ldg(reinterpret_cast<const float4 *>(p.s_v + static_cast<size_t>(hu) * D + d));
+                res.x *= sv.x;
+                res.y *= sv.y;
+                res.z *= sv.z;
+                res.w *= sv.w;
+            }
+            *reinterpret_cast<float4 *>(p.out + (row0 + qi) * D + d) = res;
+            if (d == 0 && p.lse) p.lse[row0 + qi] = (M + log2f(L)) * kLn2;
+        }
+        if (threadIdx.x == 0) p.counters[u] = 0u;   // every share has arrived: ready for the next launch
+    }
+}
+
 // Fetch (and on first use configure) the kernel instance for a shape.
 struct DecodeKernel {
     const void *fn;
@@ -657,7 +1067,31 @@ DecodeKernel decode_instance()
     return k;
 }
 
+template <int D, int NT, int KIND, bool PSPLIT>
+DecodeKernel persistent_instance()
+{
+    static DecodeKernel k = [] {
+        DecodeKernel r;
+        r.fn = reinterpret_cast<const void *>(&decode_persistent_kernel<D, NT, KIND, PSPLIT>);
+        r.smem = persistent_smem_bytes<D, KIND>();
+        r.ctas_per_sm = 0;
+        if (cudaFuncSetAttribute(&decode_persistent_kernel<D, NT, KIND, PSPLIT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem) == cudaSuccess) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_persistent_kernel<D, NT, KIND, PSPLIT>,
+                                                              kThreads, r.smem) == cudaSuccess)
+                r.ctas_per_sm = n;
+        }
+        return r;
+    }();
+    return k;
+}
+
 kvc_status run_decode(const kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream);
+// Launch the balanced persistent decode kernel `k` when the batch suits it
+// (decode of at most kMaxSeqPersistent sequences whose per-unit merges stay
+// small); returns KVC_ERR_UNSUPPORTED, launching nothing, when it does not.
+kvc_status run_decode_persistent(kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream);
 
 // Kernel instance selection without launching (used by the allocation-free entry point).
 DecodeKernel select_decode_bf16(int D, int g);

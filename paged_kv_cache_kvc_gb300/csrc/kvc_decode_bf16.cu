@@ -6,6 +6,14 @@
 namespace kvc {
 
 template <int D>
+static DecodeKernel pick_bf16_persistent(int NT)
+{
+    if (NT == 1) return persistent_instance<D, 1, KV_BF16, true>();
+    if (NT == 2) return persistent_instance<D, 2, KV_BF16, true>();
+    return DecodeKernel{nullptr, 0, 0};   // 32-column groups keep the split kernel
+}
+
+template <int D>
 static DecodeKernel pick_bf16(int NT, bool psplit)
 {
     if (NT == 1) return psplit ? decode_instance<D, 1, KV_BF16, true>() : decode_instance<D, 1, KV_BF16, false>();
@@ -27,6 +35,12 @@ kvc_status launch_decode_bf16(const kvc_pool *pool, DecodeParams &p, cudaStream_
         else if (pool->D == 128) k = decode_instance<128, 4, KV_BF16, false, true>();
         else return KVC_ERR_UNSUPPORTED;
         return run_decode(pool, p, k, stream);
+    }
+    if (!e) {   // the balanced persistent kernel where the batch suits it
+        const DecodeKernel kp = pool->D == 64 ? pick_bf16_persistent<64>(NT)
+                              : pool->D == 128 ? pick_bf16_persistent<128>(NT) : DecodeKernel{nullptr, 0, 0};
+        const kvc_status st = run_decode_persistent(const_cast<kvc_pool *>(pool), p, kp, stream);
+        if (st != KVC_ERR_UNSUPPORTED) return st;
     }
     switch (pool->D) {
     case 64: k = pick_bf16<64>(NT, psplit); break;

@@ -15,6 +15,14 @@ DecodeKernel select_decode_int4(int D, int g)
 kvc_status launch_decode_int4(const kvc_pool *pool, DecodeParams &p, cudaStream_t stream)
 {
     if (pool->D != 128) return KVC_ERR_UNSUPPORTED;
+    if (p.lens) {   // the balanced persistent kernel where the batch suits it
+        const int NT = n_tiles(p.g);
+        const DecodeKernel kp = NT == 1 ? persistent_instance<128, 1, KV_INT4, false>()
+                              : NT == 2 ? persistent_instance<128, 2, KV_INT4, false>()
+                                        : DecodeKernel{nullptr, 0, 0};   // 32-column groups keep the split kernel
+        const kvc_status st = run_decode_persistent(const_cast<kvc_pool *>(pool), p, kp, stream);
+        if (st != KVC_ERR_UNSUPPORTED) return st;
+    }
     const DecodeKernel k = p.lens ? select_decode_int4(pool->D, p.ppu * p.g)
                                   : decode_instance<128, 4, KV_INT4, false, true>();   // prefill tiles
     if (!k.fn) return KVC_ERR_UNSUPPORTED;

@@ -23,8 +23,9 @@ struct kvc_pool {
     uint32_t *err;        // device error word
     CUtensorMap tmap;     // rows of D elements; box {128 B, 2*bs rows}; 128-byte swizzle
     bool tmap_ok;
-    void *ws;             // split-K partials
-    size_t ws_bytes;
+    void *ws;             // workspace: arrival counters [ws_counters], then split / record partials
+    size_t ws_bytes;      // partial bytes after the counter region
+    size_t ws_counters;   // arrival counters at the front (zero between launches)
     int num_sms;
 };
 
@@ -60,7 +61,9 @@ struct DecodeParams {
     const uint16_t *k_new;
     const uint16_t *v_new;
     uint8_t *pool;           // pool base (the fused append's global store)
-    // split-K arrival counters [B][H_KV], zero between launches; nullptr = merge in a separate kernel
+    // split-K arrival counters [B][H_KV], zero between launches; nullptr = merge in a separate kernel.
+    // The balanced persistent kernel uses part_o / part_ml as per-worker records
+    // [workers + B*H_KV][g][D] / [workers + B*H_KV][g] and counters per (b, h).
     uint32_t *counters;
 };
 

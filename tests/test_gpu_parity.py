@@ -185,6 +185,27 @@ def test_split_counts_agree(kvc):
             os.environ.pop("KVC_SPLIT_CHUNK", None)
 
 
+@pytest.mark.parametrize("case", ["workers_per_unit", "units_per_worker", "max_batch", "over_max_batch", "fp8", "int4"])
+def test_balanced_schedule(kvc, case):
+    """The balanced persistent kernel (decode batches of up to 1 024 sequences)
+    and the split kernel (KVC_PERSISTENT=0) both within tolerance of the oracle:
+    many workers sharing a unit (merged records), many short units per worker
+    (direct writes, empty sequences), the largest batch it takes and one past it."""
+    rng = np.random.default_rng(7)
+    w = {"workers_per_unit": lambda: _custom(B=8, H_Q=16, H_KV=4, d_h=128, lens=[3000, 2999, 3001, 2048, 1, 4000, 17, 3333]),
+         "units_per_worker": lambda: _custom(B=300, H_Q=8, H_KV=1, d_h=64, lens=rng.integers(0, 41, 300), seed=3),
+         "max_batch": lambda: _custom(B=1024, H_Q=8, H_KV=2, d_h=128, lens=rng.integers(0, 70, 1024), seed=4),
+         "over_max_batch": lambda: _custom(B=1025, H_Q=8, H_KV=2, d_h=128, lens=rng.integers(0, 70, 1025), seed=5),
+         "fp8": lambda: _custom(B=6, H_Q=32, H_KV=8, d_h=128, lens=[5000, 1, 0, 2500, 777, 4096], dtype="fp8"),
+         "int4": lambda: _custom(B=6, H_Q=32, H_KV=8, d_h=128, lens=[5000, 1, 0, 2500, 777, 4096], dtype="int4")}[case]()
+    for persistent in ("1", "0"):
+        os.environ["KVC_PERSISTENT"] = persistent
+        try:
+            _run(kvc, w, bytes_check=case not in ("max_batch", "over_max_batch"))
+        finally:
+            os.environ.pop("KVC_PERSISTENT", None)
+
+
 def test_block_permutation_bit_identical(kvc):
     """Same logical sequences, physical blocks permuted and tables rewritten:
     bit-identical outputs (logical order is what attention sees)."""
@@ -261,6 +282,12 @@ def test_empty_batch_and_empty_sequence(kvc):
         torch.cuda.synchronize()
         assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
         assert torch.all(torch.isfinite(out[1])) and torch.all(torch.isfinite(lse[1]))
+        out.fill_(7.0)
+        lse.fill_(7.0)
+        kvc.kvc_decode_attn(g.pool, 0, q, g.bt_dec, dev_i32([0, 0]), out, lse, scale=w.scale)   # nothing to read
+        torch.cuda.synchronize()
+        assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
     finally:
         g.close()
 
