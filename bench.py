@@ -42,7 +42,9 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ---------------------------------------------------------------- bytes
 def step_bytes(w) -> dict:
-    """Algorithmic bytes of one decode step of workload w (one layer)."""
+    """Algorithmic bytes of one step of workload w (one layer): the decode step
+    and, when the workload carries a prefill chunk, the chunk's attention (its
+    row's keys and values read once, its queries in, its outputs out)."""
     s = w.elem_bytes
     lens = w.lens_post.astype(np.int64)
     kv = int(lens.sum()) * 2 * w.H_KV * w.d_h * w.elem_bits // 8
@@ -51,9 +53,24 @@ def step_bytes(w) -> dict:
     out = w.B * w.H_Q * w.d_h * 4 + w.B * w.H_Q * 4
     append = int(2 * w.B * w.H_KV * w.d_h * (2 + s))
     lens_b = w.B * 4 * 2
-    return {"kv": kv, "table": table, "q": q, "out": out, "append": append, "lens": lens_b,
-            "attn_kernel": kv + table + q + out + w.B * 4,
-            "total": kv + table + q + out + append + lens_b}
+    r = {"kv": kv, "table": table, "q": q, "out": out, "append": append, "lens": lens_b}
+    if w.prefill is not None:
+        p = w.prefill
+        r["prefill_kv"] = p.total * 2 * w.H_KV * w.d_h * w.elem_bits // 8
+        r["prefill_table"] = -(-p.total // w.bs) * 4
+        r["prefill_q"] = p.n_q * w.H_Q * w.d_h * 2
+        r["prefill_out"] = p.n_q * w.H_Q * (w.d_h + 1) * 4
+    r["total"] = sum(r.values())
+    return r
+
+
+def prefill_flops(w) -> int:
+    """Scores and value mixture of the chunk: 4 d_h flops per (query head, visible position)."""
+    p = w.prefill
+    if p is None:
+        return 0
+    visible = p.n_q * p.q_start + p.n_q * (p.n_q + 1) // 2
+    return 4 * w.d_h * w.H_Q * visible
 
 
 # the sources the decode kernel is compiled from (its ncu counters go stale when one changes)
@@ -218,11 +235,16 @@ def run_reference(args, w, ld, rank):
 
 
 def config_dict(w):
-    return {"workload": w.name, "B": w.B, "H_Q": w.H_Q, "H_KV": w.H_KV, "d_h": w.d_h, "block_size": w.bs,
-            "layers": w.L, "context": int(w.lens_pre.max()), "attended": int(w.lens_post.max()),
-            "kv_dtype": w.dtype, "num_blocks": w.num_blocks,
-            "l2": f"inputs larger than L2: {step_bytes(w)['kv'] * w.L / 1e9:.2f} GB of KV per step vs "
-                  f"{L2_BYTES / 2**20:.0f} MiB L2"}
+    c = {"workload": w.name, "B": w.B, "H_Q": w.H_Q, "H_KV": w.H_KV, "d_h": w.d_h, "block_size": w.bs,
+         "layers": w.L, "context": int(w.lens_pre.max()), "attended": int(w.lens_post.max()),
+         "kv_dtype": w.dtype, "num_blocks": w.num_blocks,
+         "l2": f"inputs larger than L2: {step_bytes(w)['kv'] * w.L / 1e9:.2f} GB of KV per step vs "
+               f"{L2_BYTES / 2**20:.0f} MiB L2"}
+    if w.shared_prefix:
+        c["shared_prefix"] = w.shared_prefix
+    if w.prefill is not None:
+        c["prefill_chunk"] = {"queries": w.prefill.n_q, "q_start": w.prefill.q_start}
+    return c
 
 
 # ---------------------------------------------------------------- multi-rank aggregation
@@ -269,7 +291,7 @@ def main():
 
     import torch
     import paged_kv_cache_kvc_gb300 as kvc
-    from harness import GpuCase, dev_bits
+    from harness import GpuCase, dev_bits, dev_i32
 
     torch.cuda.set_device(local)
     dist = None
@@ -298,11 +320,32 @@ def main():
     stream = torch.cuda.current_stream()
     sb1 = step_bytes(w)
     sb = {k: v * L for k, v in sb1.items()}
-
-    def step():     # each layer: append + paged decode attention, one fused launch (kvc_decode_step)
+    pf = w.prefill
+    if pf is not None:   # the chunk's keys and values go in once; every step attends over them
+        row = dev_i32(w.block_tables[pf.seq])
+        pq, p_out, p_lse = [], [], []
         for layer in range(L):
-            kvc.kvc_decode_step(g.pool, layer, q[layer], g.bt_dec, g.lens_pre, k_new[layer], v_new[layer],
-                                outs[layer], lses[layer], scale=w.scale)
+            kc = w.ctx_tokens(layer, 0, pf.seq, pf.q_start, pf.total)
+            vc = w.ctx_tokens(layer, 1, pf.seq, pf.q_start, pf.total)
+            kvc.kvc_write_tokens(g.pool, layer, row[None], dev_i32([pf.q_start]), dev_i32([0, pf.n_q]),
+                                 dev_bits(kc), dev_bits(vc))
+            pq.append(dev_bits(w.prefill_q(layer)))
+            p_out.append(torch.empty((pf.n_q, w.H_Q, w.d_h), dtype=torch.float32, device="cuda"))
+            p_lse.append(torch.empty((pf.n_q, w.H_Q), dtype=torch.float32, device="cuda"))
+        torch.cuda.synchronize()
+
+    def launch(layer, q_, bt_, lp_, k_, v_, o_, l_, pq_=None, po_=None, pl_=None, strm=None):
+        """One layer of the step: the fused decode step, with the prefill chunk in the same launch."""
+        if pf is None:
+            kvc.kvc_decode_step(g.pool, layer, q_, bt_, lp_, k_, v_, o_, l_, scale=w.scale, stream=strm)
+        else:
+            kvc.kvc_mixed_step(g.pool, layer, q_, bt_, lp_, k_, v_, o_, l_, pq_, row, pf.q_start, po_, pl_,
+                               scale=w.scale, stream=strm)
+
+    def step():     # each layer: append + paged decode attention (+ the chunk), one launch
+        for layer in range(L):
+            launch(layer, q[layer], g.bt_dec, g.lens_pre, k_new[layer], v_new[layer], outs[layer], lses[layer],
+                   *((pq[layer], p_out[layer], p_lse[layer]) if pf is not None else ()))
 
     def barrier():
         if dist is not None:
@@ -350,18 +393,23 @@ def main():
     # double-buffered, so step i's inputs arrive while step i-1 computes and its
     # results leave while step i+1 computes (a serving loop's overlap).
     pin = lambda t: t.cpu().pin_memory()
-    q_h, k_h, v_h = [pin(t) for t in q], [pin(t) for t in k_new], [pin(t) for t in v_new]
+    # per-layer inputs and results of the step (the chunk's queries and outputs too, if any)
+    ins = {"q": q, "k": k_new, "v": v_new}
+    res = {"out": outs, "lse": lses}
+    if pf is not None:
+        ins["pq"] = pq
+        res.update(p_out=p_out, p_lse=p_lse)
+    host_in = {n: [pin(t) for t in ts] for n, ts in ins.items()}
     bt_h, lp_h = pin(g.bt_dec), pin(g.lens_pre)
     sets = []          # two device buffer sets: inputs and results of alternate steps
     for _ in range(2):
-        sets.append({"q": [torch.empty_like(t) for t in q], "k": [torch.empty_like(t) for t in k_new],
-                     "v": [torch.empty_like(t) for t in v_new], "bt": torch.empty_like(g.bt_dec),
-                     "lp": torch.empty_like(g.lens_pre), "out": [torch.empty_like(t) for t in outs],
-                     "lse": [torch.empty_like(t) for t in lses],
-                     "out_h": [torch.empty_like(t, device="cpu").pin_memory() for t in outs],
-                     "lse_h": [torch.empty_like(t, device="cpu").pin_memory() for t in lses]})
-    h2d = sum(t.numel() * t.element_size() for t in q_h + k_h + v_h + [bt_h, lp_h])
-    d2h = sum(t.numel() * 4 for t in sets[0]["out_h"] + sets[0]["lse_h"])
+        d = {n: [torch.empty_like(t) for t in ts] for n, ts in list(ins.items()) + list(res.items())}
+        d.update({n + "_h": [torch.empty_like(t, device="cpu").pin_memory() for t in ts] for n, ts in res.items()})
+        d.update(bt=torch.empty_like(g.bt_dec), lp=torch.empty_like(g.lens_pre))
+        sets.append(d)
+    h2d = sum(t.numel() * t.element_size() for ts in host_in.values() for t in ts) + \
+        sum(t.numel() * t.element_size() for t in (bt_h, lp_h))
+    d2h = sum(t.numel() * t.element_size() for n in res for t in sets[0][n + "_h"])
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
     computed, drained = [ev(), ev()], [ev(), ev()]
@@ -375,22 +423,22 @@ def main():
             s_in.wait_event(computed[i % 2])          # step i-2 has finished reading this set's inputs
             b["bt"].copy_(bt_h, non_blocking=True)
             b["lp"].copy_(lp_h, non_blocking=True)
-            for layer in range(L):
-                b["q"][layer].copy_(q_h[layer], non_blocking=True)
-                b["k"][layer].copy_(k_h[layer], non_blocking=True)
-                b["v"][layer].copy_(v_h[layer], non_blocking=True)
+            for n, ts in host_in.items():
+                for layer in range(L):
+                    b[n][layer].copy_(ts[layer], non_blocking=True)
             loaded.record(s_in)
         stream.wait_event(loaded)
         stream.wait_event(drained[i % 2])             # step i-2's results have left this set
         for layer in range(L):
-            kvc.kvc_decode_step(g.pool, layer, b["q"][layer], b["bt"], b["lp"], b["k"][layer], b["v"][layer],
-                                b["out"][layer], b["lse"][layer], scale=w.scale, stream=stream)
+            launch(layer, b["q"][layer], b["bt"], b["lp"], b["k"][layer], b["v"][layer], b["out"][layer],
+                   b["lse"][layer], *((b["pq"][layer], b["p_out"][layer], b["p_lse"][layer]) if pf else ()),
+                   strm=stream)
         computed[i % 2].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(computed[i % 2])
-            for layer in range(L):
-                b["out_h"][layer].copy_(b["out"][layer], non_blocking=True)
-                b["lse_h"][layer].copy_(b["lse"][layer], non_blocking=True)
+            for n in res:
+                for layer in range(L):
+                    b[n + "_h"][layer].copy_(b[n][layer], non_blocking=True)
             drained[i % 2].record(s_out)
 
     for i in range(min(4, K)):                        # warm the copy path
@@ -406,8 +454,9 @@ def main():
     barrier()
     e2e_ms = e_start.elapsed_time(e_end) / K
     torch.cuda.synchronize()
-    for layer in range(L):                            # the copied-back results are the kernel's
-        assert torch.equal(sets[(K - 1) % 2]["out_h"][layer], sets[(K - 1) % 2]["out"][layer].cpu())
+    for n in res:                                     # the copied-back results are the kernel's
+        for layer in range(L):
+            assert torch.equal(sets[(K - 1) % 2][n + "_h"][layer], sets[(K - 1) % 2][n][layer].cpu())
 
     # ---- max over ranks
     ms, e2e_ms, attn_ms = max_over_ranks([ms, e2e_ms, attn_ms], dist, "cuda")
@@ -431,12 +480,17 @@ def main():
                         "ms_per_step": e2e_ms, "tokens_per_s": w.B * world / (e2e_ms * 1e-3)},
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                              "frac": achieved / hbm, "traffic": profiled_traffic(w.name),
-                             "kernel": "decode_kernel with fused append (kvc_decode_step)",
+                             "kernel": ("mixed_kernel: decode step with fused append and the prefill chunk in "
+                                        "one launch (kvc_mixed_step)" if pf is not None else
+                                        "decode_kernel with fused append (kvc_decode_step)"),
                              "peak_source": f"{peak_kind} hbm_gbs",
                              "algorithmic_bytes_per_launch": sb1["total"], "launch_ms": attn_ms,
                              "note": splits_note},
                 "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
                 "step_bytes": sb}
+        if pf is not None:   # the chunk's causal attention rides in the same launch
+            line["prefill"] = {"queries": pf.n_q, "q_start": pf.q_start, "flops_per_step": prefill_flops(w) * L,
+                               "tflops_in_step": prefill_flops(w) * L / (ms * 1e-3) / 1e12}
         print(json.dumps(line), flush=True)
     g.close()
     if dist is not None:

@@ -237,6 +237,26 @@ KVC_API kvc_status kvc_prefill_attn(kvc_pool *pool, int32_t layer, const void *q
                             const int32_t *block_table_row, int32_t max_blocks, int32_t q_start,
                             float *out, float *lse, float scale, kvc_stream_t stream);
 
+/* A decode step and a prefill chunk in ONE launch ("KV cache: Generation
+ * state, latency, and allocation" 21.3: chunked prefill runs beside the
+ * decode steps of other requests; the xf_kv_cache page, "End-to-end flow").
+ * Computes exactly what kvc_decode_step(q .. lse) followed by
+ * kvc_prefill_attn(prefill_q .. prefill_lse) compute, in one kernel whose CTAs
+ * are the two calls' CTAs interleaved, so the chunk's tensor-core work runs
+ * while the decode CTAs stream the cache from HBM.  The prefill row's
+ * positions 0 .. q_start + n_q - 1 must already be in the pool and must not be
+ * among the positions the decode part appends (they are written during the
+ * launch).  n_q == 0 or B == 0 reduces to the other call alone.  Decode groups
+ * of more than 16 query heads, and head widths other than 128 (64 for bf16
+ * pools), run the two calls as two launches.
+ * Arguments, requirements and errors as kvc_decode_step and kvc_prefill_attn. */
+KVC_API kvc_status kvc_mixed_step(kvc_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
+                                  const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, int32_t B,
+                                  const void *k_new, const void *v_new, float *out, float *lse,
+                                  const void *prefill_q, int32_t n_q, const int32_t *prefill_block_table_row,
+                                  int32_t prefill_max_blocks, int32_t q_start, float *prefill_out, float *prefill_lse,
+                                  float scale, kvc_stream_t stream);
+
 /* Pre-size the decode workspace for up to max_batch sequences of up to
  * max_blocks table entries and num_q_heads query heads, so that later calls
  * allocate nothing.  Errors: KVC_ERR_ARG, KVC_ERR_OOM. */

@@ -47,6 +47,7 @@ EXPORTS = ["kvc_pool_create", "kvc_pool_destroy", "kvc_pool_info", "kvc_pool_set
            "kvc_calibrate_scales",
            "kvc_append", "kvc_write_tokens", "kvc_decode_attn", "kvc_prefill_attn", "kvc_pool_reserve",
            "kvc_bytes", "kvc_pool_sync_status", "kvc_status_str", "kvc_launch_count", "kvc_decode_attn_noalloc", "kvc_decode_step",
+           "kvc_mixed_step",
            "kvc_alloc_create", "kvc_alloc_destroy", "kvc_alloc_new_seq", "kvc_alloc_fork", "kvc_alloc_reserve",
            "kvc_alloc_commit", "kvc_alloc_release", "kvc_alloc_publish", "kvc_alloc_match", "kvc_alloc_seq_info",
            "kvc_alloc_block_tables", "kvc_alloc_counts", "kvc_alloc_refcount", "kvc_copy_blocks"]
@@ -78,6 +79,9 @@ def load(path: str = LIB_PATH):
     L.kvc_decode_attn_noalloc.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, vp, vp, ctypes.c_float, vp]
     L.kvc_prefill_attn.restype = st
     L.kvc_prefill_attn.argtypes = [vp, i32, vp, i32, i32, vp, i32, i32, vp, vp, ctypes.c_float, vp]
+    L.kvc_mixed_step.restype = st
+    L.kvc_mixed_step.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, vp, vp, vp, vp,
+                                 vp, i32, vp, i32, i32, vp, vp, ctypes.c_float, vp]
     L.kvc_pool_reserve.restype, L.kvc_pool_reserve.argtypes = st, [vp, i32, i32, i32]
     L.kvc_bytes.restype, L.kvc_bytes.argtypes = u64, [i64] * 6
     L.kvc_pool_sync_status.restype, L.kvc_pool_sync_status.argtypes = st, [vp, vp]
@@ -286,6 +290,27 @@ def kvc_prefill_attn(pool, layer, q, block_table_row, q_start, out, lse=None, sc
                                    int(q_start), _dev(out, torch.float32, "out"),
                                    _dev(lse, torch.float32, "lse", optional=True), float(scale), _stream(stream)),
            "kvc_prefill_attn")
+
+
+def kvc_mixed_step(pool, layer, q, block_tables, seq_lens_pre, k_new, v_new, out, lse, prefill_q, prefill_block_table_row,
+                   q_start, prefill_out, prefill_lse=None, scale=None, stream=None):
+    """kvc_decode_step and kvc_prefill_attn in one launch."""
+    B, H_Q, D = q.shape
+    n_q = prefill_q.shape[0]
+    if scale is None:
+        scale = D ** -0.5
+    _check(load().kvc_mixed_step(_h(pool), layer, _dev(q, torch.bfloat16, "q"), H_Q,
+                                 _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+                                 _dev(seq_lens_pre, torch.int32, "seq_lens"), B, _dev(k_new, torch.bfloat16, "k_new"),
+                                 _dev(v_new, torch.bfloat16, "v_new"), _dev(out, torch.float32, "out"),
+                                 _dev(lse, torch.float32, "lse", optional=True),
+                                 _dev(prefill_q, torch.bfloat16, "prefill_q"), n_q,
+                                 _dev(prefill_block_table_row, torch.int32, "prefill_block_table_row"),
+                                 prefill_block_table_row.shape[-1], int(q_start),
+                                 _dev(prefill_out, torch.float32, "prefill_out"),
+                                 _dev(prefill_lse, torch.float32, "prefill_lse", optional=True), float(scale),
+                                 _stream(stream)),
+           "kvc_mixed_step")
 
 
 def kvc_pool_reserve(pool, max_batch, num_q_heads, max_blocks):

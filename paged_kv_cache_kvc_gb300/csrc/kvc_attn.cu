@@ -40,9 +40,17 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int D)
 // own blocks, so the kernel is bound by HBM once enough bytes are in flight;
 // each CTA keeps 4 warps x (R - 1) stages in flight, so HBM wants more CTAs
 // than one per resident slot.  Measured on GB300: about 1.7 CTAs per resident
-// slot is best (a split costs a partial write and the merge).  Blocks per
-// split stay between 16 (x the query n-tiles: a split's partials grow with
-// the group size) and 1024.  KVC_SPLIT_CHUNK overrides (rounded up to 4).
+// slot is best (a split costs a partial write and the merge).  No split is
+// longer than kMaxChunk blocks, so that in a batch of unequal lengths the
+// longest sequences do not set the launch's length (GB300, 64 sequences of
+// log-uniform lengths 1 200..32 768: 299 us with 1 024-block splits, 253 us
+// with 256-block splits); the hardware hands the many CTAs to SMs as they
+// free, which also evens out SMs that stream at different rates.  Splits of
+// one sequence are equal to within 4 blocks; a split holds at least 16 blocks
+// (x the query n-tiles: a split's partials grow with the group size).
+// KVC_SPLIT_CHUNK overrides (rounded up to 4).
+constexpr int kMaxChunk = 288;
+
 void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits,
                   int n_tiles)
 {
@@ -51,10 +59,10 @@ void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_
     if (ch <= 0) {
         const double slots = static_cast<double>(pool->num_sms) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
         long ns = units > 0 ? std::lround(1.7 * slots / units) : 1;
+        ns = std::max(ns, static_cast<long>((max_blocks + kMaxChunk - 1) / kMaxChunk));
         if (ns < 1) ns = 1;
         ch = static_cast<int>((max_blocks + ns - 1) / ns);
         if (ch < 16 * n_tiles) ch = 16 * n_tiles;
-        if (ch > 1024) ch = 1024;
     }
     ch = (ch + 3) & ~3;
     *chunk = ch;
@@ -102,13 +110,6 @@ static size_t workspace_bytes(int B, int H_Q, int max_splits, int D)
     return n * D * sizeof(float) + n * sizeof(float2);
 }
 
-// persistent records: o [workers + units][g][D], then (max, sum) [workers + units][g]
-static size_t record_bytes(int workers, int units, int g, int D)
-{
-    const size_t n = (static_cast<size_t>(workers) + units) * g;
-    return n * D * sizeof(float) + n * sizeof(float2);
-}
-
 kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream)
 {
     kvc_pool *pool = const_cast<kvc_pool *>(cpool);
@@ -144,39 +145,38 @@ kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel
     return KVC_OK;
 }
 
-kvc_status run_decode_persistent(kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream)
+// A decode step (pd) and a prefill chunk (pp) in one mixed_kernel launch; each
+// part keeps the split plan it would get alone and its own partials and counters.
+static kvc_status run_mixed(kvc_pool *pool, DecodeParams &pd, DecodeParams &pp, const DecodeKernel &k,
+                            cudaStream_t stream)
 {
-    // Opt-in (KVC_PERSISTENT=1): its static ranges finish with the slowest SM (on GB300
-    // the SMs of one launch stream at rates up to ~25 % apart), so the split kernel,
-    // whose CTAs the hardware hands to whichever SM frees first, stays the default.
-    // A split size forced by KVC_SPLIT_CHUNK selects the split kernel.
-    const char *opt = std::getenv("KVC_PERSISTENT");
-    if (!opt || opt[0] != '1') return KVC_ERR_UNSUPPORTED;
-    if (std::getenv("KVC_SPLIT_CHUNK")) return KVC_ERR_UNSUPPORTED;
-    if (!p.lens || p.B > kMaxSeqPersistent || !k.fn || k.ctas_per_sm <= 0) return KVC_ERR_UNSUPPORTED;
-    if (static_cast<int64_t>(p.B) * p.max_blocks >= (int64_t(1) << 31)) return KVC_ERR_UNSUPPORTED;
-    const int units = p.B * p.H_KV;
-    // ranges of the flattened blocks, each served by H_KV workers: every resident warp
-    // takes part, but no range is shorter than kMinBlocksPerWorker blocks at full tables
-    int64_t ranges = static_cast<int64_t>(pool->num_sms) * k.ctas_per_sm * kWarps / p.H_KV;
-    ranges = std::max<int64_t>(1, std::min(ranges, static_cast<int64_t>(p.B) * p.max_blocks / kMinBlocksPerWorker));
-    // a unit's merge reads (ranges per sequence + 2) records of g rows: keep it a small job
-    if (static_cast<double>(p.g) * (static_cast<double>(ranges) / p.B + 2.0) > 256.0) return KVC_ERR_UNSUPPORTED;
-    const int64_t workers = ranges * p.H_KV;
-    if (workers > static_cast<int64_t>(pool->num_sms) * k.ctas_per_sm * kWarps * 4) return KVC_ERR_UNSUPPORTED;
-    const int grid = static_cast<int>((workers + kWarps - 1) / kWarps);
-    const int nw = grid * kWarps;
-    kvc_status st = ensure_workspace(pool, static_cast<size_t>(units), record_bytes(nw, units, p.g, pool->D));
+    if (!k.fn || k.ctas_per_sm <= 0) return KVC_ERR_UNSUPPORTED;
+    choose_split(pool, pd.B * pd.H_KV, pd.max_blocks, k.ctas_per_sm, &pd.chunk, &pd.max_splits, n_tiles(pd.g));
+    choose_split(pool, pp.B * pp.H_KV, pp.max_blocks, k.ctas_per_sm, &pp.chunk, &pp.max_splits,
+                 n_tiles(pp.ppu * pp.g));
+    const int splits = std::max(pd.max_splits, pp.max_splits);
+    if (splits > 65535 || static_cast<int64_t>(pd.B) + pp.B > 65535) return KVC_ERR_UNSUPPORTED;
+    const size_t ud = static_cast<size_t>(pd.B) * pd.H_KV, up = static_cast<size_t>(pp.B) * pp.H_KV;
+    const size_t nd = pd.max_splits > 1 ? static_cast<size_t>(pd.n_pos) * pd.H_Q * pd.max_splits : 0;
+    const size_t np = pp.max_splits > 1 ? static_cast<size_t>(pp.n_pos) * pp.H_Q * pp.max_splits : 0;
+    const size_t row = static_cast<size_t>(pool->D) * sizeof(float) + sizeof(float2);
+    kvc_status st = ensure_workspace(pool, ud + up, (nd + np) * row);
     if (st != KVC_OK) return st;
-    p.part_o = ws_data(pool);
-    p.part_ml = reinterpret_cast<float2 *>(p.part_o + (static_cast<size_t>(nw) + units) * p.g * pool->D);
-    p.counters = ws_counters(pool);
-    p.chunk = 0;
-    p.max_splits = 0;
-    void *args[] = {const_cast<CUtensorMap *>(&pool->tmap), &p};
-    const cudaError_t e = cudaLaunchKernel(k.fn, dim3(grid), dim3(kThreads), args, k.smem, stream);
+    float *data = ws_data(pool);
+    pd.part_o = nd ? data : nullptr;
+    pd.part_ml = nd ? reinterpret_cast<float2 *>(data + nd * pool->D) : nullptr;
+    pd.counters = (nd && pd.ppu * pd.g * pd.max_splits <= 64) ? ws_counters(pool) : nullptr;
+    float *data_p = data + nd * pool->D + nd * 2;
+    pp.part_o = np ? data_p : nullptr;
+    pp.part_ml = np ? reinterpret_cast<float2 *>(data_p + np * pool->D) : nullptr;
+    pp.counters = (np && pp.ppu * pp.g * pp.max_splits <= 64) ? ws_counters(pool) + ud : nullptr;
+    void *args[] = {const_cast<CUtensorMap *>(&pool->tmap), &pd, &pp};
+    cudaError_t e = cudaLaunchKernel(k.fn, dim3(splits, pool->H_KV, pd.B + pp.B), dim3(kThreads), args, k.smem,
+                                     stream);
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (nd && !pd.counters && (st = launch_split_merge(pd, pool->D, stream)) != KVC_OK) return st;
+    if (np && !pp.counters && (st = launch_split_merge(pp, pool->D, stream)) != KVC_OK) return st;
     return KVC_OK;
 }
 
@@ -288,6 +288,8 @@ extern "C" kvc_status kvc_prefill_attn(kvc_pool *pool, int32_t layer, const void
     p.lens = nullptr;
     p.bt_stride = 0;
     p.len_base = q_start;
+    // the chunk reads positions < q_start + n_q: plan splits over those blocks only
+    p.max_blocks = static_cast<int32_t>((static_cast<int64_t>(q_start) + n_q + kBS - 1) / kBS);
     int ppu = 32 / p.g;     // measured on GB300 (600-query chunk, g = 4): 1 -> 346 us, 4 -> 143 us, 8 -> 135 us
     if (const char *e = std::getenv("KVC_PREFILL_PPU")) ppu = std::atoi(e);
     ppu = std::max(1, std::min(ppu, 32 / p.g));
@@ -297,6 +299,62 @@ extern "C" kvc_status kvc_prefill_attn(kvc_pool *pool, int32_t layer, const void
     return dispatch(pool, p, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" kvc_status kvc_mixed_step(kvc_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
+                                     const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
+                                     int32_t B, const void *k_new, const void *v_new, float *out, float *lse,
+                                     const void *prefill_q, int32_t n_q, const int32_t *prefill_block_table_row,
+                                     int32_t prefill_max_blocks, int32_t q_start, float *prefill_out,
+                                     float *prefill_lse, float scale, kvc_stream_t stream)
+{
+    if (B < 0 || B > 65535 || n_q < 0 || n_q > 65535 || q_start < 0) return KVC_ERR_ARG;
+    if (n_q == 0)
+        return kvc_decode_step(pool, layer, q, num_q_heads, block_tables, max_blocks, seq_lens, B, k_new, v_new, out,
+                               lse, scale, stream);
+    if (B == 0)
+        return kvc_prefill_attn(pool, layer, prefill_q, n_q, num_q_heads, prefill_block_table_row,
+                                prefill_max_blocks, q_start, prefill_out, prefill_lse, scale, stream);
+    if (!seq_lens || !aligned(seq_lens, 4) || !k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16))
+        return KVC_ERR_ARG;
+    kvc_status st = common_attn_checks(pool, layer, q, num_q_heads, block_tables, max_blocks, out, lse, scale);
+    if (st != KVC_OK) return st;
+    st = common_attn_checks(pool, layer, prefill_q, num_q_heads, prefill_block_table_row, prefill_max_blocks,
+                            prefill_out, prefill_lse, scale);
+    if (st != KVC_OK) return st;
+    if (static_cast<int64_t>(q_start) + n_q > static_cast<int64_t>(prefill_max_blocks) * kBS) return KVC_ERR_RANGE;
+    DecodeParams pd{};
+    fill_common(pd, pool, layer, q, num_q_heads, block_tables, max_blocks, out, lse, scale);
+    pd.lens = seq_lens;
+    pd.bt_stride = max_blocks;
+    pd.B = B;
+    pd.ppu = 1;
+    pd.n_pos = B;
+    pd.k_new = static_cast<const uint16_t *>(k_new);
+    pd.v_new = static_cast<const uint16_t *>(v_new);
+    pd.pool = pool->base;
+    DecodeParams pp{};
+    fill_common(pp, pool, layer, prefill_q, num_q_heads, prefill_block_table_row, prefill_max_blocks, prefill_out,
+                prefill_lse, scale);
+    pp.lens = nullptr;
+    pp.bt_stride = 0;
+    pp.len_base = q_start;
+    pp.max_blocks = static_cast<int32_t>((static_cast<int64_t>(q_start) + n_q + kBS - 1) / kBS);
+    pp.ppu = std::max(1, 32 / pp.g);
+    pp.n_pos = n_q;
+    pp.B = (n_q + pp.ppu - 1) / pp.ppu;
+    DecodeKernel k{nullptr, 0, 0};
+    if (pool->dtype == KVC_FP8_E4M3) k = select_mixed_fp8(pool->D, pd.g);
+    else if (pool->dtype == KVC_INT4) k = select_mixed_int4(pool->D, pd.g);
+    else k = select_mixed_bf16(pool->D, pd.g);
+    if (!k.fn) {   // no mixed instance for this shape: the two launches in order
+        st = kvc_decode_step(pool, layer, q, num_q_heads, block_tables, max_blocks, seq_lens, B, k_new, v_new, out,
+                             lse, scale, stream);
+        if (st != KVC_OK) return st;
+        return kvc_prefill_attn(pool, layer, prefill_q, n_q, num_q_heads, prefill_block_table_row,
+                                prefill_max_blocks, q_start, prefill_out, prefill_lse, scale, stream);
+    }
+    return run_mixed(pool, pd, pp, k, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_t num_q_heads, int32_t max_blocks)
 {
     if (!pool || max_batch < 0 || num_q_heads <= 0 || max_blocks <= 0) return KVC_ERR_ARG;
@@ -304,12 +362,8 @@ extern "C" kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_
     if (st != KVC_OK) return st;
     // the largest split count any batch of this size can get is the 16-block floor
     const int max_splits = (max_blocks + 15) / 16;
-    const int g = num_q_heads / pool->H_KV;
-    const int workers = pool->num_sms * 8 * kWarps;   // the persistent kernel's records: at most 8 CTAs per SM
     const size_t units = static_cast<size_t>(max_batch) * pool->H_KV;
-    return ensure_workspace(pool, units,
-                            std::max(workspace_bytes(max_batch, num_q_heads, max_splits, pool->D),
-                                     record_bytes(workers, static_cast<int>(units), g, pool->D)));
+    return ensure_workspace(pool, units, workspace_bytes(max_batch, num_q_heads, max_splits, pool->D));
 }
 
 namespace kvc {

@@ -363,16 +363,16 @@ __device__ __forceinline__ void block_update(uint32_t st, const uint32_t (&qf)[N
 // CAUSAL: columns may see different numbers of positions (prefill tiles), so
 // the mask is per column and a column may see nothing in a block; decode
 // instances (every column sees the unit's whole length) skip both.
+// One CTA of the split kernel: split `split` of unit (b, h).
 template <int D, int NT, int KIND, bool PSPLIT, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmap,
-                                                          const DecodeParams p)
+__device__ __forceinline__ void decode_cta(const CUtensorMap &tmap, const DecodeParams &p, const int split,
+                                           const int h, const int b)
 {
     using C = DecodeCfg<D, KIND>;
-    constexpr bool FP8 = KIND == KV_E4M3, INT4 = KIND == KV_INT4, QUANT = KIND != KV_BF16;
+    constexpr bool INT4 = KIND == KV_INT4, QUANT = KIND != KV_BF16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, tg = lane & 3;
     const int hq0 = h * p.g;
@@ -646,397 +646,32 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     if (threadIdx.x == 0) p.counters[static_cast<size_t>(b) * p.H_KV + h] = 0u;   // ready for the next launch
 }
 
-// ---------------------------------------------------------------------------
-// Balanced persistent decode.
-//
-// One launch of (SMs x resident CTAs) CTAs whose warps are independent
-// workers.  The batch's logical blocks are flattened sequence by sequence
-// into T positions; they are cut into NG equal contiguous ranges, and each
-// range is served by a group of H_KV workers, worker (r, h) reading KV head
-// h of range r's blocks.  Every worker streams the same number of blocks, so
-// the launch has no wave tail and each warp pays its prologue once; the
-// H_KV workers of a range read the H_KV adjacent head tiles of each physical
-// block at about the same time (as the split kernel's CTAs of one sequence
-// do).  A warp keeps its TMA ring running across sequence boundaries; on
-// entering a sequence it loads that unit's query fragments and clears its
-// running state.
-//
-// A unit u = (b, h) covered by one worker is written out by it directly.
-// Otherwise each covering worker writes a partial (m, l, o) record for its
-// share -- record (r + b) * H_KV + h, unique because the ranges and the
-// sequences are both contiguous and increasing -- and counts itself on the
-// unit's arrival counter; the worker that completes the count merges the
-// unit's records (the log-sum-exp merge of the split path) after its CTA's
-// warps have all finished their ranges, with the whole CTA.  Only a range's
-// first and last sequence can be shared, so a warp has at most two merges to
-// do.  The merge order is fixed, so results are the same from run to run.
-constexpr int kMaxSeqPersistent = 1024;   // sequences per launch (prefix sums held in shared memory)
-constexpr int kMinBlocksPerWorker = 8;
-
-template <int D, int KIND>
-__host__ __device__ constexpr int persistent_smem_bytes()
+// grid (split, KV head, unit)
+template <int D, int NT, int KIND, bool PSPLIT, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                          const DecodeParams p)
 {
-    using C = DecodeCfg<D, KIND>;
-    return 1024 /* alignment slack */ + kWarps * C::R * C::STAGE + kWarps * C::R * 8 /* mbarriers */ +
-           (kMaxSeqPersistent + 1) * 4 /* block prefix sums */ + (2 * kWarps + kWarps) * 4 /* merges, scan */;
+    decode_cta<D, NT, KIND, PSPLIT, CAUSAL>(tmap, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
-// range holding flattened position P when T positions are cut into ng ranges
-__device__ __forceinline__ int range_of(int64_t P, int64_t T, int ng)
-{
-    return static_cast<int>(((P + 1) * ng - 1) / T);
-}
-
+// A decode step and a prefill chunk in one launch (pages' "chunked prefill"
+// beside decode): grid (split, KV head, decode units + prefill tiles).  The
+// prefill tiles, compute-heavy and L2-resident, are spread evenly among the
+// HBM-bound decode units (tile i of P sits at the z where floor(z*P/Z)
+// steps), so the two kinds of work overlap on the SMs.
 template <int D, int NT, int KIND, bool PSPLIT>
-__global__ void __launch_bounds__(kThreads) decode_persistent_kernel(const __grid_constant__ CUtensorMap tmap,
-                                                                     const DecodeParams p)
+__global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                         const DecodeParams pd, const DecodeParams pp)
 {
-    using C = DecodeCfg<D, KIND>;
-    constexpr bool QUANT = KIND != KV_BF16;
-    constexpr int PER = (kMaxSeqPersistent + kThreads - 1) / kThreads;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWarps * C::R * C::STAGE);
-    int *cum = reinterpret_cast<int *>(bars + kWarps * C::R);   // [B + 1] blocks of the sequences before b
-    int *pend = cum + kMaxSeqPersistent + 1;                     // [kWarps][2] units to merge, -1 = none
-    int *wsum = pend + 2 * kWarps;                               // [kWarps] scan carries
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gq = lane >> 2, tg = lane & 3;
-    const int B = p.B, H = p.H_KV, g = p.g;
-
-    // ---- prologue: block prefix sums over the sequences (a length out of range counts as empty)
-    int nb_loc[PER];
-    int tot = 0;
-    const int b0 = threadIdx.x * PER;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int b = b0 + i;
-        int nb = 0;
-        if (b < B) {
-            const int len = seq_len(p, b);
-            if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) {
-                if (blockIdx.x == 0) atomicOr(p.err, KVC_EBIT_RANGE);
-            } else {
-                nb = (len + kBS - 1) / kBS;
-            }
-        }
-        nb_loc[i] = nb;
-        tot += nb;
-    }
-    int incl = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += t;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    if (lane == 0) {
-        for (int s = 0; s < C::R; ++s) mbar_init(smem_u32(&bars[warp * C::R + s]), 1);
-        fence_barrier_init();
-    }
-    if (lane < 2) pend[2 * warp + lane] = -1;
-    if (threadIdx.x == 0) prefetch_tensormap(&tmap);
-    __syncthreads();
-    {
-        int run = incl - tot;
-        for (int w = 0; w < warp; ++w) run += wsum[w];
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            if (b0 + i < B) cum[b0 + i] = run;
-            run += nb_loc[i];
-        }
-        if (threadIdx.x == kThreads - 1) cum[B] = run;
-    }
-    __syncthreads();
-
-    // empty sequences: zero output, lse = -inf
-    for (int b = blockIdx.x; b < B; b += gridDim.x) {
-        if (cum[b + 1] != cum[b]) continue;
-        for (int i = threadIdx.x; i < p.H_Q * D; i += kThreads) p.out[static_cast<size_t>(b) * p.H_Q * D + i] = 0.f;
-        if (p.lse)
-            for (int i = threadIdx.x; i < p.H_Q; i += kThreads) p.lse[static_cast<size_t>(b) * p.H_Q + i] = -INFINITY;
-    }
-
-    const int64_t T = cum[B];
-    if (T == 0) return;   // uniform across the CTA
-    const int NG = static_cast<int>(min(static_cast<int64_t>(gridDim.x) * kWarps / H,
-                                        max(static_cast<int64_t>(1), T / kMinBlocksPerWorker)));
-    const int W = warp * gridDim.x + blockIdx.x;   // consecutive workers sit on different SMs
-    const int r = W / H, h = W - r * H;            // range r, KV head h
-    const int64_t lo = r < NG ? (static_cast<int64_t>(r) * T) / NG : 0;
-    const int n = r < NG ? static_cast<int>((static_cast<int64_t>(r + 1) * T) / NG - lo) : 0;
-
-    const uint32_t st_base = smem_u32(smem + warp * C::R * C::STAGE);
-    const uint32_t bar_base = smem_u32(&bars[warp * C::R]);
-    const int64_t row_head = (static_cast<int64_t>(p.layer) * p.N) * H + h;
-
-    // Where local position jj of this worker lies: sequence, block, table entry.
-    // Lanes hold 32 consecutive positions per batch (current and next batch).
-    auto lookup = [&](int jj, int32_t &b, int32_t &blk, int32_t &phys) {
-        if (jj >= n) {
-            b = -1;
-            blk = 0;
-            phys = -1;
-            return;
-        }
-        const int64_t P = lo + jj;
-        int a = 0, z = B;   // largest b with cum[b] <= P (a sequence with blocks)
-        while (z - a > 1) {
-            const int m = (a + z) >> 1;
-            if (cum[m] <= P) a = m;
-            else z = m;
-        }
-        b = a;
-        blk = static_cast<int>(P - cum[a]);
-        phys = __ldg(p.bt + static_cast<int64_t>(a) * p.bt_stride + blk);
-    };
-    int32_t c_b, c_blk, c_ph, n_b, n_blk, n_ph;
-    lookup(lane, c_b, c_blk, c_ph);
-    lookup(32 + lane, n_b, n_blk, n_ph);
-    auto pick = [&](int32_t cur, int32_t nxt, int jj, int jbase) {
-        return __shfl_sync(kFull, (jj - jbase < 32) ? cur : nxt, (jj - jbase) & 31);
-    };
-    auto issue = [&](int jj, int jbase) {   // warp-collective; lane 0 issues
-        const int32_t phys = pick(c_ph, n_ph, jj, jbase);
-        if (lane == 0) {
-            const uint32_t bar = bar_base + 8u * static_cast<uint32_t>(jj % C::R);
-            if (phys < 0 || static_cast<int64_t>(phys) >= p.N) {
-                atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
-                mbar_arrive(bar);   // complete the phase without data; the consumer skips it
-            } else {
-                const int32_t y = static_cast<int32_t>((row_head + static_cast<int64_t>(phys) * H) * C::BOX_ROWS);
-                const uint32_t dst = st_base + static_cast<uint32_t>((jj % C::R) * C::STAGE);
-                mbar_arrive_expect_tx(bar, C::STAGE);
-#pragma unroll
-                for (int band = 0; band < C::BANDS; ++band)
-                    tma_load_2d(dst + band * C::BOX_BYTES, &tmap, bar, band * C::BOX_X, y);
-            }
-        }
-    };
-    for (int jj = 0; jj < min(C::R, n); ++jj) issue(jj, 0);
-
-    uint32_t qf[NT][C::KSTEPS][2];
-    float m_run[NT][2], l_run[NT][2];
-    float oacc[C::MT][NT][4];
-    int clen[NT][2];   // unused by non-causal blocks
-#pragma unroll
-    for (int jn = 0; jn < NT; ++jn) clen[jn][0] = clen[jn][1] = 0;
-
-    int ub = -1, ulen = 0, unblk = 0, u_nr = 0;   // the unit (ub, h) in progress
-    int npend = 0;
-    const int uh = h;
-
-    auto start_unit = [&](int32_t b) {
-        ub = b;
-        ulen = seq_len(p, ub);
-        unblk = cum[ub + 1] - cum[ub];
-        const int r0 = range_of(cum[ub], T, NG);
-        u_nr = range_of(cum[ub + 1] - 1, T, NG) - r0 + 1;
-        const int hq0 = uh * g;
-#pragma unroll
-        for (int jn = 0; jn < NT; ++jn) {
-            const int qi = 8 * jn + gq;
-            const bool real = qi < g;
-            const uint16_t *qrow = p.q + (real ? static_cast<size_t>(ub) * p.H_Q + hq0 + qi : static_cast<size_t>(0)) * D;
-#pragma unroll
-            for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                if constexpr (!QUANT) {
-                    qf[jn][kk][0] = real ? *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 2 * tg) : 0u;
-                    qf[jn][kk][1] = real ? *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 8 + 2 * tg) : 0u;
-                } else if constexpr (KIND == KV_INT4) {
-                    const int base = 32 * tg + 8 * (kk >> 1) + 2 * (kk & 1);
-                    const float *sk = p.s_k + static_cast<size_t>(uh) * D;
-                    auto qv = [&](int c) {
-                        const uint16_t raw = real ? qrow[c] : uint16_t(0);
-                        return __uint_as_float(static_cast<uint32_t>(raw) << 16) * __ldg(sk + c);
-                    };
-                    qf[jn][kk][0] = pack_f16(qv(base), qv(base + 4));
-                    qf[jn][kk][1] = pack_f16(qv(base + 1), qv(base + 5));
-                } else {
-                    const int c0 = (D / 4) * tg + 4 * kk;
-                    const uint2 raw = real ? *reinterpret_cast<const uint2 *>(qrow + c0) : make_uint2(0u, 0u);
-                    const float *sk = p.s_k + static_cast<size_t>(uh) * D + c0;
-                    qf[jn][kk][0] = pack_f16(bf16_lo(raw.x) * __ldg(sk + 0), bf16_hi(raw.x) * __ldg(sk + 1));
-                    qf[jn][kk][1] = pack_f16(bf16_lo(raw.y) * __ldg(sk + 2), bf16_hi(raw.y) * __ldg(sk + 3));
-                }
-            }
-        }
-#pragma unroll
-        for (int jn = 0; jn < NT; ++jn) {
-            m_run[jn][0] = m_run[jn][1] = -INFINITY;
-            l_run[jn][0] = l_run[jn][1] = 0.f;
-#pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) oacc[mt][jn][0] = oacc[mt][jn][1] = oacc[mt][jn][2] = oacc[mt][jn][3] = 0.f;
-        }
-    };
-
-    // Output channel of accumulator element (mt, c) for this thread (e4m3 / int4 permute channels).
-    auto dim_of = [&](int mt, int c) { return QUANT ? gq * (D / 8) + 2 * mt + (c >> 1) : 16 * mt + gq + 8 * (c >> 1); };
-
-    auto finish_unit = [&]() {
-#pragma unroll
-        for (int jn = 0; jn < NT; ++jn)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float l = l_run[jn][c];
-                l += __shfl_xor_sync(kFull, l, 4);
-                l += __shfl_xor_sync(kFull, l, 8);
-                l += __shfl_xor_sync(kFull, l, 16);
-                l_run[jn][c] = l;
-            }
-        const size_t row0 = static_cast<size_t>(ub) * p.H_Q + static_cast<size_t>(uh) * g;   // first out row
-        if (u_nr == 1) {
-#pragma unroll
-            for (int jn = 0; jn < NT; ++jn)
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int qi = 8 * jn + 2 * tg + (c & 1);
-                        if (qi >= g) continue;
-                        const int dim = dim_of(mt, c);
-                        float o = oacc[mt][jn][c] / l_run[jn][c & 1];
-                        if constexpr (QUANT) o *= __ldg(p.s_v + static_cast<size_t>(uh) * D + dim);
-                        p.out[(row0 + qi) * D + dim] = o;
-                    }
-            if (p.lse && gq == 0)
-#pragma unroll
-                for (int jn = 0; jn < NT; ++jn)
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int qi = 8 * jn + 2 * tg + c;
-                        if (qi < g) p.lse[row0 + qi] = (m_run[jn][c] + log2f(l_run[jn][c])) * kLn2;
-                    }
-            return;
-        }
-        const int u = ub * H + uh;
-        const size_t rec = (static_cast<size_t>(r + ub) * H + uh) * g;   // this worker's record of unit u
-#pragma unroll
-        for (int jn = 0; jn < NT; ++jn)
-#pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int qi = 8 * jn + 2 * tg + (c & 1);
-                    if (qi < g) p.part_o[(rec + qi) * D + dim_of(mt, c)] = oacc[mt][jn][c];
-                }
-        if (gq == 0)
-#pragma unroll
-            for (int jn = 0; jn < NT; ++jn)
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int qi = 8 * jn + 2 * tg + c;
-                    if (qi < g) p.part_ml[rec + qi] = make_float2(m_run[jn][c], l_run[jn][c]);
-                }
-        __threadfence();   // release the record before counting it
-        __syncwarp();
-        uint32_t prev = 0;
-        if (lane == 0) prev = atomicAdd(p.counters + u, 1u);
-        prev = __shfl_sync(kFull, prev, 0);
-        if (prev == static_cast<uint32_t>(u_nr - 1)) {   // the unit's last share: merge it at the end
-            if (lane == 0 && npend < 2) pend[2 * warp + npend] = u;
-            ++npend;
-        }
-    };
-
-    int j = 0;
-    bool timed_out = false;
-    for (; j < n; ++j) {
-        const int jbase = j & ~31;
-        if (j > 0 && (j & 31) == 0) {
-            c_b = n_b;
-            c_blk = n_blk;
-            c_ph = n_ph;
-            lookup(j + 32 + lane, n_b, n_blk, n_ph);
-        }
-        const int s = j % C::R;
-        const bool ok = mbar_wait_bounded(bar_base + 8u * s, static_cast<uint32_t>((j / C::R) & 1));
-        if (!__all_sync(kFull, ok)) {
-            timed_out = true;
-            break;
-        }
-        const int32_t b = pick(c_b, n_b, j, jbase);
-        const int32_t blk = pick(c_blk, n_blk, j, jbase);
-        const int32_t phys = pick(c_ph, n_ph, j, jbase);
-        if (b != ub) {
-            if (ub >= 0) finish_unit();
-            start_unit(b);
-        }
-        if (phys >= 0 && static_cast<int64_t>(phys) < p.N) {
-            const uint32_t st = st_base + static_cast<uint32_t>(s * C::STAGE);
-            const int valid = min(kBS, ulen - blk * kBS);
-            if (KIND != KV_INT4 && valid < kBS) {   // value rows past the sequence end may hold NaN
-                const int nz = (kBS - valid) * C::BANDS * 8;
-                for (int i = lane; i < nz; i += 32) sts128_zero(st + swz(kBS + valid + i / (C::BANDS * 8), i % (C::BANDS * 8)));
-            }
-            if (p.k_new && blk == unblk - 1) append_row<D, KIND>(p, st, ub, uh, phys, valid - 1, lane);
-            __syncwarp();
-            block_update<D, NT, KIND, PSPLIT, false>(st, qf, m_run, l_run, oacc, valid, blk * kBS, clen,
-                                                     p.scale_log2, lane);
-        }
-        __syncwarp();
-        if (j + C::R < n) {
-            if (lane == 0) fence_proxy_async_smem();
-            issue(j + C::R, jbase);
-        }
-    }
-
-    if (timed_out) {   // record, then let copies already in flight land before the CTA exits
-        if (lane == 0) {
-            atomicOr(p.err, KVC_EBIT_TIMEOUT);
-            for (int jj = j; jj < min(n, j + C::R); ++jj)
-                (void)mbar_wait_bounded(bar_base + 8u * (jj % C::R), static_cast<uint32_t>((jj / C::R) & 1), 100000000ull);
-        }
-        __syncwarp();
-    } else if (ub >= 0) {
-        finish_unit();
-    }
-    if (npend > 2 && lane == 0) atomicOr(p.err, KVC_EBIT_RANGE);   // cannot happen: only first and last units are shared
-
-    // ---- merges of the units whose last share finished in this CTA (whole CTA, after every warp's range)
-    __syncthreads();
-    __threadfence();
-    for (int k = 0; k < 2 * kWarps; ++k) {
-        const int u = pend[k];
-        if (u < 0) continue;
-        const int b = u / H, hu = u - b * H;
-        const int r0 = range_of(cum[b], T, NG);
-        const int nr = range_of(cum[b + 1] - 1, T, NG) - r0 + 1;
-        const size_t row0 = static_cast<size_t>(b) * p.H_Q + static_cast<size_t>(hu) * g;
-        auto rec_of = [&](int i) { return (static_cast<size_t>(r0 + i + b) * H + hu) * g; };
-        for (int i = threadIdx.x; i < g * (D / 4); i += kThreads) {
-            const int qi = i / (D / 4), d = 4 * (i - qi * (D / 4));
-            float M = -INFINITY;
-            for (int k2 = 0; k2 < nr; ++k2) M = fmaxf(M, __ldcg(&p.part_ml[rec_of(k2) + qi].x));
-            const float Mref = M == -INFINITY ? 0.f : M;
-            float L = 0.f;
-            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int k2 = 0; k2 < nr; ++k2) {
-                const size_t rec = rec_of(k2) + qi;
-                const float2 ml = __ldcg(p.part_ml + rec);
-                const float4 o = __ldcg(reinterpret_cast<const float4 *>(p.part_o + rec * D + d));
-                const float e = fast_exp2(ml.x - Mref);
-                L += e * ml.y;
-                O.x += e * o.x;
-                O.y += e * o.y;
-                O.z += e * o.z;
-                O.w += e * o.w;
-            }
-            const float inv = 1.f / L;
-            float4 res = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
-            if constexpr (QUANT) {
-                const float4 sv = __ldg(reinterpret_cast<const float4 *>(p.s_v + static_cast<size_t>(hu) * D + d));
-                res.x *= sv.x;
-                res.y *= sv.y;
-                res.z *= sv.z;
-                res.w *= sv.w;
-            }
-            *reinterpret_cast<float4 *>(p.out + (row0 + qi) * D + d) = res;
-            if (d == 0 && p.lse) p.lse[row0 + qi] = (M + log2f(L)) * kLn2;
-        }
-        if (threadIdx.x == 0) p.counters[u] = 0u;   // every share has arrived: ready for the next launch
+    const int z = blockIdx.z;
+    const int64_t Z = gridDim.z, P = pp.B;
+    const int before = static_cast<int>((static_cast<int64_t>(z) * P) / Z);
+    const int upto = static_cast<int>((static_cast<int64_t>(z + 1) * P) / Z);
+    if (upto > before) {
+        if (static_cast<int>(blockIdx.x) < pp.max_splits)
+            decode_cta<D, 4, KIND, false, true>(tmap, pp, blockIdx.x, blockIdx.y, before);
+    } else if (static_cast<int>(blockIdx.x) < pd.max_splits) {
+        decode_cta<D, NT, KIND, PSPLIT, false>(tmap, pd, blockIdx.x, blockIdx.y, z - before);
     }
 }
 
@@ -1068,18 +703,19 @@ DecodeKernel decode_instance()
 }
 
 template <int D, int NT, int KIND, bool PSPLIT>
-DecodeKernel persistent_instance()
+DecodeKernel mixed_instance()
 {
     static DecodeKernel k = [] {
         DecodeKernel r;
-        r.fn = reinterpret_cast<const void *>(&decode_persistent_kernel<D, NT, KIND, PSPLIT>);
-        r.smem = persistent_smem_bytes<D, KIND>();
+        r.fn = reinterpret_cast<const void *>(&mixed_kernel<D, NT, KIND, PSPLIT>);
+        r.smem = decode_smem_bytes<D, NT, KIND>() > decode_smem_bytes<D, 4, KIND>() ? decode_smem_bytes<D, NT, KIND>()
+                                                                                     : decode_smem_bytes<D, 4, KIND>();
         r.ctas_per_sm = 0;
-        if (cudaFuncSetAttribute(&decode_persistent_kernel<D, NT, KIND, PSPLIT>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem) == cudaSuccess) {
+        if (cudaFuncSetAttribute(&mixed_kernel<D, NT, KIND, PSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 r.smem) == cudaSuccess) {
             int n = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_persistent_kernel<D, NT, KIND, PSPLIT>,
-                                                              kThreads, r.smem) == cudaSuccess)
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &mixed_kernel<D, NT, KIND, PSPLIT>, kThreads,
+                                                              r.smem) == cudaSuccess)
                 r.ctas_per_sm = n;
         }
         return r;
@@ -1087,11 +723,12 @@ DecodeKernel persistent_instance()
     return k;
 }
 
+// Mixed-launch kernel for a pool kind and decode group size (nullptr: unsupported shape).
+DecodeKernel select_mixed_bf16(int D, int g);
+DecodeKernel select_mixed_fp8(int D, int g);
+DecodeKernel select_mixed_int4(int D, int g);
+
 kvc_status run_decode(const kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream);
-// Launch the balanced persistent decode kernel `k` when the batch suits it
-// (decode of at most kMaxSeqPersistent sequences whose per-unit merges stay
-// small); returns KVC_ERR_UNSUPPORTED, launching nothing, when it does not.
-kvc_status run_decode_persistent(kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream);
 
 // Kernel instance selection without launching (used by the allocation-free entry point).
 DecodeKernel select_decode_bf16(int D, int g);

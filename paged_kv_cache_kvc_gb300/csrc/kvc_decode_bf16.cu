@@ -6,14 +6,6 @@
 namespace kvc {
 
 template <int D>
-static DecodeKernel pick_bf16_persistent(int NT)
-{
-    if (NT == 1) return persistent_instance<D, 1, KV_BF16, true>();
-    if (NT == 2) return persistent_instance<D, 2, KV_BF16, true>();
-    return DecodeKernel{nullptr, 0, 0};   // 32-column groups keep the split kernel
-}
-
-template <int D>
 static DecodeKernel pick_bf16(int NT, bool psplit)
 {
     if (NT == 1) return psplit ? decode_instance<D, 1, KV_BF16, true>() : decode_instance<D, 1, KV_BF16, false>();
@@ -36,12 +28,6 @@ kvc_status launch_decode_bf16(const kvc_pool *pool, DecodeParams &p, cudaStream_
         else return KVC_ERR_UNSUPPORTED;
         return run_decode(pool, p, k, stream);
     }
-    if (!e) {   // the balanced persistent kernel where the batch suits it
-        const DecodeKernel kp = pool->D == 64 ? pick_bf16_persistent<64>(NT)
-                              : pool->D == 128 ? pick_bf16_persistent<128>(NT) : DecodeKernel{nullptr, 0, 0};
-        const kvc_status st = run_decode_persistent(const_cast<kvc_pool *>(pool), p, kp, stream);
-        if (st != KVC_ERR_UNSUPPORTED) return st;
-    }
     switch (pool->D) {
     case 64: k = pick_bf16<64>(NT, psplit); break;
     case 128: k = pick_bf16<128>(NT, psplit); break;
@@ -62,6 +48,20 @@ DecodeKernel select_decode_bf16(int D, int g)
     const bool psplit = e ? e[0] != '0' : NT <= 2;
     if (D == 64) return pick_bf16<64>(NT, psplit);
     if (D == 128) return pick_bf16<128>(NT, psplit);
+    return DecodeKernel{nullptr, 0, 0};
+}
+
+}  // namespace kvc
+
+namespace kvc {
+
+// The mixed decode + prefill kernel for a bf16 pool: decode groups of up to 16 query heads.
+DecodeKernel select_mixed_bf16(int D, int g)
+{
+    const int NT = n_tiles(g);
+    if (NT > 2) return DecodeKernel{nullptr, 0, 0};
+    if (D == 64) return NT == 1 ? mixed_instance<64, 1, KV_BF16, true>() : mixed_instance<64, 2, KV_BF16, true>();
+    if (D == 128) return NT == 1 ? mixed_instance<128, 1, KV_BF16, true>() : mixed_instance<128, 2, KV_BF16, true>();
     return DecodeKernel{nullptr, 0, 0};
 }
 

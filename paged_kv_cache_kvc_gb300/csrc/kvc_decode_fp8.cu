@@ -8,13 +8,6 @@ kvc_status launch_decode_fp8(const kvc_pool *pool, DecodeParams &p, cudaStream_t
     const int NT = n_tiles(p.ppu * p.g);
     if (pool->D != 128) return KVC_ERR_UNSUPPORTED;
     if (!p.lens) return run_decode(pool, p, decode_instance<128, 4, KV_E4M3, false, true>(), stream);
-    {   // the balanced persistent kernel where the batch suits it
-        const DecodeKernel kp = NT == 1 ? persistent_instance<128, 1, KV_E4M3, false>()
-                              : NT == 2 ? persistent_instance<128, 2, KV_E4M3, false>()
-                                        : DecodeKernel{nullptr, 0, 0};   // 32-column groups keep the split kernel
-        const kvc_status st = run_decode_persistent(const_cast<kvc_pool *>(pool), p, kp, stream);
-        if (st != KVC_ERR_UNSUPPORTED) return st;
-    }
     DecodeKernel k = NT == 1 ? decode_instance<128, 1, KV_E4M3, false>()
                    : NT == 2 ? decode_instance<128, 2, KV_E4M3, false>()
                              : decode_instance<128, 4, KV_E4M3, false>();
@@ -33,6 +26,18 @@ DecodeKernel select_decode_fp8(int D, int g)
     return NT == 1 ? decode_instance<128, 1, KV_E4M3, false>()
          : NT == 2 ? decode_instance<128, 2, KV_E4M3, false>()
                    : decode_instance<128, 4, KV_E4M3, false>();
+}
+
+}  // namespace kvc
+
+namespace kvc {
+
+// The mixed decode + prefill kernel for an e4m3 pool: d_h 128, decode groups of up to 16 query heads.
+DecodeKernel select_mixed_fp8(int D, int g)
+{
+    const int NT = n_tiles(g);
+    if (D != 128 || NT > 2) return DecodeKernel{nullptr, 0, 0};
+    return NT == 1 ? mixed_instance<128, 1, KV_E4M3, false>() : mixed_instance<128, 2, KV_E4M3, false>();
 }
 
 }  // namespace kvc

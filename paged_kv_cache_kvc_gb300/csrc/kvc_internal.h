@@ -61,9 +61,7 @@ struct DecodeParams {
     const uint16_t *k_new;
     const uint16_t *v_new;
     uint8_t *pool;           // pool base (the fused append's global store)
-    // split-K arrival counters [B][H_KV], zero between launches; nullptr = merge in a separate kernel.
-    // The balanced persistent kernel uses part_o / part_ml as per-worker records
-    // [workers + B*H_KV][g][D] / [workers + B*H_KV][g] and counters per (b, h).
+    // split-K arrival counters [B][H_KV], zero between launches; nullptr = merge in a separate kernel
     uint32_t *counters;
 };
 

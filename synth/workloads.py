@@ -192,8 +192,9 @@ def _uniform(name, seed, B, H_Q, H_KV, d, ctx, L, dtype) -> Workload:
     return Workload(name, seed, B, H_Q, H_KV, d, bs, L, dtype, N, lens, bt)
 
 
-def _ragged_prefix(seed, B=64, shared=1200, chunk=600, lo=128, hi=32768) -> Workload:
+def _ragged_prefix(seed, B=64, shared=1200, chunk=600, lo=128, hi=32768, H_Q=32, H_KV=8, dtype="bf16") -> Workload:
     bs = 16
+    assert shared % bs == 0, "the shared prefix fills whole blocks"
     u = uniform_f64(seed, stream_id(_LENS), B)
     raw = np.rint(np.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))).astype(np.int64)
     lens = np.maximum(raw, shared).astype(np.int32)
@@ -204,7 +205,7 @@ def _ragged_prefix(seed, B=64, shared=1200, chunk=600, lo=128, hi=32768) -> Work
     N = sb + int((nb - sb).sum())
     perm = permutation(seed, stream_id(_PERM), N)
     bt = _tables(need, perm, bs, int(nb.max()), shared_blocks=sb)
-    w = Workload("ragged_prefix", seed, B, 32, 8, 128, bs, 1, "bf16", N, lens, bt,
+    w = Workload("ragged_prefix", seed, B, H_Q, H_KV, 128, bs, 1, dtype, N, lens, bt,
                  shared_prefix=shared, prefill=Prefill(seq=B, q_start=shared, n_q=chunk, total=total))
     w.notes["clamped_to_prefix"] = int((raw < shared).sum())
     return w

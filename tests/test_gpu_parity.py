@@ -20,6 +20,26 @@ from harness import (GpuCase, OracleCase, check_attention, dev_bits, dev_i32, fi
 pytestmark = pytest.mark.gpu
 
 
+class _env:
+    """Set one environment variable (None: unset it) for a block."""
+
+    def __init__(self, var, val):
+        self.var, self.val = var, val
+
+    def __enter__(self):
+        self.old = os.environ.get(self.var)
+        if self.val is None:
+            os.environ.pop(self.var, None)
+        else:
+            os.environ[self.var] = self.val
+
+    def __exit__(self, *a):
+        if self.old is None:
+            os.environ.pop(self.var, None)
+        else:
+            os.environ[self.var] = self.old
+
+
 def _run(kvc, w, layers=(0,), fill=0xFF, bytes_check=True, decode_layers=None):
     """Load context, append, decode on the GPU and in the oracle; compare."""
     g = GpuCase(kvc, w, fill_byte=fill)
@@ -107,6 +127,67 @@ def test_ragged_prefix_and_prefill_chunk(kvc):
         g.close()
 
 
+@pytest.mark.parametrize("case", ["ragged_prefix", "small", "fp8", "int4", "mqa"])
+def test_mixed_step_equals_step_then_prefill(kvc, case):
+    """kvc_mixed_step (a decode step and a prefill chunk in one launch) leaves
+    the pool bytes of kvc_decode_step followed by kvc_prefill_attn and gives
+    their outputs: bit-identical for bf16 pools (the same split plans), and
+    decode and prefill both within tolerance of the oracle.  The MQA case has no
+    mixed instance (32-head groups) and runs as two launches."""
+    kw = {"ragged_prefix": {},
+          "small": dict(B=6, shared=96, chunk=70, lo=16, hi=900),
+          "fp8": dict(B=6, shared=96, chunk=70, lo=16, hi=900, dtype="fp8"),
+          "int4": dict(B=6, shared=96, chunk=70, lo=16, hi=900, dtype="int4"),
+          "mqa": dict(B=3, shared=48, chunk=33, lo=16, hi=300, H_KV=1)}[case]
+    w = synth.make_workload("ragged_prefix", seed=1, **kw)
+    p = w.prefill
+    ld = layer_data(w, 0)
+    kc = w.ctx_tokens(0, 0, p.seq, p.q_start, p.total)
+    vc = w.ctx_tokens(0, 1, p.seq, p.q_start, p.total)
+    qc = w.prefill_q(0)
+    res = []
+    for mixed in (False, True):
+        g = GpuCase(kvc, w, fill_byte=0xA5)
+        try:
+            g.load_context(0, ld)
+            row = dev_i32(w.block_tables[p.seq:p.seq + 1])
+            kvc.kvc_write_tokens(g.pool, 0, row, dev_i32([p.q_start]), dev_i32([0, p.n_q]), dev_bits(kc), dev_bits(vc))
+            q, k, v = g.step_inputs(ld)
+            out = torch.empty((w.B, w.H_Q, w.d_h), device="cuda")
+            lse = torch.empty((w.B, w.H_Q), device="cuda")
+            o2 = torch.empty((p.n_q, w.H_Q, w.d_h), device="cuda")
+            l2 = torch.empty((p.n_q, w.H_Q), device="cuda")
+            n0 = kvc.kvc_launch_count()
+            if mixed:
+                kvc.kvc_mixed_step(g.pool, 0, q, g.bt_dec, g.lens_pre, k, v, out, lse, dev_bits(qc), row[0],
+                                   p.q_start, o2, l2, scale=w.scale)
+            else:
+                kvc.kvc_decode_step(g.pool, 0, q, g.bt_dec, g.lens_pre, k, v, out, lse, scale=w.scale)
+                kvc.kvc_prefill_attn(g.pool, 0, dev_bits(qc), row[0], p.q_start, o2, l2, scale=w.scale)
+            torch.cuda.synchronize()
+            assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+            res.append((g.layer_bytes(0), out.cpu(), lse.cpu(), o2.cpu(), l2.cpu(), kvc.kvc_launch_count() - n0))
+        finally:
+            g.close()
+    n, first = first_mismatch(res[0][0], res[1][0])
+    assert n == 0, f"{n} pool bytes differ, first at {first}"
+    if case != "mqa":
+        assert res[1][5] < res[0][5], "the mixed step should take fewer launches"
+    if w.dtype == "bf16":
+        for a, b in zip(res[0][1:5], res[1][1:5]):
+            assert torch.equal(a, b)
+    ref = OracleCase(w).run_layer(ld, image=False)
+    check_attention(res[1][1], res[1][2], ref["out"], ref["lse"], w.dtype, f"mixed decode {case}")
+    sc = ref["scales"]
+    K = np.concatenate([ld.k_ctx[:w.shared_prefix], kc])
+    V = np.concatenate([ld.v_ctx[:w.shared_prefix], vc])
+    if sc is not None:
+        qz = oracle.quantize_e4m3 if w.dtype == "fp8" else oracle.quantize_int4
+        K, V = qz(K, sc[0]), qz(V, sc[1])
+    ro, rl = oracle.prefill(qc, K, V, p.q_start, w.H_KV, scales=sc, scale=w.scale, kind=w.dtype)
+    check_attention(res[1][3], res[1][4], ro, rl, w.dtype, f"mixed prefill {case}")
+
+
 def test_prefix_sharing_equals_private_copies(kvc):
     """The shared-block run equals a run where every row holds a private copy
     of the prefix blocks: bit-identical outputs (same arithmetic order)."""
@@ -185,25 +266,18 @@ def test_split_counts_agree(kvc):
             os.environ.pop("KVC_SPLIT_CHUNK", None)
 
 
-@pytest.mark.parametrize("case", ["workers_per_unit", "units_per_worker", "max_batch", "over_max_batch", "fp8", "int4"])
-def test_balanced_schedule(kvc, case):
-    """The balanced persistent kernel (decode batches of up to 1 024 sequences)
-    and the split kernel (KVC_PERSISTENT=0) both within tolerance of the oracle:
-    many workers sharing a unit (merged records), many short units per worker
-    (direct writes, empty sequences), the largest batch it takes and one past it."""
+@pytest.mark.parametrize("case", ["many_splits", "many_short", "large_batch", "fp8", "int4"])
+def test_batch_shapes(kvc, case):
+    """Batches whose split plans differ: long sequences over many splits merged
+    by their last CTA, many short sequences (first tokens included), a batch of
+    1 025 sequences, e4m3 and int4 pools with lengths from 1 to 5 001."""
     rng = np.random.default_rng(7)
-    w = {"workers_per_unit": lambda: _custom(B=8, H_Q=16, H_KV=4, d_h=128, lens=[3000, 2999, 3001, 2048, 1, 4000, 17, 3333]),
-         "units_per_worker": lambda: _custom(B=300, H_Q=8, H_KV=1, d_h=64, lens=rng.integers(0, 41, 300), seed=3),
-         "max_batch": lambda: _custom(B=1024, H_Q=8, H_KV=2, d_h=128, lens=rng.integers(0, 70, 1024), seed=4),
-         "over_max_batch": lambda: _custom(B=1025, H_Q=8, H_KV=2, d_h=128, lens=rng.integers(0, 70, 1025), seed=5),
+    w = {"many_splits": lambda: _custom(B=8, H_Q=16, H_KV=4, d_h=128, lens=[3000, 2999, 3001, 2048, 1, 9000, 17, 3333]),
+         "many_short": lambda: _custom(B=300, H_Q=8, H_KV=1, d_h=64, lens=rng.integers(0, 41, 300), seed=3),
+         "large_batch": lambda: _custom(B=1025, H_Q=8, H_KV=1, d_h=128, lens=rng.integers(0, 70, 1025), seed=5),
          "fp8": lambda: _custom(B=6, H_Q=32, H_KV=8, d_h=128, lens=[5000, 1, 0, 2500, 777, 4096], dtype="fp8"),
          "int4": lambda: _custom(B=6, H_Q=32, H_KV=8, d_h=128, lens=[5000, 1, 0, 2500, 777, 4096], dtype="int4")}[case]()
-    for persistent in ("1", "0"):
-        os.environ["KVC_PERSISTENT"] = persistent
-        try:
-            _run(kvc, w, bytes_check=case not in ("max_batch", "over_max_batch"))
-        finally:
-            os.environ.pop("KVC_PERSISTENT", None)
+    _run(kvc, w, bytes_check=case != "large_batch")
 
 
 def test_block_permutation_bit_identical(kvc):
@@ -593,8 +667,11 @@ def test_prefill_tiles(kvc, ppu, H_KV, dtype):
                 assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
                 sc = None
                 K, V = ld.k_ctx, ld.v_ctx
-                if dtype != "bf16":
-                    sc = g.pool.scales_view()[0].cpu().numpy()
+                if dtype != "bf16":   # the oracle's own calibration (the GPU's is checked against it)
+                    cal = oracle.fp8_scales if dtype == "fp8" else oracle.int4_scales
+                    sc = np.stack([cal(K), cal(V)]).astype(np.float32)
+                    got = g.pool.scales_view()[0].cpu().numpy()
+                    assert np.array_equal(got.view(np.uint32), sc.view(np.uint32)), "scales differ"
                     qz = oracle.quantize_e4m3 if dtype == "fp8" else oracle.quantize_int4
                     K, V = qz(K, sc[0]), qz(V, sc[1])
                 ro, rl = oracle.prefill(qc, K, V, q_start, H_KV, scales=sc, scale=w.scale, kind=dtype)
