@@ -3,7 +3,7 @@
 #include <cmath>
 #include <cstdlib>
 
-#include "kvc_decode.cuh"
+#include "kvc_prefill.cuh"
 
 namespace kvc {
 
@@ -145,15 +145,41 @@ kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel
     return KVC_OK;
 }
 
+// The query-tiled prefill kernel serves bf16 pools with groups of at most 4 query
+// heads (KVC_PREFILL_PPU, which sizes the split kernel's causal tiles, selects those).
+static bool fast_prefill(const kvc_pool *pool, int g)
+{
+    return pool->dtype == KVC_BF16 && g <= 4 && (pool->D == 64 || pool->D == 128) && !std::getenv("KVC_PREFILL_PPU");
+}
+
+static kvc_status launch_prefill_fast(kvc_pool *pool, DecodeParams &p, cudaStream_t stream)
+{
+    const DecodeKernel k = select_prefill_bf16(pool->D, p.g);
+    if (!k.fn || k.ctas_per_sm <= 0) return KVC_ERR_UNSUPPORTED;
+    if (p.B > 65535) return KVC_ERR_UNSUPPORTED;
+    p.chunk = p.max_blocks;
+    p.max_splits = 1;
+    void *args[] = {const_cast<CUtensorMap *>(&pool->tmap), &p};
+    const cudaError_t e = cudaLaunchKernel(k.fn, dim3(1, pool->H_KV, p.B), dim3(kThreads), args, k.smem, stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return KVC_OK;
+}
+
 // A decode step (pd) and a prefill chunk (pp) in one mixed_kernel launch; each
 // part keeps the split plan it would get alone and its own partials and counters.
 static kvc_status run_mixed(kvc_pool *pool, DecodeParams &pd, DecodeParams &pp, const DecodeKernel &k,
-                            cudaStream_t stream)
+                            bool fast_prefill, cudaStream_t stream)
 {
     if (!k.fn || k.ctas_per_sm <= 0) return KVC_ERR_UNSUPPORTED;
     choose_split(pool, pd.B * pd.H_KV, pd.max_blocks, k.ctas_per_sm, &pd.chunk, &pd.max_splits, n_tiles(pd.g));
-    choose_split(pool, pp.B * pp.H_KV, pp.max_blocks, k.ctas_per_sm, &pp.chunk, &pp.max_splits,
-                 n_tiles(pp.ppu * pp.g));
+    if (fast_prefill) {   // query tiles read their whole causal range: no splits
+        pp.chunk = pp.max_blocks;
+        pp.max_splits = 1;
+    } else {
+        choose_split(pool, pp.B * pp.H_KV, pp.max_blocks, k.ctas_per_sm, &pp.chunk, &pp.max_splits,
+                     n_tiles(pp.ppu * pp.g));
+    }
     const int splits = std::max(pd.max_splits, pp.max_splits);
     if (splits > 65535 || static_cast<int64_t>(pd.B) + pp.B > 65535) return KVC_ERR_UNSUPPORTED;
     const size_t ud = static_cast<size_t>(pd.B) * pd.H_KV, up = static_cast<size_t>(pp.B) * pp.H_KV;
@@ -290,11 +316,16 @@ extern "C" kvc_status kvc_prefill_attn(kvc_pool *pool, int32_t layer, const void
     p.len_base = q_start;
     // the chunk reads positions < q_start + n_q: plan splits over those blocks only
     p.max_blocks = static_cast<int32_t>((static_cast<int64_t>(q_start) + n_q + kBS - 1) / kBS);
+    p.n_pos = n_q;
+    if (fast_prefill(pool, p.g)) {   // query tiles of 64 / g positions x g heads on the M dimension
+        p.ppu = 64 / p.g;
+        p.B = (n_q + p.ppu - 1) / p.ppu;
+        return launch_prefill_fast(pool, p, static_cast<cudaStream_t>(stream));
+    }
     int ppu = 32 / p.g;     // measured on GB300 (600-query chunk, g = 4): 1 -> 346 us, 4 -> 143 us, 8 -> 135 us
     if (const char *e = std::getenv("KVC_PREFILL_PPU")) ppu = std::atoi(e);
     ppu = std::max(1, std::min(ppu, 32 / p.g));
     p.ppu = ppu;
-    p.n_pos = n_q;
     p.B = (n_q + ppu - 1) / ppu;
     return dispatch(pool, p, static_cast<cudaStream_t>(stream));
 }
@@ -338,13 +369,14 @@ extern "C" kvc_status kvc_mixed_step(kvc_pool *pool, int32_t layer, const void *
     pp.bt_stride = 0;
     pp.len_base = q_start;
     pp.max_blocks = static_cast<int32_t>((static_cast<int64_t>(q_start) + n_q + kBS - 1) / kBS);
-    pp.ppu = std::max(1, 32 / pp.g);
+    const bool fast = fast_prefill(pool, pp.g);
+    pp.ppu = fast ? 64 / pp.g : std::max(1, 32 / pp.g);
     pp.n_pos = n_q;
     pp.B = (n_q + pp.ppu - 1) / pp.ppu;
     DecodeKernel k{nullptr, 0, 0};
     if (pool->dtype == KVC_FP8_E4M3) k = select_mixed_fp8(pool->D, pd.g);
     else if (pool->dtype == KVC_INT4) k = select_mixed_int4(pool->D, pd.g);
-    else k = select_mixed_bf16(pool->D, pd.g);
+    else k = select_mixed_bf16(pool->D, pd.g, fast);
     if (!k.fn) {   // no mixed instance for this shape: the two launches in order
         st = kvc_decode_step(pool, layer, q, num_q_heads, block_tables, max_blocks, seq_lens, B, k_new, v_new, out,
                              lse, scale, stream);
@@ -352,7 +384,7 @@ extern "C" kvc_status kvc_mixed_step(kvc_pool *pool, int32_t layer, const void *
         return kvc_prefill_attn(pool, layer, prefill_q, n_q, num_q_heads, prefill_block_table_row,
                                 prefill_max_blocks, q_start, prefill_out, prefill_lse, scale, stream);
     }
-    return run_mixed(pool, pd, pp, k, static_cast<cudaStream_t>(stream));
+    return run_mixed(pool, pd, pp, k, fast, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_t num_q_heads, int32_t max_blocks)

@@ -654,27 +654,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     decode_cta<D, NT, KIND, PSPLIT, CAUSAL>(tmap, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
-// A decode step and a prefill chunk in one launch (pages' "chunked prefill"
-// beside decode): grid (split, KV head, decode units + prefill tiles).  The
-// prefill tiles, compute-heavy and L2-resident, are spread evenly among the
-// HBM-bound decode units (tile i of P sits at the z where floor(z*P/Z)
-// steps), so the two kinds of work overlap on the SMs.
-template <int D, int NT, int KIND, bool PSPLIT>
-__global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__ CUtensorMap tmap,
-                                                         const DecodeParams pd, const DecodeParams pp)
-{
-    const int z = blockIdx.z;
-    const int64_t Z = gridDim.z, P = pp.B;
-    const int before = static_cast<int>((static_cast<int64_t>(z) * P) / Z);
-    const int upto = static_cast<int>((static_cast<int64_t>(z + 1) * P) / Z);
-    if (upto > before) {
-        if (static_cast<int>(blockIdx.x) < pp.max_splits)
-            decode_cta<D, 4, KIND, false, true>(tmap, pp, blockIdx.x, blockIdx.y, before);
-    } else if (static_cast<int>(blockIdx.x) < pd.max_splits) {
-        decode_cta<D, NT, KIND, PSPLIT, false>(tmap, pd, blockIdx.x, blockIdx.y, z - before);
-    }
-}
-
 // Fetch (and on first use configure) the kernel instance for a shape.
 struct DecodeKernel {
     const void *fn;
@@ -701,32 +680,6 @@ DecodeKernel decode_instance()
     }();
     return k;
 }
-
-template <int D, int NT, int KIND, bool PSPLIT>
-DecodeKernel mixed_instance()
-{
-    static DecodeKernel k = [] {
-        DecodeKernel r;
-        r.fn = reinterpret_cast<const void *>(&mixed_kernel<D, NT, KIND, PSPLIT>);
-        r.smem = decode_smem_bytes<D, NT, KIND>() > decode_smem_bytes<D, 4, KIND>() ? decode_smem_bytes<D, NT, KIND>()
-                                                                                     : decode_smem_bytes<D, 4, KIND>();
-        r.ctas_per_sm = 0;
-        if (cudaFuncSetAttribute(&mixed_kernel<D, NT, KIND, PSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 r.smem) == cudaSuccess) {
-            int n = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &mixed_kernel<D, NT, KIND, PSPLIT>, kThreads,
-                                                              r.smem) == cudaSuccess)
-                r.ctas_per_sm = n;
-        }
-        return r;
-    }();
-    return k;
-}
-
-// Mixed-launch kernel for a pool kind and decode group size (nullptr: unsupported shape).
-DecodeKernel select_mixed_bf16(int D, int g);
-DecodeKernel select_mixed_fp8(int D, int g);
-DecodeKernel select_mixed_int4(int D, int g);
 
 kvc_status run_decode(const kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream);
 

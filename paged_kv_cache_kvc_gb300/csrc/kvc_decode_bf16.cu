@@ -1,7 +1,7 @@
 // bf16-pool instances of the decode-attention kernel.
 #include <cstdlib>
 
-#include "kvc_decode.cuh"
+#include "kvc_prefill.cuh"
 
 namespace kvc {
 
@@ -55,13 +55,27 @@ DecodeKernel select_decode_bf16(int D, int g)
 
 namespace kvc {
 
-// The mixed decode + prefill kernel for a bf16 pool: decode groups of up to 16 query heads.
-DecodeKernel select_mixed_bf16(int D, int g)
+// The mixed decode + prefill kernel for a bf16 pool: decode groups of up to 16 query heads;
+// fast_prefill (groups of at most 4) takes the query-tiled prefill.
+DecodeKernel select_mixed_bf16(int D, int g, bool fast_prefill)
 {
     const int NT = n_tiles(g);
-    if (NT > 2) return DecodeKernel{nullptr, 0, 0};
-    if (D == 64) return NT == 1 ? mixed_instance<64, 1, KV_BF16, true>() : mixed_instance<64, 2, KV_BF16, true>();
-    if (D == 128) return NT == 1 ? mixed_instance<128, 1, KV_BF16, true>() : mixed_instance<128, 2, KV_BF16, true>();
+    if (NT > 2 || (fast_prefill && g > 4)) return DecodeKernel{nullptr, 0, 0};
+    const bool fast = fast_prefill;
+    if (D == 64)
+        return NT == 2 ? mixed_instance<64, 2, KV_BF16, true, false>()
+             : fast    ? mixed_instance<64, 1, KV_BF16, true, true>() : mixed_instance<64, 1, KV_BF16, true, false>();
+    if (D == 128)
+        return NT == 2 ? mixed_instance<128, 2, KV_BF16, true, false>()
+             : fast    ? mixed_instance<128, 1, KV_BF16, true, true>() : mixed_instance<128, 1, KV_BF16, true, false>();
+    return DecodeKernel{nullptr, 0, 0};
+}
+
+DecodeKernel select_prefill_bf16(int D, int g)
+{
+    if (g > 4) return DecodeKernel{nullptr, 0, 0};
+    if (D == 64) return prefill_instance<64>();
+    if (D == 128) return prefill_instance<128>();
     return DecodeKernel{nullptr, 0, 0};
 }
 

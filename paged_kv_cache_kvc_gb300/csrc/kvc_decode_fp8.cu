@@ -1,5 +1,5 @@
 // e4m3-pool instances of the decode-attention kernel.
-#include "kvc_decode.cuh"
+#include "kvc_prefill.cuh"
 
 namespace kvc {
 
@@ -37,7 +37,7 @@ DecodeKernel select_mixed_fp8(int D, int g)
 {
     const int NT = n_tiles(g);
     if (D != 128 || NT > 2) return DecodeKernel{nullptr, 0, 0};
-    return NT == 1 ? mixed_instance<128, 1, KV_E4M3, false>() : mixed_instance<128, 2, KV_E4M3, false>();
+    return NT == 1 ? mixed_instance<128, 1, KV_E4M3, false, false>() : mixed_instance<128, 2, KV_E4M3, false, false>();
 }
 
 }  // namespace kvc

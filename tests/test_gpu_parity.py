@@ -642,6 +642,33 @@ def test_allocator_copy_on_write_decode(kvc, dtype):
         alloc.close()
 
 
+@pytest.mark.parametrize("d_h", [64, 128])
+@pytest.mark.parametrize("H_KV", [32, 16, 8])
+def test_prefill_query_tiles(kvc, H_KV, d_h):
+    """The query-tiled prefill kernel (bf16, groups of 1, 2, 4 query heads): chunks
+    starting at 0 and inside a block, short and partial query tiles, several
+    64-key stages, a row whose last block is part-filled; NaN in every unused
+    pool byte; against the oracle."""
+    H_Q = 32
+    for q_start, n_q in ((0, 37), (45, 23), (200, 61), (1, 130), (333, 200)):
+        total = q_start + n_q
+        w = _custom(B=1, H_Q=H_Q, H_KV=H_KV, d_h=d_h, lens=[total], seed=q_start + n_q + H_KV)
+        ld = layer_data(w, 0, with_step=False)
+        g = GpuCase(kvc, w, fill_byte=0xFF)
+        try:
+            g.load_context(0, ld)
+            qc = synth.normal_bf16(11, n_q, n_q * H_Q * d_h).reshape(n_q, H_Q, d_h)
+            out = torch.full((n_q, H_Q, d_h), float("nan"), device="cuda")
+            lse = torch.full((n_q, H_Q), float("nan"), device="cuda")
+            kvc.kvc_prefill_attn(g.pool, 0, dev_bits(qc), g.bt[0], q_start, out, lse, scale=w.scale)
+            torch.cuda.synchronize()
+            assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+            ro, rl = oracle.prefill(qc, ld.k_ctx, ld.v_ctx, q_start, H_KV, scale=w.scale)
+            check_attention(out, lse, ro, rl, "bf16", f"query tiles q_start={q_start} n_q={n_q}")
+        finally:
+            g.close()
+
+
 @pytest.mark.parametrize("ppu", ["1", "3", "4", "8"])
 @pytest.mark.parametrize("H_KV,dtype", [(8, "bf16"), (2, "bf16"), (32, "bf16"), (8, "fp8"), (8, "int4")])
 def test_prefill_tiles(kvc, ppu, H_KV, dtype):
