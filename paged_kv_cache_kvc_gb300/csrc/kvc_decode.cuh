@@ -109,6 +109,16 @@ __device__ __forceinline__ uint32_t nibbles_to_f16x2(uint32_t x)
     return r;
 }
 
+// int4: the nibbles at bits 4..7 and 20..23 of x -> f16x2 of q, exact: masked into
+// the mantissa they read 1024 + 16 u, and (1024 + 16 u) / 16 - 72 = u - 8 in one fma
+__device__ __forceinline__ uint32_t nibbles_hi_to_f16x2(uint32_t x)
+{
+    const uint32_t biased = (x & 0x00F000F0u) | 0x64006400u;
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(biased), "r"(0x2C002C00u), "r"(0xD480D480u));
+    return r;
+}
+
 // int4 quantisation of one value: rint(x / s) clamped to [-7, 7], stored + 8; NaN stores 0
 __device__ __forceinline__ uint32_t int4_code(float x, float s)
 {
@@ -192,17 +202,22 @@ __device__ __forceinline__ void block_update(uint32_t st, const uint32_t (&qf)[N
     using C = DecodeCfg<D, KIND>;
     constexpr bool INT4 = KIND == KV_INT4, QUANT = KIND != KV_BF16;
     const int gq = lane >> 2, tg = lane & 3;
-    // ---- S^T = K Q^T
-    float sc[NT][4];
+    // ---- S^T = K Q^T; with one n-tile, even and odd k-steps accumulate apart (two
+    // dependent mma chains of D/32 instead of one of D/16), summed after
+    constexpr int NACC = NT == 1 ? 2 : 1;
+    float sc[NT][4], sc2[NT][4];
 #pragma unroll
-    for (int jn = 0; jn < NT; ++jn) sc[jn][0] = sc[jn][1] = sc[jn][2] = sc[jn][3] = 0.f;
+    for (int jn = 0; jn < NT; ++jn)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sc[jn][c] = sc2[jn][c] = 0.f;
+    auto acc = [&](int jn, int kk) -> float(&)[4] { return (NACC == 2 && (kk & 1)) ? sc2[jn] : sc[jn]; };
     if constexpr (!QUANT) {
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
             uint32_t a[4];
             ldsm_x4(a, st + swz((lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)));
 #pragma unroll
-            for (int jn = 0; jn < NT; ++jn) mma_bf16(sc[jn], a, qf[jn][kk]);
+            for (int jn = 0; jn < NT; ++jn) mma_bf16(acc(jn, kk), a, qf[jn][kk]);
         }
     } else if constexpr (INT4) {
         uint32_t kw[2][4];   // rows gq, gq+8: this thread's 32-channel chunk tg (8 nibbles a word)
@@ -217,13 +232,14 @@ __device__ __forceinline__ void block_update(uint32_t st, const uint32_t (&qf)[N
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
             const int sh = 8 * (kk & 1);   // nibbles (2e, 2e+4) and (2e+1, 2e+5) of word kk / 2
+            const uint32_t w0 = kw[0][kk >> 1] >> sh, w1 = kw[1][kk >> 1] >> sh;
             uint32_t a[4];
-            a[0] = nibbles_to_f16x2(kw[0][kk >> 1] >> sh);
-            a[2] = nibbles_to_f16x2(kw[0][kk >> 1] >> (sh + 4));
-            a[1] = nibbles_to_f16x2(kw[1][kk >> 1] >> sh);
-            a[3] = nibbles_to_f16x2(kw[1][kk >> 1] >> (sh + 4));
+            a[0] = nibbles_to_f16x2(w0);
+            a[2] = nibbles_hi_to_f16x2(w0);
+            a[1] = nibbles_to_f16x2(w1);
+            a[3] = nibbles_hi_to_f16x2(w1);
 #pragma unroll
-            for (int jn = 0; jn < NT; ++jn) mma_f16(sc[jn], a, qf[jn][kk]);
+            for (int jn = 0; jn < NT; ++jn) mma_f16(acc(jn, kk), a, qf[jn][kk]);
         }
     } else {
         uint32_t kw[2][D / 16];   // rows gq, gq+8: this thread's D/4 code bytes each
@@ -243,9 +259,12 @@ __device__ __forceinline__ void block_update(uint32_t st, const uint32_t (&qf)[N
             e4m3x4_to_f16x2x2(kw[0][kk], a[0], a[2]);
             e4m3x4_to_f16x2x2(kw[1][kk], a[1], a[3]);
 #pragma unroll
-            for (int jn = 0; jn < NT; ++jn) mma_f16(sc[jn], a, qf[jn][kk]);
+            for (int jn = 0; jn < NT; ++jn) mma_f16(acc(jn, kk), a, qf[jn][kk]);
         }
     }
+    if constexpr (NACC == 2)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sc[0][c] += sc2[0][c];
 
     // ---- online softmax (log2 domain); column = query head, rows = tokens gq, gq+8
     uint32_t pb[NT][2], pl[NT][2];
@@ -322,8 +341,8 @@ __device__ __forceinline__ void block_update(uint32_t st, const uint32_t (&qf)[N
                 constexpr uint32_t kSel[4] = {0x4400u, 0x5511u, 0x6622u, 0x7733u};   // [A.b_k, A.b_k, B.b_k, B.b_k]
                 const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], kSel[k]);
                 const uint32_t x89 = __byte_perm(vw[2][w], vw[3][w], kSel[k]);
-                const uint32_t a[4] = {nibbles_to_f16x2(x01), nibbles_to_f16x2(x01 >> 4),
-                                       nibbles_to_f16x2(x89), nibbles_to_f16x2(x89 >> 4)};
+                const uint32_t a[4] = {nibbles_to_f16x2(x01), nibbles_hi_to_f16x2(x01),
+                                       nibbles_to_f16x2(x89), nibbles_hi_to_f16x2(x89)};
 #pragma unroll
                 for (int jn = 0; jn < NT; ++jn) mma_f16(oacc[4 * w + k][jn], a, pb[jn]);
             }
