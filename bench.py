@@ -74,8 +74,8 @@ def prefill_flops(w) -> int:
 
 
 # the sources the decode kernel is compiled from (its ncu counters go stale when one changes)
-KERNEL_SOURCES = ["kvc_decode.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_decode_bf16.cu", "kvc_decode_fp8.cu",
-                  "kvc_attn.cu"]
+KERNEL_SOURCES = ["kvc_decode.cuh", "kvc_prefill.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_decode_bf16.cu",
+                  "kvc_decode_fp8.cu", "kvc_decode_int4.cu", "kvc_attn.cu"]
 
 
 def source_digest() -> str:
@@ -87,11 +87,13 @@ def source_digest() -> str:
 
 
 def profiled_traffic(workload: str):
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
-    if it was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_step_{workload}.md")
-    if not os.path.exists(path):
+    """Per-launch DRAM bytes of the step's kernel from the committed ncu summary
+    (profiles/*_<workload>.md), if it was taken on the current kernel sources; else None."""
+    import glob
+    paths = sorted(glob.glob(os.path.join(ROOT, "profiles", f"*_step_{workload}.md")))
+    if not paths:
         return None
+    path = paths[0]
     fields = {}
     for line in open(path):
         if line.startswith("<!-- ") and ":" in line:
