@@ -394,42 +394,63 @@ def main():
     # pinned host memory and its results back.  Copies run on their own streams,
     # double-buffered, so step i's inputs arrive while step i-1 computes and its
     # results leave while step i+1 computes (a serving loop's overlap).
-    pin = lambda t: t.cpu().pin_memory()
-    # per-layer inputs and results of the step (the chunk's queries and outputs too, if any)
+    # per-layer inputs and results of the step (the chunk's queries and outputs too, if any); each side
+    # lives in one buffer (256-byte aligned views), so a step is one host-to-device copy and one back
     ins = {"q": q, "k": k_new, "v": v_new}
     res = {"out": outs, "lse": lses}
     if pf is not None:
         ins["pq"] = pq
         res.update(p_out=p_out, p_lse=p_lse)
-    host_in = {n: [pin(t) for t in ts] for n, ts in ins.items()}
-    bt_h, lp_h = pin(g.bt_dec), pin(g.lens_pre)
+    in_list = [t for ts in ins.values() for t in ts] + [g.bt_dec, g.lens_pre]
+    res_list = [t for ts in res.values() for t in ts]
+
+    def layout(ts):
+        offs, n = [], 0
+        for t in ts:
+            offs.append(n)
+            n += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, n
+
+    def views(buf, ts, offs):
+        return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(ts, offs)]
+
+    in_offs, in_bytes = layout(in_list)
+    res_offs, res_bytes = layout(res_list)
+    host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    for hv, t in zip(views(host_in, in_list, in_offs), in_list):
+        hv.copy_(t.cpu())
     sets = []          # two device buffer sets: inputs and results of alternate steps
     for _ in range(2):
-        d = {n: [torch.empty_like(t) for t in ts] for n, ts in list(ins.items()) + list(res.items())}
-        d.update({n + "_h": [torch.empty_like(t, device="cpu").pin_memory() for t in ts] for n, ts in res.items()})
-        d.update(bt=torch.empty_like(g.bt_dec), lp=torch.empty_like(g.lens_pre))
+        d_in = torch.empty(in_bytes, dtype=torch.uint8, device="cuda")
+        d_res = torch.empty(res_bytes, dtype=torch.uint8, device="cuda")
+        h_res = torch.empty(res_bytes, dtype=torch.uint8).pin_memory()
+        iv, rv = views(d_in, in_list, in_offs), views(d_res, res_list, res_offs)
+        d = {"in": d_in, "res": d_res, "res_h": h_res, "res_views": rv, "res_h_views": views(h_res, res_list, res_offs)}
+        k_ = 0
+        for n, ts in ins.items():
+            d[n] = iv[k_:k_ + len(ts)]
+            k_ += len(ts)
+        d["bt"], d["lp"] = iv[k_], iv[k_ + 1]
+        k_ = 0
+        for n, ts in res.items():
+            d[n] = rv[k_:k_ + len(ts)]
+            k_ += len(ts)
         sets.append(d)
-    h2d = sum(t.numel() * t.element_size() for ts in host_in.values() for t in ts) + \
-        sum(t.numel() * t.element_size() for t in (bt_h, lp_h))
-    d2h = sum(t.numel() * t.element_size() for n in res for t in sets[0][n + "_h"])
+    h2d = sum(t.numel() * t.element_size() for t in in_list)
+    d2h = sum(t.numel() * t.element_size() for t in res_list)
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
-    computed, drained = [ev(), ev()], [ev(), ev()]
+    computed, drained, loaded = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     for e in computed + drained:
         e.record(stream)
 
     def e2e_step(i):
         b = sets[i % 2]
-        loaded = ev()
         with torch.cuda.stream(s_in):
             s_in.wait_event(computed[i % 2])          # step i-2 has finished reading this set's inputs
-            b["bt"].copy_(bt_h, non_blocking=True)
-            b["lp"].copy_(lp_h, non_blocking=True)
-            for n, ts in host_in.items():
-                for layer in range(L):
-                    b[n][layer].copy_(ts[layer], non_blocking=True)
-            loaded.record(s_in)
-        stream.wait_event(loaded)
+            b["in"].copy_(host_in, non_blocking=True)
+            loaded[i % 2].record(s_in)
+        stream.wait_event(loaded[i % 2])
         stream.wait_event(drained[i % 2])             # step i-2's results have left this set
         for layer in range(L):
             launch(layer, b["q"][layer], b["bt"], b["lp"], b["k"][layer], b["v"][layer], b["out"][layer],
@@ -438,9 +459,7 @@ def main():
         computed[i % 2].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(computed[i % 2])
-            for n in res:
-                for layer in range(L):
-                    b[n + "_h"][layer].copy_(b[n][layer], non_blocking=True)
+            b["res_h"].copy_(b["res"], non_blocking=True)
             drained[i % 2].record(s_out)
 
     for i in range(min(4, K)):                        # warm the copy path
@@ -456,9 +475,9 @@ def main():
     barrier()
     e2e_ms = e_start.elapsed_time(e_end) / K
     torch.cuda.synchronize()
-    for n in res:                                     # the copied-back results are the kernel's
-        for layer in range(L):
-            assert torch.equal(sets[(K - 1) % 2][n + "_h"][layer], sets[(K - 1) % 2][n][layer].cpu())
+    last = sets[(K - 1) % 2]                          # the copied-back results are the kernel's
+    for hv, dv in zip(last["res_h_views"], last["res_views"]):
+        assert torch.equal(hv, dv.cpu())
 
     # ---- max over ranks
     ms, e2e_ms, attn_ms = max_over_ranks([ms, e2e_ms, attn_ms], dist, "cuda")
