@@ -69,6 +69,14 @@ void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_
     *max_splits = (max_blocks + ch - 1) / ch;
 }
 
+// The last split CTA of a unit merges its partials in the kernel while that is a
+// small job (query columns x splits partial rows); larger merges run as merge_kernel.
+static int merge_rows_limit()
+{
+    const char *e = std::getenv("KVC_MERGE_ROWS");
+    return e ? std::atoi(e) : 64;
+}
+
 // The workspace holds the arrival counters at its front, at a fixed place
 // whatever the batch (every launch leaves them at zero, so a later launch of
 // another shape may use them), then the partials.  It grows by reallocation
@@ -125,7 +133,7 @@ kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel
         p.part_ml = reinterpret_cast<float2 *>(p.part_o + n * pool->D);
         // the last split CTA merges its group in the kernel when that is a small job (g * splits
         // partial rows); otherwise one merge CTA per (sequence, query head) does it afterwards
-        p.counters = (p.ppu * p.g * p.max_splits <= 64) ? ws_counters(pool) : nullptr;
+        p.counters = (p.ppu * p.g * p.max_splits <= merge_rows_limit()) ? ws_counters(pool) : nullptr;
     } else {
         p.part_o = nullptr;
         p.part_ml = nullptr;
@@ -191,11 +199,11 @@ static kvc_status run_mixed(kvc_pool *pool, DecodeParams &pd, DecodeParams &pp, 
     float *data = ws_data(pool);
     pd.part_o = nd ? data : nullptr;
     pd.part_ml = nd ? reinterpret_cast<float2 *>(data + nd * pool->D) : nullptr;
-    pd.counters = (nd && pd.ppu * pd.g * pd.max_splits <= 64) ? ws_counters(pool) : nullptr;
+    pd.counters = (nd && pd.ppu * pd.g * pd.max_splits <= merge_rows_limit()) ? ws_counters(pool) : nullptr;
     float *data_p = data + nd * pool->D + nd * 2;
     pp.part_o = np ? data_p : nullptr;
     pp.part_ml = np ? reinterpret_cast<float2 *>(data_p + np * pool->D) : nullptr;
-    pp.counters = (np && pp.ppu * pp.g * pp.max_splits <= 64) ? ws_counters(pool) + ud : nullptr;
+    pp.counters = (np && pp.ppu * pp.g * pp.max_splits <= merge_rows_limit()) ? ws_counters(pool) + ud : nullptr;
     void *args[] = {const_cast<CUtensorMap *>(&pool->tmap), &pd, &pp};
     cudaError_t e = cudaLaunchKernel(k.fn, dim3(splits, pool->H_KV, pd.B + pp.B), dim3(kThreads), args, k.smem,
                                      stream);
