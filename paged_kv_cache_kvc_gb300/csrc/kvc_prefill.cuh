@@ -10,8 +10,8 @@
 // head h * g + (w mod g), so the g heads that share a KV head share every
 // staged key/value tile.  Per stage the CTA stages 64 keys (4 blocks of the
 // row, one contiguous keys-then-values run per block and head, TMA with the
-// 128-byte swizzle) in a ring of 3 stages, and each warp runs, on mma.sync
-// m16n8k16 with fp32 accumulation:
+// 128-byte swizzle) in a ring of 3 stages; the last warp done with a stage
+// refills it.  Each warp runs, on mma.sync m16n8k16 with fp32 accumulation:
 //   S[16 pos x 64 keys]  = Q[16 x D] K^T          (Q fragments in registers)
 //   online softmax per row (quad shuffles), causal mask on key > position
 //   O[16 x D]           += P[16 x 64] V            (P re-packed from S in registers)
@@ -32,7 +32,7 @@ struct PrefillCfg {
     static constexpr int BANDS = D * 2 / 128;
     static constexpr int KSTEPS = D / 16;                       // QK k-steps
     static constexpr int NDIM = D / 8;                          // PV n-tiles
-    static constexpr int SMEM = 1024 /* alignment slack */ + kPrefillRing * STAGE + kPrefillRing * 8 + 64;
+    static constexpr int SMEM = 1024 /* alignment slack */ + kPrefillRing * STAGE + kPrefillRing * 8 + 64;   // + masks, counts
 };
 
 // CTA (tile, h) of a prefill chunk: p.len_base = q_start, p.n_pos = n_q,
@@ -47,6 +47,7 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &tmap, const Decod
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kPrefillRing * C::STAGE);
     uint32_t *valid_mask = reinterpret_cast<uint32_t *>(bars + kPrefillRing);   // [ring] blocks staged per stage
+    int *done_warps = reinterpret_cast<int *>(valid_mask + kPrefillRing);         // [ring] warps finished with it
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, tg = lane & 3;
@@ -62,13 +63,16 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &tmap, const Decod
     const int64_t row_layer = static_cast<int64_t>(p.layer) * p.N;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kPrefillRing; ++s) mbar_init(smem_u32(&bars[s]), 1);
+        for (int s = 0; s < kPrefillRing; ++s) {
+            mbar_init(smem_u32(&bars[s]), 1);
+            done_warps[s] = 0;
+        }
         fence_barrier_init();
         prefetch_tensormap(&tmap);
     }
     __syncthreads();
 
-    // stage tile jj (thread 0): the row's blocks 4jj .. 4jj+3 that hold needed keys
+    // stage tile jj (one thread): the row's blocks 4jj .. 4jj+3 that hold needed keys
     auto issue = [&](int jj) {
         const int s = jj % kPrefillRing;
         const uint32_t bar = smem_u32(&bars[s]);
@@ -102,6 +106,7 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &tmap, const Decod
     };
     if (threadIdx.x == 0)
         for (int jj = 0; jj < min(kPrefillRing, n_tiles); ++jj) issue(jj);
+    __syncthreads();   // the first stages' masks are written
 
     // ---- query fragments (A operand: rows = positions pos0 + gq (+8), k = channel)
     uint32_t qf[C::KSTEPS][4];
@@ -125,32 +130,30 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &tmap, const Decod
 #pragma unroll
     for (int nd = 0; nd < C::NDIM; ++nd) oacc[nd][0] = oacc[nd][1] = oacc[nd][2] = oacc[nd][3] = 0.f;
 
-    bool timed_out = false;
-    int j = 0;
-    for (; j < n_tiles; ++j) {
-        const int s = j % kPrefillRing;
-        const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), static_cast<uint32_t>((j / kPrefillRing) & 1));
-        if (__syncthreads_or(!ok)) {
-            timed_out = true;
-            break;
-        }
-        const uint32_t st = smem_u32(smem + s * C::STAGE);
-        const uint32_t mask = valid_mask[s];
-        const int key0 = j * kPrefillKeys;
-        // value rows that must read as zero (their weights are 0, but 0 * NaN is not):
-        // blocks not staged, and slots past the row's end
-        if (mask != (1u << C::BLOCKS) - 1u || (j + 1) * kPrefillKeys > total) {
-            for (int i = threadIdx.x; i < C::BLOCKS * kBS * C::BANDS * 8; i += kThreads) {
+    // wait (bounded) for tile jj's stage; zero the value rows that must read as zero (their
+    // weights are 0, but 0 * NaN is not): blocks not staged, and slots past the row's end.
+    // Every warp zeroes them for itself (the same zeros; the stage's copies have landed).
+    auto acquire = [&](int jj, uint32_t &st, uint32_t &mask) -> bool {
+        const int s = jj % kPrefillRing;
+        const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), static_cast<uint32_t>((jj / kPrefillRing) & 1));
+        if (!__all_sync(kFull, ok)) return false;
+        st = smem_u32(smem + s * C::STAGE);
+        mask = valid_mask[s];
+        const int key0 = jj * kPrefillKeys;
+        if (mask != (1u << C::BLOCKS) - 1u || key0 + kPrefillKeys > total) {
+            for (int i = lane; i < C::BLOCKS * kBS * C::BANDS * 8; i += 32) {
                 const int k = i / (kBS * C::BANDS * 8), rem = i - k * (kBS * C::BANDS * 8);
                 const int slot = rem / (C::BANDS * 8), ch = rem - slot * (C::BANDS * 8);
                 const bool dead = !(mask >> k & 1u) || key0 + k * kBS + slot >= total;
                 if (dead) sts128_zero(st + k * C::BLK + swz(kBS + slot, ch));
             }
-            __syncthreads();
+            __syncwarp();
         }
+        return true;
+    };
 
-        // ---- S = Q K^T over the 64 staged keys (8 n-tiles of 8 keys)
-        float sc[8][4];
+    // S = Q K^T over a stage's 64 keys (8 n-tiles of 8 keys)
+    auto qk = [&](uint32_t st, float (&sc)[8][4]) {
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
@@ -166,8 +169,10 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &tmap, const Decod
                 mma_bf16(sc[nt], qf[kk + 1], b1);
             }
         }
+    };
 
-        // ---- mask (causal, staged blocks only), online softmax (log2 domain)
+    // mask (causal, staged blocks only) and online softmax (log2 domain); P into A fragments
+    auto softmax = [&](float (&sc)[8][4], int key0, uint32_t mask, uint32_t (&pf)[4][4]) {
         float bm[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
@@ -197,9 +202,8 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &tmap, const Decod
             oacc[nd][2] *= alpha[1];
             oacc[nd][3] *= alpha[1];
         }
-        uint32_t pf[4][4];   // P as A fragments, k-step = 16 keys (n-tiles 2kk, 2kk+1)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
+        for (int nt = 0; nt < 8; ++nt) {   // k-step = 16 keys (n-tiles 2kk, 2kk+1)
             const float p0 = fast_exp2(sc[nt][0] - mref[0]), p1 = fast_exp2(sc[nt][1] - mref[0]);
             const float p2 = fast_exp2(sc[nt][2] - mref[1]), p3 = fast_exp2(sc[nt][3] - mref[1]);
             l_run[0] += p0 + p1;
@@ -207,8 +211,10 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &tmap, const Decod
             pf[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(p0, p1);
             pf[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(p2, p3);
         }
+    };
 
-        // ---- O += P V (V^T fragments by ldmatrix.trans; one block of 16 keys per k-step)
+    // O += P V (V^T fragments by ldmatrix.trans; one block of 16 keys per k-step)
+    auto pv = [&](uint32_t st, const uint32_t (&pf)[4][4]) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const uint32_t vblk = st + kk * C::BLK;
@@ -221,16 +227,45 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &tmap, const Decod
                 mma_bf16(oacc[nd + 1], pf[kk], b1);
             }
         }
+    };
 
-        __syncthreads();   // every warp is done with stage s
-        if (threadIdx.x == 0 && j + kPrefillRing < n_tiles) {
-            fence_proxy_async_smem();
-            issue(j + kPrefillRing);
+    // the last warp done with tile jj's stage refills it with tile jj + ring (no CTA-wide barrier)
+    auto release = [&](int jj) {
+        const int s = jj % kPrefillRing;
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&done_warps[s], 1) == kWarps - 1) {
+                done_warps[s] = 0;
+                if (jj + kPrefillRing < n_tiles) {
+                    __threadfence_block();
+                    fence_proxy_async_smem();
+                    issue(jj + kPrefillRing);
+                }
+            }
         }
+    };
+
+    // one stage at a time (issuing the next stage's scores ahead of this stage's value
+    // mixture measured slower on GB300: 73.6 vs 69.6 us for a 600-query chunk)
+    bool timed_out = false;
+    int j = 0;
+    for (; j < n_tiles; ++j) {
+        uint32_t st = 0, mask = 0;
+        if (!acquire(j, st, mask)) {
+            timed_out = true;
+            break;
+        }
+        float sc[8][4];
+        uint32_t pf[4][4];
+        qk(st, sc);
+        softmax(sc, j * kPrefillKeys, mask, pf);
+        pv(st, pf);
+        release(j);
     }
 
     if (timed_out) {   // record, then let copies already in flight land before the CTA exits
-        if (threadIdx.x == 0) {
+        if (lane == 0) {
             atomicOr(p.err, KVC_EBIT_TIMEOUT);
             for (int jj = j; jj < min(n_tiles, j + kPrefillRing); ++jj)
                 (void)mbar_wait_bounded(smem_u32(&bars[jj % kPrefillRing]),
@@ -239,6 +274,7 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &tmap, const Decod
         __syncthreads();
         return;
     }
+    __syncthreads();   // no warp leaves while another may still refill a stage
 
     // ---- write out / lse of the real rows
 #pragma unroll
