@@ -39,8 +39,9 @@ KIND_E4M3, KIND_BF16, KIND_INT4 = 1, 2, 3       # stored-scalar kinds (same code
 _lib = None
 
 
-def build_command(out_path: str = LIB_PATH) -> list[str]:
-    return ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", out_path, "-lm"]
+def build_command(out_path: str = LIB_PATH, mutant: int = 0) -> list[str]:
+    extra = [f"-DORC_MUTANT={mutant}"] if mutant else []
+    return ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", *extra, _SRC, "-o", out_path, "-lm"]
 
 
 def build(force: bool = False) -> str:
@@ -55,8 +56,9 @@ def build(force: bool = False) -> str:
 def lib():
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(LIB_PATH)
+        # KVC_ORACLE_LIB: a build of this source with a planted mistake (the mutation test)
+        path = os.environ.get("KVC_ORACLE_LIB") or build()
+        L = ctypes.CDLL(path)
         i64, i32, u64, vp, dbl = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_double
         L.orc_kv_bytes.restype = u64
         L.orc_kv_bytes.argtypes = [i64] * 6

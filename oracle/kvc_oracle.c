@@ -29,6 +29,15 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* Planted mistakes for the mutation test of the pins (tests/test_oracle_mutants.py):
+ * built with -DORC_MUTANT=n, the oracle carries mistake n -- a dropped term, a
+ * wrong constant, sign, index or operand -- and the pins must fail.  The oracle
+ * proper is built without it (ORC_MUTANT 0: every ORC_MUT(n) is false). */
+#ifndef ORC_MUTANT
+#define ORC_MUTANT 0
+#endif
+#define ORC_MUT(n) (ORC_MUTANT == (n))
+
 /* stored-scalar kinds: bf16 (2 bytes), OCP E4M3 (1 byte), int4 (half a byte in
  * the pool; one byte per element in logical lists) */
 #define ORC_KIND_E4M3 1
@@ -49,7 +58,7 @@ static int logical_bytes(int kind) { return kind == ORC_KIND_BF16 ? 2 : 1; }
  * UINT64_MAX when a factor is negative or the product overflows. */
 uint64_t orc_kv_bytes(int64_t layers, int64_t B, int64_t H_KV, int64_t T, int64_t d_h, int64_t s)
 {
-    const int64_t f[6] = {2, layers, B, H_KV, T, d_h};
+    const int64_t f[6] = {ORC_MUT(1) ? 1 : 2, layers, B, H_KV, T, d_h};   /* 1: keys only */
     uint64_t acc = (uint64_t)(s < 0 ? 0 : s);
     if (s < 0) return UINT64_MAX;
     for (int i = 0; i < 6; ++i) {
@@ -64,14 +73,14 @@ uint64_t orc_kv_bytes(int64_t layers, int64_t B, int64_t H_KV, int64_t T, int64_
 /* [P1] Eq. 21.3: growth for one more processed position in each of B requests. */
 uint64_t orc_kv_bytes_growth(int64_t layers, int64_t B, int64_t H_KV, int64_t d_h, int64_t s)
 {
-    return orc_kv_bytes(layers, B, H_KV, 1, d_h, s);
+    return orc_kv_bytes(layers, B, H_KV, ORC_MUT(2) ? 2 : 1, d_h, s);   /* 2: two positions */
 }
 
 /* ---------------------------------------------------------------- scalars
  * bf16 -> double: the bit pattern is the upper half of an IEEE binary32. */
 double orc_bf16_to_double(uint16_t bits)
 {
-    const uint32_t w = (uint32_t)bits << 16;
+    const uint32_t w = (uint32_t)bits << (ORC_MUT(3) ? 15 : 16);   /* 3: misplaced half */
     float f;
     memcpy(&f, &w, 4);
     return (double)f;
@@ -88,8 +97,8 @@ double orc_e4m3_to_double(uint8_t code)
     const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
     double v;
     if (e == 15 && m == 7) return NAN;
-    if (e == 0) v = ldexp((double)m, -9);
-    else v = ldexp(8.0 + m, e - 10);   /* (1 + m/8) * 2^(e-7) */
+    if (e == 0) v = ldexp((double)m, ORC_MUT(4) ? -10 : -9);              /* 4: subnormal step */
+    else v = ldexp(8.0 + m, e - (ORC_MUT(5) ? 11 : 10));   /* (1 + m/8) * 2^(e-7); 5: bias 8 */
     return sign ? -v : v;
 }
 
@@ -104,13 +113,14 @@ uint8_t orc_e4m3_from_float(float x)
     const uint8_t sign = signbit(x) ? 0x80 : 0x00;
     if (isnan(x)) return sign | 0x7F;
     const double a = fabs((double)x);
-    if (a >= 448.0) return sign | 0x7E;
+    if (a >= 448.0) return sign | (ORC_MUT(6) ? 0x7F : 0x7E);   /* 6: overflow to NaN */
     if (a == 0.0) return sign;
     int E;
     (void)frexp(a, &E);
     int e = E - 1;
     if (e < -6) e = -6;
-    const double q = rint(a / ldexp(1.0, e - 3));   /* default rounding mode: ties to even */
+    const double q = ORC_MUT(7) ? trunc(a / ldexp(1.0, e - 3))    /* 7: round toward zero */
+                                : rint(a / ldexp(1.0, e - 3));    /* default rounding mode: ties to even */
     int code = (e + 6) * 8 + (int)q;
     if (code > 0x7E) code = 0x7E;
     return sign | (uint8_t)code;
@@ -125,11 +135,11 @@ uint8_t orc_int4_encode(float y)
     if (isnan(y)) return 8;
     double r = rint((double)y);
     if (r > 7.0) r = 7.0;
-    if (r < -7.0) r = -7.0;
+    if (r < (ORC_MUT(8) ? -8.0 : -7.0)) r = ORC_MUT(8) ? -8.0 : -7.0;   /* 8: asymmetric clamp */
     return (uint8_t)(r + 8.0);
 }
 
-double orc_int4_decode(uint8_t nibble) { return (double)nibble - 8.0; }
+double orc_int4_decode(uint8_t nibble) { return (double)nibble - (ORC_MUT(9) ? 7.0 : 8.0); }   /* 9: bias 7 */
 
 /* int4 scale for one channel: absmax over positions / 7 in fp32 (1 if 0). */
 void orc_int4_scales(const uint16_t *x, int64_t n_tokens, int32_t H_KV, int32_t d_h, float *scale_out)
@@ -140,7 +150,7 @@ void orc_int4_scales(const uint16_t *x, int64_t n_tokens, int32_t H_KV, int32_t 
             const float v = fabsf((float)orc_bf16_to_double(x[t * H_KV * d_h + hc]));
             if (v > amax) amax = v;
         }
-        scale_out[hc] = (amax > 0.0f) ? amax / 7.0f : 1.0f;
+        scale_out[hc] = (amax > 0.0f) ? amax / (ORC_MUT(10) ? 8.0f : 7.0f) : 1.0f;   /* 10: /8 */
     }
 }
 
@@ -154,7 +164,7 @@ void orc_fp8_scales(const uint16_t *x, int64_t n_tokens, int32_t H_KV, int32_t d
             const float v = fabsf((float)orc_bf16_to_double(x[t * H_KV * d_h + hc]));
             if (v > amax) amax = v;
         }
-        scale_out[hc] = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+        scale_out[hc] = (amax > 0.0f) ? amax / (ORC_MUT(11) ? 240.0f : 448.0f) : 1.0f;   /* 11: E4M3FNUZ max */
     }
 }
 
@@ -192,12 +202,12 @@ int orc_locate(const int32_t *bt_row, int32_t max_blocks, int64_t t, int32_t bs,
                int64_t *phys, int32_t *slot)
 {
     if (t < 0 || bs <= 0) return ORC_ERR_ARG;
-    const int64_t lb = t / bs;
+    const int64_t lb = ORC_MUT(12) ? (t + 1) / bs : t / bs;   /* 12: off by one position */
     if (lb >= max_blocks) return ORC_ERR_RANGE;
     const int32_t p = bt_row[lb];
     if (p < 0 || (int64_t)p >= num_blocks) return ORC_ERR_BAD_BLOCK;
     *phys = p;
-    *slot = (int32_t)(t % bs);
+    *slot = (int32_t)(ORC_MUT(13) ? (bs - 1 - t % bs) : t % bs);   /* 13: slots reversed */
     return ORC_OK;
 }
 
@@ -205,6 +215,9 @@ int orc_locate(const int32_t *bt_row, int32_t max_blocks, int64_t t, int32_t bs,
 uint64_t orc_pool_offset(int64_t num_blocks, int32_t bs, int32_t H_KV, int32_t d_h,
                          int32_t layer, int64_t phys, int32_t kv, int32_t h, int32_t slot, int32_t c)
 {
+    if (ORC_MUT(14))   /* 14: K|V outside the head index ([p][kv][h]) */
+        return (((((uint64_t)layer * (uint64_t)num_blocks + (uint64_t)phys) * 2u + (uint64_t)kv) * (uint64_t)H_KV
+                 + (uint64_t)h) * (uint64_t)bs + (uint64_t)slot) * (uint64_t)d_h + (uint64_t)c;
     return (((((uint64_t)layer * (uint64_t)num_blocks + (uint64_t)phys) * (uint64_t)H_KV + (uint64_t)h) * 2u
              + (uint64_t)kv) * (uint64_t)bs + (uint64_t)slot) * (uint64_t)d_h + (uint64_t)c;
 }
@@ -252,7 +265,7 @@ int orc_write_tokens(uint8_t *img, int64_t num_blocks, int32_t bs, int32_t H_KV,
                             img[off] = orc_e4m3_from_float(xf / sc);
                         } else {
                             const uint8_t nib = orc_int4_encode(xf / sc);
-                            const int shift = (off % 2) ? 4 : 0;
+                            const int shift = ((off % 2) ^ (ORC_MUT(15) ? 1 : 0)) ? 4 : 0;   /* 15: nibbles swapped */
                             img[off / 2] = (uint8_t)((img[off / 2] & ~(0x0F << shift)) | (nib << shift));
                         }
                     }
@@ -319,28 +332,31 @@ static void attend_one(const double *q, const uint8_t *K, const uint8_t *V, int6
         return;
     }
     double m = -INFINITY;
+    if (ORC_MUT(17) && n > 1) --n;   /* 17: the newest position masked out */
     for (int64_t t = 0; t < n; ++t) {
         double dot = 0.0;
         for (int32_t c = 0; c < d_h; ++c) {
             const int64_t idx = (t * H_KV + h) * d_h + c;
             dot += q[c] * stored_value(K, idx, kind, sk ? &sk[h * d_h + c] : NULL);
         }
-        x[t] = scale * dot;
+        x[t] = ORC_MUT(16) ? dot : scale * dot;   /* 16: softmax scale dropped */
         if (x[t] > m) m = x[t];
     }
     double Z = 0.0;
     for (int64_t t = 0; t < n; ++t) {
         x[t] = exp(x[t] - m);          /* x now holds the unnormalised weights */
+        if (ORC_MUT(22)) x[t] = exp(x[t]);   /* 22: exponentiated twice */
         Z += x[t];
     }
     for (int32_t c = 0; c < d_h; ++c) out[c] = 0.0;
     for (int64_t t = 0; t < n; ++t)
         for (int32_t c = 0; c < d_h; ++c) {
             const int64_t idx = (t * H_KV + h) * d_h + c;
-            out[c] += x[t] * stored_value(V, idx, kind, sv ? &sv[h * d_h + c] : NULL);
+            const float *svc = ORC_MUT(18) ? (sk ? &sk[h * d_h + c] : NULL) : (sv ? &sv[h * d_h + c] : NULL);
+            out[c] += x[t] * stored_value(V, idx, kind, svc);   /* 18: values scaled by the key scales */
         }
-    for (int32_t c = 0; c < d_h; ++c) out[c] /= Z;
-    *lse = m + log(Z);
+    for (int32_t c = 0; c < d_h; ++c) out[c] /= ORC_MUT(23) ? (double)n : Z;   /* 23: mean, not softmax */
+    *lse = m + (ORC_MUT(19) ? log2(Z) : log(Z));   /* 19: log base 2 */
 }
 
 /* Decode attention for a batch over logical lists.
@@ -361,7 +377,7 @@ int orc_decode(const uint16_t *q, const uint8_t *K, const uint8_t *V, const int6
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t bh = 0; bh < (int64_t)B * H_Q; ++bh) {
         const int64_t b = bh / H_Q;
-        const int32_t hq = (int32_t)(bh % H_Q), h = hq / g;
+        const int32_t hq = (int32_t)(bh % H_Q), h = ORC_MUT(20) ? hq % H_KV : hq / g;   /* 20: interleaved groups */
         double *x = (double *)malloc(sizeof(double) * (size_t)(n[b] > 0 ? n[b] : 1));
         double qd[1024];
         if (!x || d_h > 1024) {
@@ -392,7 +408,7 @@ int orc_prefill(const uint16_t *q, int64_t n_q, const uint8_t *K, const uint8_t 
     int64_t *n = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n_q > 0 ? n_q : 1));
     if (!cu || !n) { free(cu); free(n); return ORC_ERR_ARG; }
     for (int64_t i = 0; i <= n_q; ++i) cu[i] = 0;        /* every query reads the same list */
-    for (int64_t i = 0; i < n_q; ++i) n[i] = q_start + i + 1;
+    for (int64_t i = 0; i < n_q; ++i) n[i] = q_start + i + (ORC_MUT(21) ? 0 : 1);   /* 21: own key hidden */
     const int st = orc_decode(q, K, V, cu, n, (int32_t)n_q, H_Q, H_KV, d_h, kind, scales, scale, out, lse);
     free(cu);
     free(n);

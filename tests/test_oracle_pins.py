@@ -112,6 +112,28 @@ def test_table_21_1_address_translation():
             assert st == oracle.OK and (phys, slot) == (int(w[4]), int(w[5]))
 
 
+def test_pool_layout_structure():
+    """The pool image's layout (the library's documented format, not the pages'):
+    every element has its own offset and the offsets fill the allocation; the keys
+    then the values of one (layer, block, head) form one contiguous run of
+    2 * bs * d_h elements, slot-major; the heads of a block follow each other; a
+    layer's region is N * H_KV * 2 * bs * d_h elements, so one block id names the same
+    block in every layer ("KV Cache Explained", "Why PagedAttention allocates KV in
+    blocks": 2 MiB per 16-token block across 32 layers for 8 KV heads of width 128
+    in bf16)."""
+    L, N, H, bs, d = 3, 5, 4, 4, 8
+    img = oracle.PoolImage(N, bs, L, H, d, 2)
+    # visiting (layer, block, head, K|V, slot, channel) in that nesting order walks the
+    # allocation element by element: 0, 1, 2, ... -- which is every property above at once
+    offs = [img.offset(l, p, kv, h, slot, c)
+            for l in range(L) for p in range(N) for h in range(H)
+            for kv in range(2) for slot in range(bs) for c in range(d)]
+    assert offs == list(range(L * N * H * 2 * bs * d))
+    llama = oracle.PoolImage(1, 16, 32, 8, 128, 2)
+    per_block_all_layers = 32 * (llama.offset(0, 1, 0, 0, 0, 0) - llama.offset(0, 0, 0, 0, 0, 0)) * 2
+    assert per_block_all_layers == 2 * 2**20
+
+
 def test_table_21_1_appends_through_pool_image():
     """Replay steps 1-2 with distinct token values and check where the bytes land."""
     bs, N, tables, lens, steps = _table_fixture()
