@@ -61,8 +61,9 @@ struct DecodeCfg {
     static constexpr int BOX_ROWS = LINES ? STAGE / 128 : 2 * kBS;
     static constexpr int BOX_X = LINES ? 0 : 128 * 8 / BITS;   // elements per band row
     static constexpr int CHUNKS = ROW_BYTES / 16;             // 16-byte chunks per token row
-    // ring bytes per CTA: 96 KiB (2 CTAs per SM) for bf16; e4m3 takes 48 KiB so that 4 CTAs (16 warps) share an SM
-    static constexpr int RING_BYTES = KIND == KV_E4M3 ? 49152 : 98304;
+    // ring bytes per CTA, sized for CTAs per SM (measured on GB300): bf16 64 KiB (2 stages a warp,
+    // 3 CTAs an SM), e4m3 48 KiB (3 stages, 4 CTAs), int4 4 stages
+    static constexpr int RING_BYTES = KIND == KV_E4M3 ? 49152 : (KIND == KV_BF16 ? 65536 : 98304);
     static constexpr int R0 = RING_BYTES / (kWarps * STAGE);
     static constexpr int R = R0 < 2 ? 2 : (R0 > 4 ? 4 : R0);   // ring depth per warp
     static constexpr int KSTEPS = D / 16;
