@@ -258,8 +258,11 @@ KVC_API kvc_status kvc_mixed_step(kvc_pool *pool, int32_t layer, const void *q, 
                                   float scale, kvc_stream_t stream);
 
 /* Pre-size the decode workspace for up to max_batch sequences of up to
- * max_blocks table entries and num_q_heads query heads, so that later calls
- * allocate nothing.  Errors: KVC_ERR_ARG, KVC_ERR_OOM. */
+ * max_blocks table entries and num_q_heads query heads, so that later
+ * kvc_decode_attn / kvc_decode_step calls allocate nothing (a kvc_mixed_step
+ * also needs counters for its chunk's query tiles: reserve with max_batch plus
+ * the chunk's tiles, n_q / (64 / g) or n_q / (32 / g) rounded up, to cover it).
+ * Errors: KVC_ERR_ARG, KVC_ERR_OOM. */
 KVC_API kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_t num_q_heads, int32_t max_blocks);
 
 /* Decode attention that allocates no device memory.  The pages have no
