@@ -20,26 +20,6 @@ from harness import (GpuCase, OracleCase, check_attention, dev_bits, dev_i32, fi
 pytestmark = pytest.mark.gpu
 
 
-class _env:
-    """Set one environment variable (None: unset it) for a block."""
-
-    def __init__(self, var, val):
-        self.var, self.val = var, val
-
-    def __enter__(self):
-        self.old = os.environ.get(self.var)
-        if self.val is None:
-            os.environ.pop(self.var, None)
-        else:
-            os.environ[self.var] = self.val
-
-    def __exit__(self, *a):
-        if self.old is None:
-            os.environ.pop(self.var, None)
-        else:
-            os.environ[self.var] = self.old
-
-
 def _run(kvc, w, layers=(0,), fill=0xFF, bytes_check=True, decode_layers=None):
     """Load context, append, decode on the GPU and in the oracle; compare."""
     g = GpuCase(kvc, w, fill_byte=fill)
