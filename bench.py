@@ -74,15 +74,21 @@ def prefill_flops(w) -> int:
 
 
 # the sources the decode kernel is compiled from (its ncu counters go stale when one changes)
-KERNEL_SOURCES = ["kvc_decode.cuh", "kvc_prefill.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_decode_bf16.cu",
-                  "kvc_decode_fp8.cu", "kvc_decode_int4.cu", "kvc_attn.cu"]
+# the sources a step's kernel is compiled from (its ncu counters go stale when one changes):
+# the decode step's kernel, and the mixed step's (decode + prefill chunk) kernel
+KERNEL_SOURCES = {
+    "decode": ["kvc_decode.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_attn.cu"],
+    "mixed": ["kvc_decode.cuh", "kvc_prefill.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_attn.cu"],
+}
 
 
-def source_digest() -> str:
-    h = hashlib.sha256()
+def source_digest(kind: str = "decode", read=None) -> str:
+    """sha256 prefix of the kernel family's sources (read(name) -> bytes; default: the tree)."""
     csrc = os.path.join(ROOT, "paged_kv_cache_kvc_gb300", "csrc")
-    for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+    read = read or (lambda f: open(os.path.join(csrc, f), "rb").read())
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        h.update(read(f))
     return h.hexdigest()[:16]
 
 
@@ -99,7 +105,8 @@ def profiled_traffic(workload: str):
         if line.startswith("<!-- ") and ":" in line:
             k, v = line[5:].split("-->")[0].split(":", 1)
             fields[k.strip()] = v.strip()
-    if fields.get("source_sha") != source_digest() or fields.get("workload") != workload:
+    kind = fields.get("kernel_family", "decode")
+    if kind not in KERNEL_SOURCES or fields.get("source_sha") != source_digest(kind) or fields.get("workload") != workload:
         return None
     try:
         return int(float(fields["dram_bytes_per_launch"]))

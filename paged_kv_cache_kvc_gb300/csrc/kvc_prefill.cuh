@@ -22,9 +22,9 @@
 namespace kvc {
 
 constexpr int kPrefillKeys = 64;   // keys per stage: 4 blocks
-constexpr int kPrefillRing = 3;
+constexpr int kPrefillRing = 3;   // stages of the standalone kernel
 
-template <int D>
+template <int D, int RING = kPrefillRing>
 struct PrefillCfg {
     static constexpr int BLK = 2 * kBS * D * 2;                 // one block-head of bf16 keys then values
     static constexpr int BLOCKS = kPrefillKeys / kBS;
@@ -32,17 +32,18 @@ struct PrefillCfg {
     static constexpr int BANDS = D * 2 / 128;
     static constexpr int KSTEPS = D / 16;                       // QK k-steps
     static constexpr int NDIM = D / 8;                          // PV n-tiles
-    static constexpr int SMEM = 1024 /* alignment slack */ + kPrefillRing * STAGE + kPrefillRing * 8 + 64;   // + masks, counts
+    static constexpr int SMEM = 1024 /* alignment slack */ + RING * STAGE + RING * 8 + 64;   // + masks, counts
 };
 
 // CTA (tile, h) of a prefill chunk: p.len_base = q_start, p.n_pos = n_q,
 // p.ppu = 64 / g positions per tile, p.bt = the row's table, p.max_blocks >=
 // the blocks holding positions < q_start + n_q.
-template <int D>
+template <int D, int RING = kPrefillRing>
 __device__ __forceinline__ void prefill_cta(const CUtensorMap &tmap, const DecodeParams &p, const int tile,
                                             const int h)
 {
-    using C = PrefillCfg<D>;
+    using C = PrefillCfg<D, RING>;
+    constexpr int kPrefillRing = RING;   // this instance's stages
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kPrefillRing * C::STAGE);
@@ -306,6 +307,10 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
     prefill_cta<D>(tmap, p, blockIdx.z, blockIdx.y);
 }
 
+// In the mixed launch the query tiles keep 2 stages, and the kernel is held to 3
+// CTAs per SM (the bf16 decode CTAs' occupancy).
+constexpr int kMixedPrefillRing = 2;
+
 // A decode step and a prefill chunk in one launch ("KV cache: Generation
 // state, latency, and allocation" 21.3: chunked prefill beside decode):
 // grid (split, KV head, decode units + prefill tiles).  The prefill tiles,
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
 // (bf16 pools, groups of at most 4 query heads); otherwise the split kernel's
 // causal tiles.
 template <int D, int NT, int KIND, bool PSPLIT, bool FASTPRE>
-__global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__ CUtensorMap tmap,
+__global__ void __launch_bounds__(kThreads, FASTPRE ? 3 : 1) mixed_kernel(const __grid_constant__ CUtensorMap tmap,
                                                          const DecodeParams pd, const DecodeParams pp)
 {
     const int z = blockIdx.z;
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__
     const int upto = static_cast<int>((static_cast<int64_t>(z + 1) * P) / Z);
     if (upto > before) {
         if constexpr (FASTPRE) {
-            if (blockIdx.x == 0) prefill_cta<D>(tmap, pp, before, blockIdx.y);
+            if (blockIdx.x == 0) prefill_cta<D, kMixedPrefillRing>(tmap, pp, before, blockIdx.y);
         } else if (static_cast<int>(blockIdx.x) < pp.max_splits) {
             decode_cta<D, 4, KIND, false, true>(tmap, pp, blockIdx.x, blockIdx.y, before);
         }
@@ -359,7 +364,7 @@ template <int D, int NT, int KIND, bool PSPLIT, bool FASTPRE>
 DecodeKernel mixed_instance()
 {
     constexpr int smem = cmax(cmax(decode_smem_bytes<D, NT, KIND>(), decode_smem_bytes<D, 4, KIND>()),
-                              FASTPRE ? PrefillCfg<D>::SMEM : 0);
+                              FASTPRE ? PrefillCfg<D, kMixedPrefillRing>::SMEM : 0);
     static DecodeKernel k = configured_kernel<&mixed_fn<D, NT, KIND, PSPLIT, FASTPRE>, smem>();
     return k;
 }
