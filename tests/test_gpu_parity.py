@@ -168,6 +168,53 @@ def test_mixed_step_equals_step_then_prefill(kvc, case):
     check_attention(res[1][3], res[1][4], ro, rl, w.dtype, f"mixed prefill {case}")
 
 
+def test_mixed_step_edges(kvc):
+    """kvc_mixed_step with no chunk queries is kvc_decode_step, with no decode
+    sequences is kvc_prefill_attn (bit-identical outputs); a chunk running past its
+    row or a misaligned q is refused before any launch."""
+    w = synth.make_workload("ragged_prefix", seed=3, B=3, shared=32, chunk=21, lo=16, hi=300)
+    p = w.prefill
+    ld = layer_data(w, 0)
+    kc = w.ctx_tokens(0, 0, p.seq, p.q_start, p.total)
+    vc = w.ctx_tokens(0, 1, p.seq, p.q_start, p.total)
+    qc = dev_bits(w.prefill_q(0))
+    g = GpuCase(kvc, w)
+    try:
+        g.load_context(0, ld)
+        row = dev_i32(w.block_tables[p.seq])
+        kvc.kvc_write_tokens(g.pool, 0, row[None], dev_i32([p.q_start]), dev_i32([0, p.n_q]), dev_bits(kc), dev_bits(vc))
+        q, k, v = g.step_inputs(ld)
+        outs = [torch.empty((w.B, w.H_Q, w.d_h), device="cuda") for _ in range(2)]
+        lses = [torch.empty((w.B, w.H_Q), device="cuda") for _ in range(2)]
+        o2 = [torch.empty((p.n_q, w.H_Q, w.d_h), device="cuda") for _ in range(2)]
+        l2 = [torch.empty((p.n_q, w.H_Q), device="cuda") for _ in range(2)]
+        # no chunk queries: the decode step alone (same append position, so the pool is unchanged)
+        kvc.kvc_decode_step(g.pool, 0, q, g.bt_dec, g.lens_pre, k, v, outs[0], lses[0], scale=w.scale)
+        kvc.kvc_mixed_step(g.pool, 0, q, g.bt_dec, g.lens_pre, k, v, outs[1], lses[1], qc[:0], row, p.q_start,
+                           o2[1][:0], l2[1][:0], scale=w.scale)
+        # no decode sequences: the chunk alone
+        kvc.kvc_prefill_attn(g.pool, 0, qc, row, p.q_start, o2[0], l2[0], scale=w.scale)
+        kvc.kvc_mixed_step(g.pool, 0, q[:0], g.bt_dec[:0], g.lens_pre[:0], k[:0], v[:0], outs[1][:0], lses[1][:0],
+                           qc, row, p.q_start, o2[1], l2[1], scale=w.scale)
+        torch.cuda.synchronize()
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+        assert torch.equal(outs[0], outs[1]) and torch.equal(lses[0], lses[1])
+        assert torch.equal(o2[0], o2[1]) and torch.equal(l2[0], l2[1])
+        with pytest.raises(kvc.KvcError) as e:    # the chunk's last query would sit past the row's table
+            kvc.kvc_mixed_step(g.pool, 0, q, g.bt_dec, g.lens_pre, k, v, outs[1], lses[1], qc, row,
+                               w.max_blocks * 16 - p.n_q + 1, o2[1], l2[1], scale=w.scale)
+        assert e.value.status == kvc.KVC_ERR_RANGE
+        qbad = torch.empty(q.numel() * 2 + 8, dtype=torch.bfloat16, device="cuda")[1:1 + q.numel()].view(q.shape)
+        with pytest.raises(kvc.KvcError) as e:    # q not 16-byte aligned
+            kvc.kvc_mixed_step(g.pool, 0, qbad, g.bt_dec, g.lens_pre, k, v, outs[1], lses[1], qc, row, p.q_start,
+                               o2[1], l2[1], scale=w.scale)
+        assert e.value.status == kvc.KVC_ERR_ARG
+        torch.cuda.synchronize()
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+    finally:
+        g.close()
+
+
 def test_prefix_sharing_equals_private_copies(kvc):
     """The shared-block run equals a run where every row holds a private copy
     of the prefix blocks: bit-identical outputs (same arithmetic order)."""
