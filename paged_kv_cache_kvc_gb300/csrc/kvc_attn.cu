@@ -11,10 +11,33 @@ namespace kvc {
 //   M = max_s m_s,  L = sum_s 2^(m_s - M) l_s,  out = sum_s 2^(m_s - M) o_s / L,
 //   lse = (M + log2 L) ln 2.
 // Sequences with a single split were finished by the attention kernel.
-// grid (H_Q, query positions): one CTA per output row.
+// grid (H_Q, query positions): one CTA per output row.  The CTA reduces M and L
+// over the splits in parallel and keeps the weights 2^(m_s - M) in shared memory
+// (up to kMergeWeights splits; past that they are recomputed); the row's D/4
+// float4 columns x (128 / (D/4)) split groups sum the partials, then the groups
+// are added.  D is 64 or 128.
+constexpr int kMergeWeights = 1024;
+
+__device__ __forceinline__ float block_reduce_128(float v, bool is_max, float *red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float t = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        v = is_max ? fmaxf(v, t) : v + t;
+    }
+    __syncthreads();   // red is free
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    return is_max ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) : (red[0] + red[1]) + (red[2] + red[3]);
+}
+
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int D)
 {
-    const int hq = blockIdx.x, pos = blockIdx.y;
+    __shared__ float red[4];
+    __shared__ float wsh[kMergeWeights];
+    __shared__ float4 part[128];
+    const int hq = blockIdx.x, pos = blockIdx.y, tid = threadIdx.x;
     int len = seq_len(p, pos / p.ppu);
     if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) len = 0;
     const int nblk = (len + kBS - 1) / kBS;
@@ -23,17 +46,45 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int D)
     const size_t bq = static_cast<size_t>(pos) * p.H_Q + hq;
     const float2 *ml = p.part_ml + bq * p.max_splits;
     const float *po = p.part_o + bq * p.max_splits * D;
-    float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s].x);
-    float L = 0.f;
-    for (int s = 0; s < ns; ++s) L += fast_exp2(ml[s].x - M) * ml[s].y;
-    const float inv = 1.f / L;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float o = 0.f;
-        for (int s = 0; s < ns; ++s) o += fast_exp2(ml[s].x - M) * po[static_cast<size_t>(s) * D + d];
-        p.out[bq * D + d] = o * inv;
+
+    float m = -INFINITY;
+    for (int s = tid; s < ns; s += 128) m = fmaxf(m, ml[s].x);
+    const float M = block_reduce_128(m, true, red);
+    const float Mref = M == -INFINITY ? 0.f : M;   // no visible position at all (device-detected errors)
+    float l = 0.f;
+    for (int s = tid; s < ns; s += 128) {
+        const float2 v = ml[s];
+        const float e = fast_exp2(v.x - Mref);
+        l += e * v.y;
+        if (s < kMergeWeights) wsh[s] = e;
     }
-    if (threadIdx.x == 0 && p.lse) p.lse[bq] = (M + log2f(L)) * kLn2;
+    const float L = block_reduce_128(l, false, red);   // its barriers also publish wsh
+
+    const int nd4 = D / 4, groups = 128 / nd4, d4 = tid % nd4, grp = tid / nd4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = grp; s < ns; s += groups) {
+        const float e = s < kMergeWeights ? wsh[s] : fast_exp2(ml[s].x - Mref);
+        const float4 o = __ldg(reinterpret_cast<const float4 *>(po + static_cast<size_t>(s) * D) + d4);
+        acc.x += e * o.x;
+        acc.y += e * o.y;
+        acc.z += e * o.z;
+        acc.w += e * o.w;
+    }
+    part[tid] = acc;
+    __syncthreads();
+    if (grp == 0) {
+        for (int g2 = 1; g2 < groups; ++g2) {
+            const float4 o = part[g2 * nd4 + d4];
+            acc.x += o.x;
+            acc.y += o.y;
+            acc.z += o.z;
+            acc.w += o.w;
+        }
+        const float inv = 1.f / L;
+        reinterpret_cast<float4 *>(p.out + bq * D)[d4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    if (tid == 0 && p.lse) p.lse[bq] = (M + log2f(L)) * kLn2;
 }
 
 // Blocks per split.  Sequences are independent and every CTA reads only its
@@ -194,13 +245,13 @@ static kvc_status run_mixed(kvc_pool *pool, DecodeParams &pd, DecodeParams &pp, 
     const size_t nd = pd.max_splits > 1 ? static_cast<size_t>(pd.n_pos) * pd.H_Q * pd.max_splits : 0;
     const size_t np = pp.max_splits > 1 ? static_cast<size_t>(pp.n_pos) * pp.H_Q * pp.max_splits : 0;
     const size_t row = static_cast<size_t>(pool->D) * sizeof(float) + sizeof(float2);
-    kvc_status st = ensure_workspace(pool, ud + up, (nd + np) * row);
+    kvc_status st = ensure_workspace(pool, ud + up, (nd + np) * row + 256);
     if (st != KVC_OK) return st;
     float *data = ws_data(pool);
     pd.part_o = nd ? data : nullptr;
     pd.part_ml = nd ? reinterpret_cast<float2 *>(data + nd * pool->D) : nullptr;
     pd.counters = (nd && pd.ppu * pd.g * pd.max_splits <= merge_rows_limit()) ? ws_counters(pool) : nullptr;
-    float *data_p = data + nd * pool->D + nd * 2;
+    float *data_p = data + ((nd * pool->D + nd * 2 + 63) & ~static_cast<size_t>(63));   // 256-byte aligned
     pp.part_o = np ? data_p : nullptr;
     pp.part_ml = np ? reinterpret_cast<float2 *>(data_p + np * pool->D) : nullptr;
     pp.counters = (np && pp.ppu * pp.g * pp.max_splits <= merge_rows_limit()) ? ws_counters(pool) + ud : nullptr;
