@@ -11,12 +11,20 @@ namespace kvc {
 //   M = max_s m_s,  L = sum_s 2^(m_s - M) l_s,  out = sum_s 2^(m_s - M) o_s / L,
 //   lse = (M + log2 L) ln 2.
 // Sequences with a single split were finished by the attention kernel.
-// grid (H_Q, query positions): one CTA per output row.  The CTA reduces M and L
-// over the splits in parallel and keeps the weights 2^(m_s - M) in shared memory
-// (up to kMergeWeights splits; past that they are recomputed); the row's D/4
-// float4 columns x (128 / (D/4)) split groups sum the partials, then the groups
-// are added.  D is 64 or 128.
+// grid (H_Q, query positions): one CTA per output row.  The merge is a few
+// kilobytes per row, so its time is memory latency: every thread issues its
+// loads of (m, l) and of up to kMergePre partial rows at once, before the
+// sequence's length (and so its split count) is known -- every slot below
+// max_splits lies inside the partials buffer, and slots past the split count are
+// masked out by selection.  The CTA then reduces M and L over the splits, keeps
+// the weights 2^(m_s - M) in shared memory (up to kMergeWeights splits; past that
+// they are recomputed), and its D/4 float4 columns x (128 / (D/4)) split groups
+// sum the partials before the groups are added.
+// It is launched as a programmatic dependent of the attention kernel, so its
+// CTAs are scheduled while that kernel drains; griddepcontrol.wait holds them
+// until the attention kernel has finished and its partials are visible.
 constexpr int kMergeWeights = 1024;
+constexpr int kMergePre = 12;   // partial rows a thread loads up front
 
 __device__ __forceinline__ float block_reduce_128(float v, bool is_max, float *red)
 {
@@ -32,27 +40,56 @@ __device__ __forceinline__ float block_reduce_128(float v, bool is_max, float *r
     return is_max ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) : (red[0] + red[1]) + (red[2] + red[3]);
 }
 
-__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int D)
+__device__ __forceinline__ float4 fma4(float e, const float4 &o, float4 acc)
 {
+    acc.x = fmaf(e, o.x, acc.x);
+    acc.y = fmaf(e, o.y, acc.y);
+    acc.z = fmaf(e, o.z, acc.z);
+    acc.w = fmaf(e, o.w, acc.w);
+    return acc;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p)
+{
+    constexpr int ND4 = D / 4, G = 128 / ND4;
+    static_assert(ND4 <= 128 && 128 % ND4 == 0, "D/4 float4 columns must divide the CTA");
     __shared__ float red[4];
     __shared__ float wsh[kMergeWeights];
     __shared__ float4 part[128];
     const int hq = blockIdx.x, pos = blockIdx.y, tid = threadIdx.x;
-    int len = seq_len(p, pos / p.ppu);
+    const int d4 = tid % ND4, grp = tid / ND4;
+    int len = seq_len(p, pos / p.ppu);   // a caller input: read before the wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    const int S = p.max_splits;
+    const size_t bq = static_cast<size_t>(pos) * p.H_Q + hq;
+    const float2 *ml = p.part_ml + bq * S;
+    const float4 *po = reinterpret_cast<const float4 *>(p.part_o + bq * S * D) + d4;
+    const float2 mv = tid < S ? ml[tid] : make_float2(0.f, 0.f);
+    float4 o[kMergePre];
+#pragma unroll
+    for (int i = 0; i < kMergePre; ++i) {
+        const int s = grp + G * i;
+        o[i] = s < S ? po[static_cast<size_t>(s) * ND4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
     if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) len = 0;
     const int nblk = (len + kBS - 1) / kBS;
-    const int ns = (nblk + p.chunk - 1) / p.chunk;
-    if (ns <= 1) return;
-    const size_t bq = static_cast<size_t>(pos) * p.H_Q + hq;
-    const float2 *ml = p.part_ml + bq * p.max_splits;
-    const float *po = p.part_o + bq * p.max_splits * D;
+    const int ns = min((nblk + p.chunk - 1) / p.chunk, S);
+    if (ns <= 1) return;   // uniform over the CTA
 
-    float m = -INFINITY;
-    for (int s = tid; s < ns; s += 128) m = fmaxf(m, ml[s].x);
+    float m = tid < ns ? mv.x : -INFINITY;
+    for (int s = tid + 128; s < ns; s += 128) m = fmaxf(m, ml[s].x);
     const float M = block_reduce_128(m, true, red);
     const float Mref = M == -INFINITY ? 0.f : M;   // no visible position at all (device-detected errors)
     float l = 0.f;
-    for (int s = tid; s < ns; s += 128) {
+    if (tid < ns) {
+        const float e = fast_exp2(mv.x - Mref);
+        l = e * mv.y;
+        wsh[tid] = e;
+    }
+    for (int s = tid + 128; s < ns; s += 128) {
         const float2 v = ml[s];
         const float e = fast_exp2(v.x - Mref);
         l += e * v.y;
@@ -60,26 +97,26 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int D)
     }
     const float L = block_reduce_128(l, false, red);   // its barriers also publish wsh
 
-    const int nd4 = D / 4, groups = 128 / nd4, d4 = tid % nd4, grp = tid / nd4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s = grp; s < ns; s += groups) {
+#pragma unroll
+    for (int i = 0; i < kMergePre; ++i) {
+        const int s = grp + G * i;
+        if (s < ns) acc = fma4(wsh[s], o[i], acc);
+    }
+    for (int s = grp + G * kMergePre; s < ns; s += G) {
         const float e = s < kMergeWeights ? wsh[s] : fast_exp2(ml[s].x - Mref);
-        const float4 o = __ldg(reinterpret_cast<const float4 *>(po + static_cast<size_t>(s) * D) + d4);
-        acc.x += e * o.x;
-        acc.y += e * o.y;
-        acc.z += e * o.z;
-        acc.w += e * o.w;
+        acc = fma4(e, po[static_cast<size_t>(s) * ND4], acc);
     }
     part[tid] = acc;
     __syncthreads();
     if (grp == 0) {
-        for (int g2 = 1; g2 < groups; ++g2) {
-            const float4 o = part[g2 * nd4 + d4];
-            acc.x += o.x;
-            acc.y += o.y;
-            acc.z += o.z;
-            acc.w += o.w;
+#pragma unroll
+        for (int g2 = 1; g2 < G; ++g2) {
+            const float4 v = part[g2 * ND4 + d4];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
         }
         const float inv = 1.f / L;
         reinterpret_cast<float4 *>(p.out + bq * D)[d4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -195,12 +232,7 @@ kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel
     cudaError_t e = cudaLaunchKernel(k.fn, grid, dim3(kThreads), args, k.smem, stream);
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    if (p.max_splits > 1 && !p.counters) {
-        merge_kernel<<<dim3(p.H_Q, p.n_pos), 128, 0, stream>>>(p, pool->D);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_status(e);
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-    }
+    if (p.max_splits > 1 && !p.counters) return launch_split_merge(p, pool->D, stream);
     return KVC_OK;
 }
 
@@ -460,10 +492,23 @@ extern "C" kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_
 namespace kvc {
 
 // Launch the split merge on its own (partials already written by the decode kernel).
+// merge_kernel as a programmatic dependent of the kernel before it on the stream
 kvc_status launch_split_merge(const DecodeParams &p, int D, cudaStream_t stream)
 {
-    merge_kernel<<<dim3(p.H_Q, p.n_pos), 128, 0, stream>>>(p, D);
-    const cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.H_Q, p.n_pos);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (D == 64) e = cudaLaunchKernelEx(&cfg, merge_kernel<64>, p);
+    else if (D == 128) e = cudaLaunchKernelEx(&cfg, merge_kernel<128>, p);
+    else return KVC_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return KVC_OK;

@@ -668,11 +668,17 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &tmap, const Decode
     if (threadIdx.x == 0) p.counters[static_cast<size_t>(b) * p.H_KV + h] = 0u;   // ready for the next launch
 }
 
+// Lets a programmatic dependent (the split merge) be scheduled once every CTA
+// of this grid has started; the dependent waits for this grid's completion
+// before it reads anything the grid wrote.
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // grid (split, KV head, unit)
 template <int D, int NT, int KIND, bool PSPLIT, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmap,
                                                           const DecodeParams p)
 {
+    allow_dependent_launch();
     decode_cta<D, NT, KIND, PSPLIT, CAUSAL>(tmap, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 

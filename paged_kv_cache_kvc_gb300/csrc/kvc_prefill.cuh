@@ -323,6 +323,7 @@ template <int D, int NT, int KIND, bool PSPLIT, bool FASTPRE>
 __global__ void __launch_bounds__(kThreads, FASTPRE ? 3 : 1) mixed_kernel(const __grid_constant__ CUtensorMap tmap,
                                                          const DecodeParams pd, const DecodeParams pp)
 {
+    allow_dependent_launch();
     const int z = blockIdx.z;
     const int64_t Z = gridDim.z, P = pp.B;
     const int before = static_cast<int>((static_cast<int64_t>(z) * P) / Z);
