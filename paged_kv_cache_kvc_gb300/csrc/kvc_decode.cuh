@@ -43,6 +43,7 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kBS = 16;                 // positions per block = mma M tile
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleSlack = 8.f;   // log2 units: stale reference maxima keep weights <= 256
 
 // stored element kinds of a pool
 constexpr int KV_BF16 = 0, KV_E4M3 = 1, KV_INT4 = 2;
@@ -269,8 +270,16 @@ __device__ __forceinline__ void block_update(uint32_t st, const uint32_t (&qf)[N
 #pragma unroll
         for (int c = 0; c < 4; ++c) sc[0][c] += sc2[0][c];
 
-    // ---- online softmax (log2 domain); column = query head, rows = tokens gq, gq+8
+    // ---- online softmax (log2 domain); column = query head, rows = tokens gq, gq+8.
+    // Decode instances move a column's reference max m_run only when a block's max
+    // exceeds it by more than kRescaleSlack (log2 units): below that the weights
+    // 2^(s - m_run) stay under 2^kRescaleSlack, l and O keep the same reference, and
+    // the output accumulators need no rescale -- the warp skips it unless one of its
+    // columns moved (conditional rescaling, as in FlashAttention-4).  The merge and
+    // lse use each partial's own reference, so the result is the same softmax.
     uint32_t pb[NT][2], pl[NT][2];
+    float alpha[NT][2];
+    bool moved = false;
     #pragma unroll
     for (int jn = 0; jn < NT; ++jn) {
 #pragma unroll
@@ -288,19 +297,24 @@ __device__ __forceinline__ void block_update(uint32_t st, const uint32_t (&qf)[N
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
-            const float mn = fmaxf(m_run[jn][c], bm);   // without CAUSAL finite: a block has a valid token
-            const float mref = (CAUSAL && mn == -INFINITY) ? 0.f : mn;   // a column with nothing visible yet
-            const float alpha = fast_exp2(m_run[jn][c] - mref);
+            float mref;
+            if constexpr (CAUSAL) {
+                const float mn = fmaxf(m_run[jn][c], bm);
+                mref = mn == -INFINITY ? 0.f : mn;   // a column with nothing visible yet
+                alpha[jn][c] = fast_exp2(m_run[jn][c] - mref);
+                m_run[jn][c] = mn;
+                moved = true;
+            } else {   // bm is finite: a block has a valid token (the first block always moves)
+                const bool up = bm > m_run[jn][c] + kRescaleSlack;
+                mref = up ? bm : m_run[jn][c];
+                alpha[jn][c] = up ? fast_exp2(m_run[jn][c] - bm) : 1.f;
+                m_run[jn][c] = mref;
+                moved |= up;
+            }
             const float p0 = fast_exp2(sc[jn][c] - mref), p1 = fast_exp2(sc[jn][c + 2] - mref);
-            m_run[jn][c] = mn;
-            l_run[jn][c] = l_run[jn][c] * alpha + p0 + p1;
+            l_run[jn][c] = l_run[jn][c] * alpha[jn][c] + p0 + p1;
             sc[jn][c] = p0;
             sc[jn][c + 2] = p1;
-#pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                oacc[mt][jn][c] *= alpha;
-                oacc[mt][jn][c + 2] *= alpha;
-            }
         }
         if constexpr (!QUANT) {
             const uint32_t h0 = pack_bf16(sc[jn][0], sc[jn][1]), h1 = pack_bf16(sc[jn][2], sc[jn][3]);
@@ -314,6 +328,17 @@ __device__ __forceinline__ void block_update(uint32_t st, const uint32_t (&qf)[N
             pb[jn][0] = movmatrix_trans(pack_f16(sc[jn][0], sc[jn][1]));
             pb[jn][1] = movmatrix_trans(pack_f16(sc[jn][2], sc[jn][3]));
         }
+    }
+    if (CAUSAL || __any_sync(kFull, moved)) {
+#pragma unroll
+        for (int jn = 0; jn < NT; ++jn)
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    oacc[mt][jn][c] *= alpha[jn][c];
+                    oacc[mt][jn][c + 2] *= alpha[jn][c];
+                }
     }
 
     // ---- O^T += V^T P^T
