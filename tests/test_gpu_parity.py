@@ -282,6 +282,53 @@ def test_group_sizes(kvc, H_KV, dtype):
     _run(kvc, _custom(B=len(lens), H_Q=32, H_KV=H_KV, d_h=128, lens=lens, dtype=dtype, seed=H_KV))
 
 
+def _f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)   # round to nearest even (finite x)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "int4"])
+@pytest.mark.parametrize("H_KV", [8, 1])
+def test_rising_and_falling_scores(kvc, dtype, H_KV):
+    """Scores that climb along a sequence by about 2 (log2 units) per block, so a
+    running maximum is overtaken within the rescale slack for several blocks and
+    then past it; one sequence whose scores fall (its maximum stays in the first
+    block); one random sequence.  Every query leans on one direction u (q = n + 1,
+    k_t = n_t + a(t)), so q.k_t grows with a(t) for every head."""
+    lens = [700, 1500, 333, 2048]
+    w = _custom(B=len(lens), H_Q=32, H_KV=H_KV, d_h=128, lens=lens, dtype=dtype, seed=11 + H_KV)
+    ld = layer_data(w, 0)
+    slope = 0.12 / 16    # a(t) per position: ~2 log2 units of score per 16-position block
+    ramp = {0: slope, 1: slope, 2: -slope, 3: 0.0}
+    k = synth.bf16_bits_to_f32(ld.k_ctx).astype(np.float32)
+    for i in range(len(ld.rows)):
+        b, t0, n = int(ld.rows[i]), int(ld.start[i]), int(ld.cu[i + 1] - ld.cu[i])
+        t = np.arange(t0, t0 + n, dtype=np.float32)
+        a = ramp[b] * (t if ramp[b] >= 0 else t - t0 - n)
+        k[ld.cu[i]:ld.cu[i + 1]] += a[:, None, None]
+    ld.k_ctx = _f32_to_bf16_bits(k)
+    kn = synth.bf16_bits_to_f32(ld.k_new).astype(np.float32)
+    kn += np.array([ramp[b] * lens[b] if ramp[b] >= 0 else 0.0 for b in range(w.B)], np.float32)[:, None, None]
+    ld.k_new = _f32_to_bf16_bits(kn)
+    ld.q = _f32_to_bf16_bits(synth.bf16_bits_to_f32(ld.q).astype(np.float32) + 1.0)
+    for chunk in (None, "8", "40"):
+        if chunk:
+            os.environ["KVC_SPLIT_CHUNK"] = chunk
+        g = GpuCase(kvc, w, fill_byte=0xFF)
+        try:
+            g.load_context(0, ld)
+            out, lse = g.step(0, ld)
+            torch.cuda.synchronize()
+            assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+        finally:
+            g.close()
+            os.environ.pop("KVC_SPLIT_CHUNK", None)
+        ref = OracleCase(w, fill_byte=0xFF).run_layer(ld, image=False)
+        check_attention(out, lse, ref["out"], ref["lse"], w.dtype, f"rising scores {dtype} H_KV={H_KV} chunk={chunk}")
+        # the scores really climb: the newest position's lse is tens of log2 units above a random one's
+        assert float(ref["lse"][0].min()) > float(ref["lse"][3].max()) + 20
+
+
 def test_split_counts_agree(kvc):
     """Changing the split size changes only rounding: all within tolerance of the oracle."""
     w = _custom(B=3, H_Q=16, H_KV=4, d_h=128, lens=[2000, 4097, 777])
