@@ -73,7 +73,6 @@ def prefill_flops(w) -> int:
     return 4 * w.d_h * w.H_Q * visible
 
 
-# the sources the decode kernel is compiled from (its ncu counters go stale when one changes)
 # the sources a step's kernel is compiled from (its ncu counters go stale when one changes):
 # the decode step's kernel, and the mixed step's (decode + prefill chunk) kernel
 KERNEL_SOURCES = {
