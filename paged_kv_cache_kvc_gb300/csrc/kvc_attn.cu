@@ -162,7 +162,7 @@ void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_
 static int merge_rows_limit()
 {
     const char *e = std::getenv("KVC_MERGE_ROWS");
-    return e ? std::atoi(e) : 64;
+    return e ? std::min(std::atoi(e), kMergeRowsMax) : 64;
 }
 
 // The workspace holds the arrival counters at its front, at a fixed place

@@ -72,6 +72,10 @@ struct DecodeCfg {
     static_assert(LINES ? (ROW_BYTES == 64) : (ROW_BYTES % 128 == 0), "rows: 64 bytes or whole 128-byte bands");
 };
 
+// In-kernel split merges hold rows x splits weights plus rows inverse sums in the
+// CTA's shared memory, so the host enables them only up to this many partial rows.
+constexpr int kMergeRowsMax = 4096;
+
 template <int D, int NT, int KIND>
 __host__ __device__ constexpr int decode_smem_bytes()
 {
@@ -79,6 +83,7 @@ __host__ __device__ constexpr int decode_smem_bytes()
     constexpr int stages = kWarps * C::R * C::STAGE;
     constexpr int combine = (kWarps * NT * 8 * 2 + kWarps * NT * 8 * D) * 4;
     constexpr int region = stages > combine ? stages : combine;
+    static_assert(region >= (kMergeRowsMax + 32) * 4, "room for the in-kernel merge's weights");
     return 1024 /* alignment slack */ + region + kWarps * C::R * 8 /* mbarriers */;
 }
 
@@ -672,23 +677,62 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &tmap, const Decode
     __syncthreads();
     if (!last_flag) return;
     __threadfence();
-    for (int i = threadIdx.x; i < rows * D; i += kThreads) {
-        const int qi = i / D, d = i - qi * D;
-        if (!col_real(qi)) continue;
+    // The merge sits at the end of the launch, so it is written for latency: one
+    // warp per query column reduces (m, l) over the splits with its lanes and
+    // leaves the weights 2^(m_s - M) and 1/L in shared memory (free again: every
+    // thread is past the combine); then each thread issues the loads of all of
+    // its float4 column's partials at once.  rows * ns <= kMergeRowsMax (host).
+    float *wsm = reinterpret_cast<float *>(smem);   // [rows][ns] weights, then [rows] 1/L
+    float *linv = wsm + rows * ns;
+    for (int qi = warp; qi < rows; qi += kWarps) {
+        if (!col_real(qi)) continue;   // warp-uniform
         const size_t bq = col_orow(qi);
         const float2 *ml = p.part_ml + bq * p.max_splits;
-        const float *po = p.part_o + bq * p.max_splits * D + d;
-        float M = -INFINITY;
-        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, __ldcg(&ml[sp].x));
-        float L = 0.f, O = 0.f;
-        for (int sp = 0; sp < ns; ++sp) {
-            const float2 v = __ldcg(ml + sp);
-            const float e = fast_exp2(v.x - M);
-            L += e * v.y;
-            O += e * __ldcg(po + static_cast<size_t>(sp) * D);
+        const float2 v0 = lane < ns ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
+        float m = v0.x;
+        for (int sp = lane + 32; sp < ns; sp += 32) m = fmaxf(m, __ldcg(&ml[sp].x));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        const float Mref = m == -INFINITY ? 0.f : m;
+        float l = 0.f;
+        if (lane < ns) {
+            const float e = fast_exp2(v0.x - Mref);
+            wsm[qi * ns + lane] = e;
+            l = e * v0.y;
         }
-        p.out[bq * D + d] = O / L;
-        if (d == 0 && p.lse) p.lse[bq] = (M + log2f(L)) * kLn2;
+        for (int sp = lane + 32; sp < ns; sp += 32) {
+            const float2 v = __ldcg(ml + sp);
+            const float e = fast_exp2(v.x - Mref);
+            wsm[qi * ns + sp] = e;
+            l += e * v.y;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
+        if (lane == 0) {
+            linv[qi] = 1.f / l;
+            if (p.lse) p.lse[bq] = (m + log2f(l)) * kLn2;
+        }
+    }
+    __syncthreads();
+    constexpr int D4 = D / 4;
+    for (int i = threadIdx.x; i < rows * D4; i += kThreads) {
+        const int qi = i / D4, d4 = i - qi * D4;
+        if (!col_real(qi)) continue;
+        const size_t bq = col_orow(qi);
+        const float4 *po = reinterpret_cast<const float4 *>(p.part_o + bq * p.max_splits * D) + d4;
+        const float *w = wsm + qi * ns;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int sp = 0; sp < ns; ++sp) {
+            const float4 o = __ldcg(po + static_cast<size_t>(sp) * D4);
+            const float e = w[sp];
+            acc.x = fmaf(e, o.x, acc.x);
+            acc.y = fmaf(e, o.y, acc.y);
+            acc.z = fmaf(e, o.z, acc.z);
+            acc.w = fmaf(e, o.w, acc.w);
+        }
+        const float inv = linv[qi];
+        reinterpret_cast<float4 *>(p.out + bq * D)[d4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
     if (threadIdx.x == 0) p.counters[static_cast<size_t>(b) * p.H_KV + h] = 0u;   // ready for the next launch
 }
