@@ -188,8 +188,12 @@ KVC_API kvc_status kvc_write_tokens(kvc_pool *pool, int32_t layer, const int32_t
  *   x_t = scale * <q[b][hq], K[b][t][h]>,  t < n
  *   out[b][hq] = sum_t softmax(x)_t V[b][t][h],   lse[b][hq] = ln sum_t exp(x_t)
  * computed in fp32 on tensor cores (bf16 or f16 operands, fp32 accumulation)
- * with a split-K online softmax and a log-sum-exp merge.  For e4m3 pools the
- * key scales are folded into q and the value scales into the output.
+ * with a split-K online softmax and a log-sum-exp merge.  The last split CTA
+ * of a (sequence, KV head) merges its partials in the same launch; when they
+ * exceed 64 partial rows (query heads x splits, e.g. 32-head groups; the
+ * KVC_MERGE_ROWS environment variable moves this limit, up to 4096) a second
+ * launch on the same stream merges them.  For e4m3 and int4 pools the key
+ * scales are folded into q and the value scales into the output.
  *   q:        device bf16 [B][H_Q][d_h], 4-byte aligned
  *   seq_lens: device int32 [B], positions attended (after the append);
  *             n = 0 gives out = 0 and lse = -inf
@@ -205,8 +209,8 @@ KVC_API kvc_status kvc_decode_attn(kvc_pool *pool, int32_t layer, const void *q,
                            const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, int32_t B,
                            float *out, float *lse, float scale, kvc_stream_t stream);
 
-/* One decode step at one layer in a single launch: kvc_append followed by
- * kvc_decode_attn ("KV cache: Generation state, latency, and allocation"
+/* One decode step at one layer in a single attention launch: kvc_append
+ * followed by kvc_decode_attn ("KV cache: Generation state, latency, and allocation"
  * Eq. 21.6 and 21.1: the pass appends its token's key and value, and the new
  * query reads every cached key plus its own).  seq_lens holds the counts
  * BEFORE the append; sequence b's k_new/v_new rows are stored at position
