@@ -329,6 +329,27 @@ def test_rising_and_falling_scores(kvc, dtype, H_KV):
         assert float(ref["lse"][0].min()) > float(ref["lse"][3].max()) + 20
 
 
+@pytest.mark.parametrize("case", ["in_kernel_65_splits", "in_kernel_32_heads", "merge_kernel_1032_splits"])
+def test_merge_paths(kvc, case):
+    """The split merge past its fast paths, against the oracle: the last split CTA
+    merging more than 32 splits (its lanes loop) or 32 query heads' rows, and
+    merge_kernel over more splits than it keeps weights for in shared memory
+    (1 024; the rest are recomputed) and than a thread preloads."""
+    env = {"in_kernel_65_splits": dict(KVC_SPLIT_CHUNK="4", KVC_MERGE_ROWS="4096"),
+           "in_kernel_32_heads": dict(KVC_SPLIT_CHUNK="16", KVC_MERGE_ROWS="4096"),
+           "merge_kernel_1032_splits": dict(KVC_SPLIT_CHUNK="4")}[case]
+    shape = {"in_kernel_65_splits": dict(H_Q=8, H_KV=8, lens=[4096, 1000]),
+             "in_kernel_32_heads": dict(H_Q=32, H_KV=1, lens=[4096, 77]),
+             "merge_kernel_1032_splits": dict(H_Q=4, H_KV=1, lens=[65999, 3])}[case]
+    w = _custom(B=len(shape["lens"]), H_Q=shape["H_Q"], H_KV=shape["H_KV"], d_h=128, lens=shape["lens"], seed=23)
+    os.environ.update(env)
+    try:
+        _run(kvc, w, bytes_check=False)
+    finally:
+        for k in env:
+            os.environ.pop(k, None)
+
+
 def test_split_counts_agree(kvc):
     """Changing the split size changes only rounding: all within tolerance of the oracle."""
     w = _custom(B=3, H_Q=16, H_KV=4, d_h=128, lens=[2000, 4097, 777])
