@@ -67,8 +67,10 @@ typedef enum {
     KVC_ERR_OOM = 2,          /* device allocation failed */
     KVC_ERR_BAD_BLOCK = 3,    /* a table entry read by the kernel is -1 or >= num_blocks (device-detected) */
     KVC_ERR_RANGE = 4,        /* a position lies past its table row, or a length is negative (device-detected) */
-    KVC_ERR_ALIAS = 5,        /* reserved: two writes of one call aimed at one slot */
-    KVC_ERR_STALE = 6,        /* reserved: a table stamped for another pool generation */
+    KVC_ERR_ALIAS = 5,        /* a write into a block other sequences still map (kvc_alloc_commit); the
+                               * device calls do not detect aliasing: see kvc_decode_step */
+    KVC_ERR_STALE = 6,        /* a lease stamp no longer current: the sequence was released or one of its
+                               * table entries was replaced (kvc_alloc_check) */
     KVC_ERR_TIMEOUT = 7,      /* a bounded device-side wait expired; results of that call are invalid */
     KVC_ERR_CUDA = 8,         /* a CUDA runtime call failed */
     KVC_ERR_UNSUPPORTED = 9   /* a valid shape this build has no kernel for (see each call) */
@@ -105,10 +107,15 @@ typedef struct {
  * PagedAttention allocates KV in blocks": the pool is initialised up front).
  * Bytes: L * N * 2 * H_KV * bs * d_h * s (s = 1/2 for int4), plus for e4m3 / int4 the scale array
  * (initialised to 1.0).  Pool contents are uninitialised.
- * Limits: 1 <= block_size <= 128, head_dim in {64, 128, 256} for bf16,
- * {128, 256} for e4m3 and 128 for int4, 1 <= H_KV <= 256, num_blocks >= 1, the pool's total
- * row count L*N*H_KV*2*bs < 2^31.  Errors: KVC_ERR_ARG, KVC_ERR_OOM,
- * KVC_ERR_CUDA; *out is NULL on error. */
+ * Limits: 1 <= block_size <= 128, head_dim 64 or 128 for bf16 and 128 for
+ * e4m3 and int4 (the widths the attention kernels serve), 1 <= H_KV <= 256,
+ * num_blocks >= 1, the pool's total row count L*N*H_KV*2*bs < 2^31.
+ * Every attention call (kvc_decode_attn, kvc_decode_step, kvc_prefill_attn,
+ * kvc_mixed_step, kvc_decode_attn_noalloc) needs block_size 16; a pool of
+ * another block size serves kvc_append, kvc_write_tokens and kvc_copy_blocks
+ * (e.g. the 4-position blocks of Table 21.1) and its attention calls return
+ * KVC_ERR_UNSUPPORTED.  Errors: KVC_ERR_ARG, KVC_ERR_OOM, KVC_ERR_CUDA; *out is
+ * NULL on error. */
 KVC_API kvc_status kvc_pool_create(int64_t num_blocks, int32_t block_size, int32_t num_layers,
                            int32_t num_kv_heads, int32_t head_dim, kvc_dtype dtype, kvc_pool **out);
 
@@ -198,8 +205,13 @@ KVC_API kvc_status kvc_write_tokens(kvc_pool *pool, int32_t layer, const int32_t
  *   seq_lens: device int32 [B], positions attended (after the append);
  *             n = 0 gives out = 0 and lse = -inf
  *   out:      device fp32 [B][H_Q][d_h];  lse: device fp32 [B][H_Q] or NULL
- * Requires block_size == 16, H_Q % H_KV == 0 and H_Q / H_KV <= 32
- * (else KVC_ERR_UNSUPPORTED / KVC_ERR_ARG).  The pool's workspace for
+ * Requires H_Q % H_KV == 0 (else KVC_ERR_ARG), block_size 16 and
+ * H_Q / H_KV <= 32 (else KVC_ERR_UNSUPPORTED); head_dim is 64 or 128 (bf16)
+ * or 128 (e4m3, int4), as kvc_pool_create admits.  Groups of 32 query heads
+ * on d_h 128 bf16 pools (MQA) run on a tensor-memory (tcgen05) kernel: one
+ * CTA per SM streams 128-position tiles, with scores and outputs in tensor
+ * memory; the environment variable KVC_TC=0 selects the split kernel for
+ * them too.  The pool's workspace for
  * split partials grows on first use with a larger batch (a cudaMalloc, so
  * make one call before capturing a CUDA graph; see kvc_pool_reserve).
  * Device-detected errors as for kvc_append; the affected sequence's outputs
@@ -233,7 +245,10 @@ KVC_API kvc_status kvc_decode_step(kvc_pool *pool, int32_t layer, const void *q,
  * "End-to-end flow": the new tokens attend to the shared prefix, the table
  * stitching shared and private blocks into one sequence).  Query i sits at
  * position q_start + i and reads positions 0 .. q_start + i, so its keys and
- * values must already be in the pool (kvc_write_tokens).
+ * values must already be in the pool (kvc_write_tokens).  bf16 pools run on a
+ * tensor-memory (tcgen05) kernel: 128 query rows (128 / g positions x the g
+ * heads of a KV head) per CTA, scores and outputs in tensor memory (KVC_TC=0
+ * selects the warp-level kernels).
  *   q: device bf16 [n_q][H_Q][d_h];  block_table_row: device int32 [max_blocks]
  *   out: device fp32 [n_q][H_Q][d_h];  lse: device fp32 [n_q][H_Q] or NULL
  * Same arithmetic, requirements and errors as kvc_decode_attn. */
@@ -241,18 +256,21 @@ KVC_API kvc_status kvc_prefill_attn(kvc_pool *pool, int32_t layer, const void *q
                             const int32_t *block_table_row, int32_t max_blocks, int32_t q_start,
                             float *out, float *lse, float scale, kvc_stream_t stream);
 
-/* A decode step and a prefill chunk in ONE launch ("KV cache: Generation
+/* A decode step and a prefill chunk together ("KV cache: Generation
  * state, latency, and allocation" 21.3: chunked prefill runs beside the
  * decode steps of other requests; the xf_kv_cache page, "End-to-end flow").
  * Computes exactly what kvc_decode_step(q .. lse) followed by
- * kvc_prefill_attn(prefill_q .. prefill_lse) compute, in one kernel whose CTAs
- * are the two calls' CTAs interleaved, so the chunk's tensor-core work runs
- * while the decode CTAs stream the cache from HBM.  The prefill row's
- * positions 0 .. q_start + n_q - 1 must already be in the pool and must not be
- * among the positions the decode part appends (they are written during the
- * launch).  n_q == 0 or B == 0 reduces to the other call alone.  Decode groups
- * of more than 16 query heads, and head widths other than 128 (64 for bf16
- * pools), run the two calls as two launches.
+ * kvc_prefill_attn(prefill_q .. prefill_lse) compute, with the chunk's work
+ * running beside the decode step's so that its tensor-core work overlaps the
+ * HBM stream: on bf16 pools the decode launch is followed by the
+ * tensor-memory prefill kernel launched as its programmatic dependent (its
+ * CTAs take SMs as the decode CTAs drain; it reads nothing the step writes
+ * and never waits on it); on e4m3 and int4 pools one kernel's CTAs are the
+ * two calls' CTAs interleaved.  The prefill row's positions
+ * 0 .. q_start + n_q - 1 must already be in the pool and must not be among
+ * the positions the decode part appends (they are written meanwhile).
+ * n_q == 0 or B == 0 reduces to the other call alone.  On e4m3 and int4 pools,
+ * decode groups of more than 16 query heads run the two calls in order.
  * Arguments, requirements and errors as kvc_decode_step and kvc_prefill_attn. */
 KVC_API kvc_status kvc_mixed_step(kvc_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
                                   const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, int32_t B,
@@ -276,17 +294,21 @@ KVC_API kvc_status kvc_pool_reserve(kvc_pool *pool, int32_t max_batch, int32_t n
  * fragment memory promised to KV blocks), and latency-critical loops where
  * cudaMalloc / cudaFree would synchronise the device and stall other streams.
  * Same arguments, arithmetic and results as kvc_decode_attn, but the split
- * partials live in a fixed 8 MiB device array inside the library (held by
- * every GPU that loads the library until the process exits) instead of the
- * pool's workspace, so no cudaMalloc, cudaFree or allocating routine runs.
+ * partials live in a fixed 8 MiB device array inside the library instead of
+ * the pool's workspace, so no cudaMalloc, cudaFree or allocating routine runs.
+ * The array exists on every GPU where the library's device code is loaded,
+ * from then until that context is destroyed; kvc_pool_create loads it, so it
+ * is reserved when the first pool of a device is created.
  * Limit: when the batch is split, B * H_Q * splits * (d_h + 2) floats must fit
  * in 8 MiB (2^21 floats), where splits is the split count kvc_decode_attn
  * would choose; a larger request returns KVC_ERR_ARG before any launch.
- * The first call on a device looks up the array's device address (a
- * cudaGetSymbolAddress with that device current); make that first call before
- * any stream capture.  Every call on a device shares the one array, and it
- * keeps the last call's contents (nothing in it needs to start at zero:
- * every partial read is written by the same call first), so calls that
+ * The array's device address is looked up (cudaGetSymbolAddress with the
+ * pool's device current) at pool creation and cached per CUDA context, so a
+ * context created anew after a device reset gets a fresh lookup; a call in a
+ * context where no pool was created does the lookup itself and should come
+ * before any stream capture.  Every call on a device shares the one array,
+ * and it keeps the last call's contents (nothing in it needs to start at
+ * zero: every partial read is written by the same call first), so calls that
  * overlap on the GPU (other streams, other threads, other pools of the same
  * device) race and must be serialised by the caller. */
 KVC_API kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
@@ -350,6 +372,21 @@ KVC_API kvc_status kvc_alloc_seq_info(const kvc_alloc *alloc, int32_t seq, int64
 KVC_API kvc_status kvc_alloc_block_tables(const kvc_alloc *alloc, const int32_t *seqs, int32_t n, int32_t max_blocks,
                                           int32_t *table, int32_t *lens);
 KVC_API kvc_status kvc_alloc_counts(const kvc_alloc *alloc, int64_t *n_free, int64_t *n_used, int64_t *n_cached);
+/* Lease stamps ("KV Cache Explained", "The lease race when KV crosses
+ * workers": a party that hands a request's blocks to another must let the
+ * receiver detect that the lease expired and the blocks may have gone to
+ * another request -- generation checks, with a mismatch treated as failure).
+ * kvc_alloc_lease returns an opaque stamp of the sequence's current table: it
+ * changes when the sequence is released (its id may then be handed out again
+ * and its blocks to other requests) and when copy-on-write replaces one of its
+ * table entries; blocks mapped at the end of the table leave earlier stamps
+ * valid (the entries they cover are unchanged).  kvc_alloc_check returns
+ * KVC_OK if `stamp` is still current and KVC_ERR_STALE otherwise; a consumer
+ * checks before it uses a table it received (e.g. before a decode step on a
+ * transferred request).  Errors: KVC_ERR_ARG for an id never handed out (check)
+ * or not live (lease). */
+KVC_API kvc_status kvc_alloc_lease(const kvc_alloc *alloc, int32_t seq, uint64_t *stamp);
+KVC_API kvc_status kvc_alloc_check(const kvc_alloc *alloc, int32_t seq, uint64_t stamp);
 /* Reference count of a block, or -1 for an id outside the pool. */
 KVC_API int32_t kvc_alloc_refcount(const kvc_alloc *alloc, int32_t block);
 

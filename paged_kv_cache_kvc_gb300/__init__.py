@@ -50,7 +50,8 @@ EXPORTS = ["kvc_pool_create", "kvc_pool_destroy", "kvc_pool_info", "kvc_pool_set
            "kvc_mixed_step",
            "kvc_alloc_create", "kvc_alloc_destroy", "kvc_alloc_new_seq", "kvc_alloc_fork", "kvc_alloc_reserve",
            "kvc_alloc_commit", "kvc_alloc_release", "kvc_alloc_publish", "kvc_alloc_match", "kvc_alloc_seq_info",
-           "kvc_alloc_block_tables", "kvc_alloc_counts", "kvc_alloc_refcount", "kvc_copy_blocks"]
+           "kvc_alloc_block_tables", "kvc_alloc_counts", "kvc_alloc_refcount", "kvc_alloc_lease", "kvc_alloc_check",
+           "kvc_copy_blocks"]
 
 
 def load(path: str = LIB_PATH):
@@ -100,6 +101,8 @@ def load(path: str = LIB_PATH):
     L.kvc_alloc_block_tables.restype, L.kvc_alloc_block_tables.argtypes = st, [vp, vp, i32, i32, vp, vp]
     L.kvc_alloc_counts.restype, L.kvc_alloc_counts.argtypes = st, [vp, vp, vp, vp]
     L.kvc_alloc_refcount.restype, L.kvc_alloc_refcount.argtypes = i32, [vp, i32]
+    L.kvc_alloc_lease.restype, L.kvc_alloc_lease.argtypes = st, [vp, i32, ctypes.POINTER(u64)]
+    L.kvc_alloc_check.restype, L.kvc_alloc_check.argtypes = st, [vp, i32, u64]
     L.kvc_copy_blocks.restype, L.kvc_copy_blocks.argtypes = st, [vp, vp, i32, vp]
     _lib = L
     return L
@@ -423,6 +426,20 @@ class Allocator:
 
     def refcount(self, block) -> int:
         return int(load().kvc_alloc_refcount(self._h(), block))
+
+    def lease(self, seq) -> int:
+        """Opaque stamp of the sequence's current block table."""
+        st = ctypes.c_uint64()
+        _check(load().kvc_alloc_lease(self._h(), seq, ctypes.byref(st)), "kvc_alloc_lease")
+        return st.value
+
+    def check(self, seq, stamp) -> bool:
+        """True while `stamp` is current; False once it is stale (KVC_ERR_STALE)."""
+        r = load().kvc_alloc_check(self._h(), seq, int(stamp))
+        if r == KVC_ERR_STALE:
+            return False
+        _check(r, "kvc_alloc_check")
+        return True
 
 
 def kvc_copy_blocks(pool, pairs, stream=None):

@@ -28,6 +28,7 @@ constexpr int32_t kFree = 0, kUsed = 1, kCached = 2;
 
 struct Seq {
     bool live = false;
+    uint32_t version = 0;            // table entries replaced by copy-on-write since the sequence began
     int64_t len = 0;                 // tokens written (committed); capacity is blocks.size() * bs
     std::vector<int32_t> blocks;
     std::vector<uint64_t> hashes;    // identity of each published full block
@@ -70,6 +71,7 @@ struct kvc_alloc {
     std::vector<CachedKey> block_key;
     std::unordered_multimap<uint64_t, int32_t> by_hash; // identity -> block
     std::vector<Seq> seqs;
+    std::vector<uint32_t> incarnation;                  // per sequence id: times it was handed out
 };
 
 namespace {
@@ -143,11 +145,19 @@ int32_t new_seq_slot(kvc_alloc *a)
         if (!a->seqs[i].live) {
             a->seqs[i] = Seq{};
             a->seqs[i].live = true;
+            ++a->incarnation[i];
             return static_cast<int32_t>(i);
         }
     a->seqs.push_back(Seq{});
     a->seqs.back().live = true;
+    a->incarnation.push_back(1);
     return static_cast<int32_t>(a->seqs.size() - 1);
+}
+
+// (times the id was handed out, copy-on-write replacements of its table entries)
+uint64_t lease_stamp(const kvc_alloc *a, int32_t s)
+{
+    return (static_cast<uint64_t>(a->incarnation[s]) << 32) | a->seqs[s].version;
 }
 
 }  // namespace
@@ -237,6 +247,7 @@ extern "C" kvc_status kvc_alloc_reserve(kvc_alloc *a, int32_t seq, int32_t n_tok
         cow_pairs[1] = fresh;
         if (n_cow) *n_cow = 1;
         s->blocks[w] = fresh;
+        ++s->version;                                   // tables handed out before now map the old block
         drop_ref(a, old);
     }
     for (int64_t i = 0; i < need_blocks; ++i) {
@@ -353,6 +364,21 @@ extern "C" kvc_status kvc_alloc_block_tables(const kvc_alloc *a, const int32_t *
             table[static_cast<int64_t>(i) * max_blocks + j] = j < static_cast<int32_t>(s->blocks.size()) ? s->blocks[j] : -1;
         if (lens) lens[i] = static_cast<int32_t>(s->len);
     }
+    return KVC_OK;
+}
+
+extern "C" kvc_status kvc_alloc_lease(const kvc_alloc *a, int32_t seq, uint64_t *stamp)
+{
+    Seq *s = get_seq(const_cast<kvc_alloc *>(a), seq);
+    if (!s || !stamp) return KVC_ERR_ARG;
+    *stamp = lease_stamp(a, seq);
+    return KVC_OK;
+}
+
+extern "C" kvc_status kvc_alloc_check(const kvc_alloc *a, int32_t seq, uint64_t stamp)
+{
+    if (!a || seq < 0 || seq >= static_cast<int32_t>(a->seqs.size())) return KVC_ERR_ARG;
+    if (!a->seqs[seq].live || lease_stamp(a, seq) != stamp) return KVC_ERR_STALE;
     return KVC_OK;
 }
 

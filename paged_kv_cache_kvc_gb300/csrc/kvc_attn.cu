@@ -3,7 +3,9 @@
 #include <cmath>
 #include <cstdlib>
 
+#include "kvc_decode_tc.cuh"
 #include "kvc_prefill.cuh"
+#include "kvc_prefill_tc.cuh"
 
 namespace kvc {
 
@@ -297,6 +299,100 @@ static kvc_status run_mixed(kvc_pool *pool, DecodeParams &pd, DecodeParams &pp, 
     return KVC_OK;
 }
 
+// Splits of the tensor-memory decode kernel: whole 128-token tiles, and about one
+// CTA per resident slot (one per SM): its 3-stage ring keeps 128 KiB in flight,
+// so more CTAs than slots only add split partials.  KVC_SPLIT_CHUNK overrides
+// (rounded up to whole tiles).
+void choose_split_tc(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits)
+{
+    const int tiles = (max_blocks + kTcBlocks - 1) / kTcBlocks;
+    int ct = 0;
+    if (const char *e = std::getenv("KVC_SPLIT_CHUNK")) ct = (std::atoi(e) + kTcBlocks - 1) / kTcBlocks;
+    if (ct <= 0) {
+        const double slots = static_cast<double>(pool->num_sms) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+        long ns = units > 0 ? std::lround(slots / units) : 1;
+        ns = std::max(1L, std::min(ns, static_cast<long>(tiles)));
+        ct = static_cast<int>((tiles + ns - 1) / ns);
+    }
+    *chunk = ct * kTcBlocks;
+    *max_splits = (max_blocks + *chunk - 1) / *chunk;
+}
+
+// The tensor-memory kernel serves decode steps of 32-head groups on d_h 128 bf16 pools
+// (KVC_TC=0 selects the split kernel for them).
+DecodeKernel tc_kernel_for(const kvc_pool *pool, const DecodeParams &p)
+{
+    const char *e = std::getenv("KVC_TC");
+    if ((e && e[0] == '0') || !p.lens || p.ppu != 1 || !pool->tmap16_ok || pool->bs != kBS)
+        return DecodeKernel{nullptr, 0, 0};
+    return select_decode_tc(pool->D, p.g, pool->dtype);
+}
+
+static kvc_status run_decode_tc(kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream)
+{
+    if (k.ctas_per_sm <= 0) return KVC_ERR_CUDA;
+    choose_split_tc(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits);
+    if (p.max_splits > 65535) return KVC_ERR_UNSUPPORTED;
+    p.counters = nullptr;   // splits are merged by merge_kernel
+    p.part_o = nullptr;
+    p.part_ml = nullptr;
+    if (p.max_splits > 1) {
+        kvc_status st = ensure_workspace(pool, static_cast<size_t>(p.B) * p.H_KV,
+                                         workspace_bytes(p.n_pos, p.H_Q, p.max_splits, pool->D));
+        if (st != KVC_OK) return st;
+        const size_t n = static_cast<size_t>(p.n_pos) * p.H_Q * p.max_splits;
+        p.part_o = ws_data(pool);
+        p.part_ml = reinterpret_cast<float2 *>(p.part_o + n * pool->D);
+    }
+    void *args[] = {const_cast<CUtensorMap *>(&pool->tmap16), &p};
+    const cudaError_t e = cudaLaunchKernel(k.fn, dim3(p.max_splits, p.H_KV, p.B), dim3(kTcThreads), args, k.smem,
+                                           stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (p.max_splits > 1) return launch_split_merge(p, pool->D, stream);
+    return KVC_OK;
+}
+
+// The tensor-memory prefill kernel serves bf16 pools of d_h 64 or 128, every group
+// size (KVC_TC=0, or KVC_PREFILL_PPU for the split kernel's causal tiles, select
+// the other kernels).
+static DecodeKernel prefill_tc_for(const kvc_pool *pool)
+{
+    const char *e = std::getenv("KVC_TC");
+    if ((e && e[0] == '0') || std::getenv("KVC_PREFILL_PPU") || !pool->tmap16_ok || pool->bs != kBS)
+        return DecodeKernel{nullptr, 0, 0};
+    return select_prefill_tc(pool->D, pool->dtype);
+}
+
+// grid (1, KV head, tile of 128 / g positions).  dependent: launched as a
+// programmatic dependent of the kernel before it on the stream, whose CTAs it may
+// run beside (it reads nothing that kernel writes and never waits on it).
+static kvc_status launch_prefill_tc(const kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, bool dependent,
+                                    cudaStream_t stream)
+{
+    if (k.ctas_per_sm <= 0) return KVC_ERR_CUDA;
+    p.ppu = 128 / p.g;
+    p.B = (p.n_pos + p.ppu - 1) / p.ppu;
+    p.chunk = p.max_blocks;
+    p.max_splits = 1;
+    if (p.B > 65535) return KVC_ERR_UNSUPPORTED;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, pool->H_KV, p.B);
+    cfg.blockDim = dim3(kPtThreads);
+    cfg.dynamicSmemBytes = k.smem;
+    cfg.stream = stream;
+    cfg.attrs = dependent ? attr : nullptr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    void *args[] = {const_cast<CUtensorMap *>(&pool->tmap16), &p};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, args);
+    if (e != cudaSuccess) return cuda_status(e);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return KVC_OK;
+}
+
 static bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
 
 static kvc_status common_attn_checks(kvc_pool *pool, int32_t layer, const void *q, int32_t H_Q, const int32_t *bt,
@@ -334,6 +430,8 @@ static void fill_common(DecodeParams &p, const kvc_pool *pool, int32_t layer, co
 
 static kvc_status dispatch(kvc_pool *pool, DecodeParams &p, cudaStream_t stream)
 {
+    const DecodeKernel tc = tc_kernel_for(pool, p);
+    if (tc.fn) return run_decode_tc(pool, p, tc, stream);
     if (pool->dtype == KVC_FP8_E4M3) return launch_decode_fp8(pool, p, stream);
     if (pool->dtype == KVC_INT4) return launch_decode_int4(pool, p, stream);
     return launch_decode_bf16(pool, p, stream);
@@ -408,6 +506,8 @@ extern "C" kvc_status kvc_prefill_attn(kvc_pool *pool, int32_t layer, const void
     // the chunk reads positions < q_start + n_q: plan splits over those blocks only
     p.max_blocks = static_cast<int32_t>((static_cast<int64_t>(q_start) + n_q + kBS - 1) / kBS);
     p.n_pos = n_q;
+    const DecodeKernel tc = prefill_tc_for(pool);
+    if (tc.fn) return launch_prefill_tc(pool, p, tc, false, static_cast<cudaStream_t>(stream));
     if (fast_prefill(pool, p.g)) {   // query tiles of 64 / g positions x g heads on the M dimension
         p.ppu = 64 / p.g;
         p.B = (n_q + p.ppu - 1) / p.ppu;
@@ -443,6 +543,22 @@ extern "C" kvc_status kvc_mixed_step(kvc_pool *pool, int32_t layer, const void *
                             prefill_out, prefill_lse, scale);
     if (st != KVC_OK) return st;
     if (static_cast<int64_t>(q_start) + n_q > static_cast<int64_t>(prefill_max_blocks) * kBS) return KVC_ERR_RANGE;
+    if (const DecodeKernel tc = prefill_tc_for(pool); tc.fn) {
+        // the decode step, then the chunk on the tensor-memory prefill kernel as a programmatic
+        // dependent: its CTAs take SMs as the decode CTAs drain, and it never waits on them
+        st = kvc_decode_step(pool, layer, q, num_q_heads, block_tables, max_blocks, seq_lens, B, k_new, v_new, out, lse,
+                             scale, stream);
+        if (st != KVC_OK) return st;
+        DecodeParams pt{};
+        fill_common(pt, pool, layer, prefill_q, num_q_heads, prefill_block_table_row, prefill_max_blocks, prefill_out,
+                    prefill_lse, scale);
+        pt.lens = nullptr;
+        pt.bt_stride = 0;
+        pt.len_base = q_start;
+        pt.max_blocks = static_cast<int32_t>((static_cast<int64_t>(q_start) + n_q + kBS - 1) / kBS);
+        pt.n_pos = n_q;
+        return launch_prefill_tc(pool, pt, tc, true, static_cast<cudaStream_t>(stream));
+    }
     DecodeParams pd{};
     fill_common(pd, pool, layer, q, num_q_heads, block_tables, max_blocks, out, lse, scale);
     pd.lens = seq_lens;

@@ -256,8 +256,8 @@ extern "C" kvc_status kvc_pool_create(int64_t num_blocks, int32_t block_size, in
     if (dtype != KVC_BF16 && dtype != KVC_FP8_E4M3 && dtype != KVC_INT4) return KVC_ERR_ARG;
     const int bits = dtype == KVC_BF16 ? 16 : (dtype == KVC_FP8_E4M3 ? 8 : 4);
     const int s = bits / 8;
-    const bool dim_ok = dtype == KVC_BF16 ? (head_dim == 64 || head_dim == 128 || head_dim == 256)
-                        : dtype == KVC_FP8_E4M3 ? (head_dim == 128 || head_dim == 256) : head_dim == 128;
+    // the head widths the attention kernels serve
+    const bool dim_ok = dtype == KVC_BF16 ? (head_dim == 64 || head_dim == 128) : head_dim == 128;
     if (!dim_ok) return KVC_ERR_ARG;
     const uint64_t rows = static_cast<uint64_t>(num_layers) * static_cast<uint64_t>(num_blocks) *
                           static_cast<uint64_t>(num_kv_heads) * 2u * static_cast<uint64_t>(block_size);
@@ -320,7 +320,19 @@ extern "C" kvc_status kvc_pool_create(int64_t num_blocks, int32_t block_size, in
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         pool->tmap_ok = (r == CUDA_SUCCESS);
+        // keys and values of 16 positions as separate boxes (the tensor-memory kernels stage
+        // them in separate regions); 16-bit pools whose blocks hold whole 16-position groups
+        pool->tmap16_ok = false;
+        if (bits == 16 && block_size % 16 == 0) {
+            cuuint32_t box16[2] = {static_cast<cuuint32_t>(128 / s), 16u};
+            const CUresult r16 = enc(&pool->tmap16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool->base, gdim, gstride,
+                                     box16, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            pool->tmap16_ok = (r16 == CUDA_SUCCESS);
+        }
     }
+    noalloc_prepare(pool->device);   // the allocation-free decode's scratch: reserved now, not mid-step
+    (void)cudaGetLastError();
     *out = pool;
     return KVC_OK;
 }

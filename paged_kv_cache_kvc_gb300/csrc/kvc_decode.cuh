@@ -361,19 +361,27 @@ __device__ __forceinline__ void block_update(uint32_t st, const uint32_t (&qf)[N
     } else if constexpr (INT4) {
         // output channels permuted as for e4m3: m-row gq of tile mt is channel 16*gq + 2*mt,
         // m-row gq+8 the next one; the thread's 16 channels are 8 bytes of each value row
-        uint32_t vw[4][2];   // value rows 2tg, 2tg+1, 2tg+8, 2tg+9
+        // value rows 2tg, 2tg+1, 2tg+8, 2tg+9.  Lanes with odd tg load each pair in the other
+        // order, so that every load's four lines (two token rows each) use all eight 16-byte
+        // chunk slots of the 128-byte swizzle (two wavefronts, not four); the byte
+        // selectors below put the pair back in order.
+        const uint32_t par = static_cast<uint32_t>(tg & 1);
+        uint32_t vw[4][2];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const uint32_t a = st + swz64(kBS + 2 * tg + (r & 1) + (r >> 1) * 8, gq >> 1) + 8 * (gq & 1);
+            const int row = kBS + 2 * tg + ((r & 1) ^ static_cast<int>(par)) + (r >> 1) * 8;
+            const uint32_t a = st + swz64(row, gq >> 1) + 8 * (gq & 1);
             asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(vw[r][0]), "=r"(vw[r][1]) : "r"(a));
         }
+        // selector of byte k: [row 2tg .b_k, same, row 2tg+1 .b_k, same]
+        const uint32_t sel0 = par ? 0x0044u : 0x4400u;
 #pragma unroll
         for (int w = 0; w < 2; ++w)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                constexpr uint32_t kSel[4] = {0x4400u, 0x5511u, 0x6622u, 0x7733u};   // [A.b_k, A.b_k, B.b_k, B.b_k]
-                const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], kSel[k]);
-                const uint32_t x89 = __byte_perm(vw[2][w], vw[3][w], kSel[k]);
+                const uint32_t sel = sel0 + 0x1111u * static_cast<uint32_t>(k);
+                const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], sel);
+                const uint32_t x89 = __byte_perm(vw[2][w], vw[3][w], sel);
                 const uint32_t a[4] = {nibbles_to_f16x2(x01), nibbles_hi_to_f16x2(x01),
                                        nibbles_to_f16x2(x89), nibbles_hi_to_f16x2(x89)};
 #pragma unroll

@@ -23,6 +23,8 @@ struct kvc_pool {
     uint32_t *err;        // device error word
     CUtensorMap tmap;     // rows of D elements; box {128 B, 2*bs rows}; 128-byte swizzle
     bool tmap_ok;
+    CUtensorMap tmap16;   // same rows, box {128 B, 16 rows}: the keys or the values of 16 positions
+    bool tmap16_ok;
     void *ws;             // workspace: arrival counters [ws_counters], then split / record partials
     size_t ws_bytes;      // partial bytes after the counter region
     size_t ws_counters;   // arrival counters at the front (zero between launches)
@@ -76,6 +78,13 @@ kvc_status launch_decode_int4(const kvc_pool *pool, DecodeParams &p, cudaStream_
 // Split-K sizing: blocks per split and the split count for a batch.
 void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits,
                   int n_tiles);
+// Split sizing of the tensor-memory decode kernel (whole 128-token tiles).
+void choose_split_tc(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits);
+
+// Look up (and so reserve) the allocation-free decode's scratch array for the current
+// context of `device`; kvc_pool_create calls it.
+void noalloc_prepare(int device);
+
 // 8-wide query n-tiles a group of g query heads occupies in the decode kernel.
 inline int n_tiles(int g) { return g <= 8 ? 1 : (g <= 16 ? 2 : 4); }
 

@@ -10,8 +10,9 @@
 // partials in kvc_noalloc_scratch.
 #include <cmath>
 #include <mutex>
+#include <unordered_map>
 
-#include "kvc_decode.cuh"
+#include "kvc_decode_tc.cuh"
 
 namespace kvc {
 
@@ -19,27 +20,65 @@ namespace kvc {
 constexpr size_t kNoallocScratchFloats = size_t(2) << 20;
 static __device__ __align__(256) float kvc_noalloc_scratch[kNoallocScratchFloats];
 
-// Device address of the scratch array, looked up once per device with that
-// device current.  (In host code the array's name is only a host-side stand-in.)
+// Device address of the scratch array in the calling thread's current context.
+// In host code the array's name is only a host-side stand-in, so the address
+// comes from cudaGetSymbolAddress, made with the pool's device current.  It is
+// looked up once per context and cached under the context's unique id: after a
+// device reset the runtime creates a new primary context (a new id), the module
+// is loaded again and the array may sit elsewhere, so the stale address of the
+// old context is never used.  Without the driver's context-id entry points the
+// address is looked up on every call.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+template <class Fn>
+static Fn driver_fn(const char *name)
+{
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return reinterpret_cast<Fn>(f);
+}
+
+static float *lookup_scratch()
+{
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, kvc_noalloc_scratch) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return static_cast<float *>(p);
+}
+
 static float *noalloc_scratch_ptr(int device)
 {
-    constexpr int kMaxDevices = 128;
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
     static std::mutex mu;
-    static float *ptrs[kMaxDevices] = {};
-    if (device < 0 || device >= kMaxDevices) return nullptr;
+    static std::unordered_map<unsigned long long, float *> by_context;
+    if (cudaSetDevice(device) != cudaSuccess) return nullptr;   // makes the device's primary context current
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return lookup_scratch();
     std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[device]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, kvc_noalloc_scratch) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return nullptr;
-        }
-        ptrs[device] = static_cast<float *>(p);
-    }
-    return ptrs[device];
+    auto it = by_context.find(id);
+    if (it != by_context.end()) return it->second;
+    float *p = lookup_scratch();
+    if (p) by_context.emplace(id, p);
+    return p;
 }
 
 static bool is_aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+// Called by kvc_pool_create with the pool's device current: loads the module and
+// reserves the array there (and caches its address) when the pool is created,
+// not in the middle of a later decode step.
+void noalloc_prepare(int device) { (void)noalloc_scratch_ptr(device); }
 
 }  // namespace kvc
 
@@ -63,7 +102,7 @@ extern "C" kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, con
         return KVC_ERR_ARG;
     kvc_status st = check_device(pool);
     if (st != KVC_OK) return st;
-    float *scratch = noalloc_scratch_ptr(pool->device);   // first call on a device: symbol lookup
+    float *scratch = noalloc_scratch_ptr(pool->device);   // cached per context; looked up at pool creation
     if (!scratch) return KVC_ERR_CUDA;
 
     DecodeParams p{};
@@ -88,13 +127,16 @@ extern "C" kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, con
     p.lse = lse;
     p.err = pool->err;
 
+    const DecodeKernel tc = tc_kernel_for(pool, p);   // the kernel kvc_decode_attn would launch
     const DecodeKernel k =
-        pool->dtype == KVC_FP8_E4M3 ? select_decode_fp8(pool->D, p.g)
+        tc.fn                       ? tc
+        : pool->dtype == KVC_FP8_E4M3 ? select_decode_fp8(pool->D, p.g)
         : pool->dtype == KVC_INT4   ? select_decode_int4(pool->D, p.g)
                                     : select_decode_bf16(pool->D, p.g);
     if (!k.fn) return KVC_ERR_UNSUPPORTED;
     if (k.ctas_per_sm <= 0) return KVC_ERR_CUDA;
-    choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits, n_tiles(p.g));
+    if (tc.fn) choose_split_tc(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits);
+    else choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits, n_tiles(p.g));
     if (p.max_splits > 65535) return KVC_ERR_UNSUPPORTED;
     if (p.max_splits > 1) {
         // partials: o [B][H_Q][splits][D] then (max, sum) [B][H_Q][splits]; every slot read is written first
@@ -104,8 +146,9 @@ extern "C" kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, con
         p.part_ml = reinterpret_cast<float2 *>(scratch + n * pool->D);
     }
     const dim3 grid(p.max_splits, p.H_KV, p.B);
-    void *args[] = {const_cast<CUtensorMap *>(&pool->tmap), &p};
-    const cudaError_t e = cudaLaunchKernel(k.fn, grid, dim3(kThreads), args, k.smem, static_cast<cudaStream_t>(stream));
+    void *args[] = {const_cast<CUtensorMap *>(tc.fn ? &pool->tmap16 : &pool->tmap), &p};
+    const cudaError_t e = cudaLaunchKernel(k.fn, grid, dim3(tc.fn ? kTcThreads : kThreads), args, k.smem,
+                                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (p.max_splits > 1) return launch_split_merge(p, pool->D, static_cast<cudaStream_t>(stream));

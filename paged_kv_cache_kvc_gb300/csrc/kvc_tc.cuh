@@ -49,6 +49,13 @@ __host__ __device__ constexpr uint32_t tc_idesc_f16(int M, int N, bool bf16, boo
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same descriptor with its start address moved by `bytes` (a multiple of 16; the
+// 14-bit field holds every shared-memory address, so the add never carries out of it).
+__host__ __device__ constexpr uint64_t tc_desc_advance(uint64_t desc, uint32_t bytes)
+{
+    return desc + (bytes >> 4);
+}
+
 // Byte offset of 16-byte chunk `ch` of 128-byte row `row` inside a run of
 // 128-byte-swizzled atoms (the layout TMA writes with the 128-byte swizzle).
 __host__ __device__ constexpr uint32_t sw128(uint32_t row, uint32_t ch)

@@ -54,6 +54,7 @@ def test_pool_create_rejects_bad_shapes_before_cuda(lib):
     import paged_kv_cache_kvc_gb300 as k
     out = ctypes.c_void_p(1)
     for args in [(0, 16, 1, 8, 128, 0), (10, 0, 1, 8, 128, 0), (10, 16, 1, 8, 96, 0), (10, 16, 1, 8, 64, 1),
+                 (10, 16, 1, 8, 256, 0), (10, 16, 1, 8, 256, 1), (10, 16, 1, 8, 64, 2), (10, 129, 1, 8, 128, 0),
                  (10, 16, 0, 8, 128, 0), (10, 16, 1, 8, 128, 7), (2**40, 16, 1, 8, 128, 0)]:
         assert lib.kvc_pool_create(*args, ctypes.byref(out)) == k.KVC_ERR_ARG
         assert out.value is None

@@ -19,8 +19,9 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "paged_kv_cache_kvc_gb300", "csrc", "kvc_tc.cuh")
 
-SMEM_CASES = [(0x0, 16, 1024, 2), (0x1F0, 16, 1024, 2), (0x12340, 16384, 1024, 2), (0x3FFF0, 8192, 1024, 2),
+SMEM_CASES = [(0x0, 16, 1024, 2), (0x1F0, 16, 1024, 2), (0x12340, 16384, 1024, 2), (0x30000, 8192, 1024, 2),
               (0x4000, 0, 512, 4), (0x8000, 2048, 256, 6), (0x10, 4096, 128, 0)]
+ADVANCE_OFFSETS = [32, 96, 2048, 16384 + 96, 14336]
 IDESC_CASES = [(128, 32, True, False, False), (128, 64, True, True, True), (128, 128, True, False, True),
                (64, 256, False, False, False), (128, 16, True, True, False), (256, 8, False, False, True)]
 
@@ -66,6 +67,10 @@ def encoded():
     for r in range(16):
         for c in range(8):
             lines.append(f'  printf("%u\\n", kvc::sw128({r}u, {c}u));')
+    for (a, l, s_, z) in SMEM_CASES:
+        for off in ADVANCE_OFFSETS:
+            lines.append(f'  printf("%d\\n", (int)(kvc::tc_desc_advance(kvc::tc_smem_desc({a}u, {l}u, {s_}u, {z}u), '
+                         f'{off}u) == kvc::tc_smem_desc({a + off}u, {l}u, {s_}u, {z}u)));')
     with tempfile.TemporaryDirectory() as d:
         src = os.path.join(d, "enc.cu")
         with open(src, "w") as f:
@@ -97,3 +102,10 @@ def test_128_byte_swizzle_chunk_placement(encoded):
         assert sorted(row) == [r * 128 + 16 * c for c in range(8)]
         for c in range(8):
             assert row[c] == r * 128 + 16 * (c ^ (r % 8))
+
+
+def test_descriptor_advance_moves_only_the_start_address(encoded):
+    """Stepping a descriptor along K (32 bytes inside a 128-byte band) or along rows (2 KiB
+    per 16 rows) equals encoding the moved address: nothing carries out of the start field."""
+    off = len(SMEM_CASES) + len(IDESC_CASES) + 16 * 8
+    assert all(int(x) == 1 for x in encoded[off:off + len(SMEM_CASES) * len(ADVANCE_OFFSETS)])
