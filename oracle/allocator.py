@@ -35,7 +35,8 @@ class BlockAllocator:
         self.ref = [0] * num_blocks
         self.identity = {}               # block -> identity (salt, prefix token tuple)
         self.index = {}                  # identity -> block
-        self.seqs = []                   # per id: None or {"blocks": [...], "len": n}
+        self.seqs = []                   # per id: None or {"blocks": [...], "len": n, "replaced": r}
+        self.handed_out = []             # per id: how many times the id was given to a new sequence
 
     # ---------------------------------------------------------- blocks
     def _forget(self, b):
@@ -77,9 +78,11 @@ class BlockAllocator:
     def _new_id(self):
         for i, s in enumerate(self.seqs):
             if s is None:
-                self.seqs[i] = {"blocks": [], "len": 0}
+                self.seqs[i] = {"blocks": [], "len": 0, "replaced": 0}
+                self.handed_out[i] += 1
                 return i
-        self.seqs.append({"blocks": [], "len": 0})
+        self.seqs.append({"blocks": [], "len": 0, "replaced": 0})
+        self.handed_out.append(1)
         return len(self.seqs) - 1
 
     def new_seq(self):
@@ -115,6 +118,7 @@ class BlockAllocator:
             old = s["blocks"][w]
             pairs.append((old, fresh))
             s["blocks"][w] = fresh
+            s["replaced"] += 1           # a table handed out earlier still maps the old block
             self._drop(old)
         for _ in range(need):
             s["blocks"].append(self._take())
@@ -156,6 +160,24 @@ class BlockAllocator:
         for b in hits:
             self._add(b)
         return i, len(hits) * self.bs
+
+    # ---------------------------------------------------------- lease stamps
+    # "KV Cache Explained", "The lease race when KV crosses workers": whoever
+    # receives a request's blocks must be able to tell that the lease expired
+    # (the blocks may belong to another request now) -- a generation check, a
+    # mismatch counting as failure.  A stamp names the sequence id's hand-out
+    # count and how many of its table entries copy-on-write has replaced.
+    def lease(self, seq):
+        s = self.seqs[seq]
+        if s is None:
+            raise ValueError("no such sequence")
+        return (self.handed_out[seq], s["replaced"])
+
+    def check(self, seq, stamp):
+        """True while the stamp still describes the live sequence's table."""
+        if not 0 <= seq < len(self.seqs):
+            raise ValueError("id never handed out")
+        return self.seqs[seq] is not None and self.lease(seq) == stamp
 
     # ---------------------------------------------------------- views
     def table(self, seq, max_blocks):

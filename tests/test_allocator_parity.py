@@ -66,6 +66,13 @@ class Pair:
     def match(self, toks, salt=0):
         return self._both(lambda: self.p.match(toks, salt), lambda: self.o.match(toks, salt))
 
+    def lease(self, s):
+        """Stamps of both sides (compared through check(), not by value)."""
+        return (self.p.lease(s), self.o.lease(s))
+
+    def check_lease(self, s, stamps):
+        return self._both(lambda: self.p.check(s, stamps[0]), lambda: self.o.check(s, stamps[1]))
+
     def check(self, live):
         assert self.p.counts() == self.o.counts()
         assert [self.p.refcount(b) for b in range(self.N)] == self.o.ref
@@ -125,8 +132,14 @@ def test_random_streams(seed, retain):
     rng.shuffle(order)
     x = Pair(N, bs, free_order=order, retain=retain)
     live = []
+    leases = []                                   # (id, stamps) taken along the way, checked later
     prefixes = [[rng.randrange(50) for _ in range(120)] for _ in range(3)]
     for step in range(1500):
+        if live and rng.random() < 0.1:
+            s = rng.choice(live)
+            leases.append((s, x.lease(s)))
+        for s, st in leases[-8:]:                  # stale after a release, an id reuse or copy-on-write
+            x.check_lease(s, st)
         op = rng.random()
         if op < 0.15 or not live:
             live.append(x.new_seq())

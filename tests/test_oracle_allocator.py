@@ -197,3 +197,40 @@ def test_invariants_under_random_operations():
         assert refs == a.ref
         assert len(set(a.free)) + len(set(a.cached)) + sum(1 for r in refs if r) == a.N
         assert not set(a.free) & set(a.cached)
+
+
+def test_lease_race_generation_check():
+    """"KV Cache Explained", "The lease race when KV crosses workers": a
+    receiver holds a request's table under a lease; the source releases the
+    request (the lease expired) and hands the same physical blocks to another
+    request; the receiver's generation check must now fail, although the block
+    ids it holds are valid and mapped again.  Mapping new blocks at the end of a
+    table keeps its stamp; copy-on-write replacing an entry does not."""
+    a = BlockAllocator(4, 4, free_order=[3, 1, 0, 2])
+    src = a.new_seq()
+    a.reserve(src, 8)
+    a.commit(src, 8)
+    stamp = a.lease(src)
+    table = a.table(src, 2)
+    assert table == [3, 1] and a.check(src, stamp)
+    a.reserve(src, 4)                 # grows into a third block: the first two entries are unchanged
+    a.commit(src, 4)
+    assert a.check(src, stamp) and a.table(src, 3)[:2] == table
+    a.release(src)                    # the lease expires at the source
+    assert not a.check(src, stamp)
+    other = a.new_seq()               # the id and the blocks go to another request
+    a.reserve(other, 16)
+    assert other == src and sorted(a.table(other, 4)) == [0, 1, 2, 3]
+    assert not a.check(src, stamp)    # same id, same block ids: still stale
+    assert a.check(other, a.lease(other))
+    # copy-on-write replacing an entry makes earlier stamps stale
+    b = BlockAllocator(8, 4)
+    x = b.new_seq()
+    b.reserve(x, 6)
+    b.commit(x, 6)
+    y = b.fork(x, 6)
+    st_y = b.lease(y)
+    assert b.reserve(y, 1) == [(1, 2)]
+    assert not b.check(y, st_y) and b.check(x, b.lease(x))
+    with pytest.raises(ValueError):
+        b.check(99, st_y)
