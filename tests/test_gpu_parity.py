@@ -20,8 +20,10 @@ from harness import (GpuCase, OracleCase, check_attention, dev_bits, dev_i32, fi
 pytestmark = pytest.mark.gpu
 
 
-def _run(kvc, w, layers=(0,), fill=0xFF, bytes_check=True, decode_layers=None):
-    """Load context, append, decode on the GPU and in the oracle; compare."""
+def _run(kvc, w, layers=(0,), fill=0xFF, bytes_check=True, decode_layers=None, fused=False):
+    """Load context, append, decode on the GPU and in the oracle; compare.
+    fused: the step as one kvc_decode_step launch (the call bench.py times),
+    else kvc_append followed by kvc_decode_attn."""
     g = GpuCase(kvc, w, fill_byte=fill)
     orc = OracleCase(w, fill_byte=fill)
     errs = []
@@ -29,7 +31,13 @@ def _run(kvc, w, layers=(0,), fill=0xFF, bytes_check=True, decode_layers=None):
         for layer in layers:
             ld = layer_data(w, layer)
             g.load_context(layer, ld)
-            out, lse = g.step(layer, ld)
+            if fused:
+                q, k_new, v_new = g.step_inputs(ld)
+                out = torch.empty((w.B, w.H_Q, w.d_h), dtype=torch.float32, device="cuda")
+                lse = torch.empty((w.B, w.H_Q), dtype=torch.float32, device="cuda")
+                kvc.kvc_decode_step(g.pool, layer, q, g.bt_dec, g.lens_pre, k_new, v_new, out, lse, scale=w.scale)
+            else:
+                out, lse = g.step(layer, ld)
             torch.cuda.synchronize()
             assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
             dec = decode_layers is None or layer in decode_layers
@@ -53,22 +61,67 @@ def test_tiny(kvc, seed):
     _run(kvc, synth.make_workload("tiny", seed=seed))
 
 
-def test_llama_gqa(kvc):
-    _run(kvc, synth.make_workload("llama_gqa", seed=0))
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_step", "append_then_attend"])
+def test_llama_gqa(kvc, fused):
+    _run(kvc, synth.make_workload("llama_gqa", seed=0), fused=fused)
 
 
 @pytest.mark.parametrize("name", ["sweep_hkv8_bf16", "sweep_hkv8_fp8", "sweep_hkv32_bf16", "sweep_hkv32_fp8",
                                   "sweep_hkv1_bf16", "sweep_hkv1_fp8", "sweep_hkv8_int4", "sweep_hkv1_int4",
                                   "sweep_hkv32_int4"])
 def test_sweep(kvc, name):
-    _run(kvc, synth.make_workload(name, seed=0))
+    """Full-size sweep workloads through the fused step, the call bench.py times."""
+    _run(kvc, synth.make_workload(name, seed=0), fused=True)
 
 
-def test_full_pool_every_layer(kvc):
-    """32 layers sharing one table: bytes of every layer bit-exact; attention of
-    four layers (first, last and two inside) against the oracle."""
+def test_full_pool_graph_replay(kvc):
+    """The 32-layer step of the 32 GiB pool exactly as bench.py times it: one
+    eager step (kernel set-up, workspace), then the 32 fused kvc_decode_step
+    launches captured in one CUDA graph and replayed into NaN-filled outputs.
+    Every layer's pool bytes bit-exact against the oracle's image; attention of
+    four layers (first, last and two inside) against the oracle.  Appending the
+    same rows at the same positions again stores the same bytes, so the eager
+    step and the replay leave one state."""
     w = synth.make_workload("full_pool", seed=0)
-    _run(kvc, w, layers=range(w.L), decode_layers={0, 7, 20, 31})
+    g = GpuCase(kvc, w, fill_byte=0xFF)
+    try:
+        ins, outs = [], []
+        for layer in range(w.L):
+            ld = layer_data(w, layer)
+            g.load_context(layer, ld)
+            ins.append(g.step_inputs(ld))
+            outs.append((torch.empty((w.B, w.H_Q, w.d_h), device="cuda"), torch.empty((w.B, w.H_Q), device="cuda")))
+            del ld
+        torch.cuda.synchronize()
+
+        def step():
+            for layer in range(w.L):
+                q, k_new, v_new = ins[layer]
+                kvc.kvc_decode_step(g.pool, layer, q, g.bt_dec, g.lens_pre, k_new, v_new, *outs[layer], scale=w.scale)
+
+        step()
+        torch.cuda.synchronize()
+        for o, l in outs:
+            o.fill_(float("nan"))
+            l.fill_(float("nan"))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+        orc = OracleCase(w, fill_byte=0xFF)
+        for layer in range(w.L):
+            ld = layer_data(w, layer)
+            dec = layer in (0, 7, 20, 31)
+            ref = orc.run_layer(ld, decode=dec)
+            n, first = first_mismatch(g.layer_bytes(layer), ref["image"].bytes)
+            assert n == 0, f"layer {layer}: {n} pool bytes differ, first at {first}"
+            if dec:
+                check_attention(outs[layer][0], outs[layer][1], ref["out"], ref["lse"], "bf16", f"full pool layer {layer}")
+            del ld, ref
+    finally:
+        g.close()
 
 
 def test_ragged_prefix_and_prefill_chunk(kvc):
@@ -109,11 +162,13 @@ def test_ragged_prefix_and_prefill_chunk(kvc):
 
 @pytest.mark.parametrize("case", ["ragged_prefix", "small", "fp8", "int4", "mqa"])
 def test_mixed_step_equals_step_then_prefill(kvc, case):
-    """kvc_mixed_step (a decode step and a prefill chunk in one launch) leaves
-    the pool bytes of kvc_decode_step followed by kvc_prefill_attn and gives
-    their outputs: bit-identical for bf16 pools (the same split plans), and
-    decode and prefill both within tolerance of the oracle.  The MQA case has no
-    mixed instance (32-head groups) and runs as two launches."""
+    """kvc_mixed_step (a decode step and a prefill chunk together) leaves the
+    pool bytes of kvc_decode_step followed by kvc_prefill_attn and gives their
+    outputs: bit-identical for bf16 pools (the same kernels and split plans),
+    and decode and prefill both within tolerance of the oracle.  e4m3 and int4
+    pools run it as one launch of the mixed kernel (fewer launches than the two
+    calls); bf16 pools run the decode launch with the tensor-memory prefill
+    kernel as its programmatic dependent (the same launches as the two calls)."""
     kw = {"ragged_prefix": {},
           "small": dict(B=6, shared=96, chunk=70, lo=16, hi=900),
           "fp8": dict(B=6, shared=96, chunk=70, lo=16, hi=900, dtype="fp8"),
@@ -151,8 +206,10 @@ def test_mixed_step_equals_step_then_prefill(kvc, case):
             g.close()
     n, first = first_mismatch(res[0][0], res[1][0])
     assert n == 0, f"{n} pool bytes differ, first at {first}"
-    if case != "mqa":
-        assert res[1][5] < res[0][5], "the mixed step should take fewer launches"
+    if w.dtype != "bf16":
+        assert res[1][5] < res[0][5], "the mixed kernel should take fewer launches"
+    else:
+        assert res[1][5] == res[0][5]
     if w.dtype == "bf16":
         for a, b in zip(res[0][1:5], res[1][1:5]):
             assert torch.equal(a, b)

@@ -2,10 +2,11 @@
 device memory during a decode step (memory pre-reserved by their own caching
 allocator, or loops that cannot afford cudaMalloc's device synchronisation).
 
-It must give the results of kvc_decode_attn, call after call, while its split
-partials live in the library's fixed per-device scratch array, and it must
-refuse a split batch whose partials would not fit that array.  Collected last
-so that a run stopping at its first failure has run every other test.
+It must allocate nothing, give the results of kvc_decode_attn call after call
+(its split partials live in the library's fixed per-device scratch array
+instead of the pool's workspace), agree with the oracle, and refuse a split
+batch whose partials would not fit that array.  Collected last so that a run
+stopping at its first failure has run every other test.
 """
 import os
 
@@ -14,44 +15,61 @@ import pytest
 import torch
 
 import synth
-from harness import TOL_LSE_REL, TOL_OUT, GpuCase, dev_i32, layer_data
+from harness import GpuCase, OracleCase, check_attention, layer_data
 
 pytestmark = pytest.mark.gpu
 
 SCRATCH_FLOATS = 2 << 20     # the array's documented size: 8 MiB
 
+# (dtype, H_KV, d_h, lens): GQA / MHA / MQA groups, bf16 / e4m3 / int4, both head widths,
+# split batches and one short batch that runs unsplit
+CASES = [("bf16", 8, 128, [5000, 3000, 17]), ("bf16", 8, 128, [700]), ("bf16", 1, 128, [4000, 33]),
+         ("bf16", 32, 128, [2500, 100]), ("bf16", 8, 64, [3000, 9]), ("bf16", 8, 128, [40, 3]),
+         ("fp8", 8, 128, [5000, 3000, 17]), ("fp8", 1, 128, [2000, 600]), ("fp8", 32, 128, [1800, 5]),
+         ("int4", 8, 128, [4100, 250]), ("int4", 1, 128, [3000, 64])]
 
-def _close(a_out, a_lse, b_out, b_lse, dtype):
-    err_o = (a_out - b_out).abs().max().item()
-    fin = torch.isfinite(b_lse)
-    assert torch.equal(torch.isfinite(a_lse), fin)
-    err_l = ((a_lse[fin] - b_lse[fin]).abs() / b_lse[fin].abs().clamp(min=1.0)).max().item()
-    assert err_o <= TOL_OUT[dtype] and err_l <= TOL_LSE_REL, (err_o, err_l)
 
-
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
-@pytest.mark.parametrize("lens", [[5000, 3000, 17], [700]])
-def test_noalloc_matches_decode_attn_twice(kvc, dtype, lens):
-    """Two calls in a row (the second with new queries, so stale scratch from the
-    first cannot pass for a result) against kvc_decode_attn."""
-    w = synth.make_workload("custom", B=len(lens), H_Q=32, H_KV=8, d_h=128, lens=lens, dtype=dtype, seed=3)
+@pytest.mark.parametrize("dtype,H_KV,d_h,lens", CASES,
+                         ids=[f"{c[0]}-hkv{c[1]}-d{c[2]}-{'x'.join(map(str, c[3]))}" for c in CASES])
+def test_noalloc_allocates_nothing_and_matches(kvc, dtype, H_KV, d_h, lens):
+    """On a fresh pool (its workspace never sized by kvc_decode_attn): one warm-up
+    call, then two calls in a row (the second with new queries, so stale scratch
+    cannot pass for a result) with the device's free memory unchanged and one or
+    two launches per call; each against the oracle, then against
+    kvc_decode_attn (same kernels, partials elsewhere: rounding-level agreement)."""
+    w = synth.make_workload("custom", B=len(lens), H_Q=32, H_KV=H_KV, d_h=d_h, lens=lens, dtype=dtype, seed=3)
     g = GpuCase(kvc, w)
     try:
         ld = layer_data(w, 0)
         g.load_context(0, ld)
         q, k_new, v_new = g.step_inputs(ld)
         kvc.kvc_append(g.pool, 0, g.bt_dec, g.lens_pre, k_new, v_new)
-        for call in range(2):
-            qc = q if call == 0 else (q.float() * -0.5).to(torch.bfloat16)
-            ref_o = torch.empty((w.B, w.H_Q, w.d_h), device="cuda")
-            ref_l = torch.empty((w.B, w.H_Q), device="cuda")
-            kvc.kvc_decode_attn(g.pool, 0, qc, g.bt_dec, g.lens_post, ref_o, ref_l, scale=w.scale)
-            out = torch.full((w.B, w.H_Q, w.d_h), float("nan"), device="cuda")
-            lse = torch.full((w.B, w.H_Q), float("nan"), device="cuda")
-            kvc.kvc_decode_attn_noalloc(g.pool, 0, qc, g.bt_dec, g.lens_post, out, lse, scale=w.scale)
+        qs = [q, (q.float() * -0.5).to(torch.bfloat16)]
+        outs = [torch.full((w.B, w.H_Q, w.d_h), float("nan"), device="cuda") for _ in qs]
+        lses = [torch.full((w.B, w.H_Q), float("nan"), device="cuda") for _ in qs]
+        ref_o = torch.empty((w.B, w.H_Q, w.d_h), device="cuda")
+        ref_l = torch.empty((w.B, w.H_Q), device="cuda")
+        kvc.kvc_decode_attn_noalloc(g.pool, 0, qs[0], g.bt_dec, g.lens_post, outs[0], lses[0], scale=w.scale)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        n0 = kvc.kvc_launch_count()
+        for i in range(2):
+            kvc.kvc_decode_attn_noalloc(g.pool, 0, qs[i], g.bt_dec, g.lens_post, outs[i], lses[i], scale=w.scale)
+        torch.cuda.synchronize()
+        launches = kvc.kvc_launch_count() - n0
+        assert torch.cuda.mem_get_info()[0] == free0, "device memory changed across allocation-free calls"
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+        assert launches in (2, 4), launches       # attention (+ the split merge) per call
+
+        orc = OracleCase(w).run_layer(ld, image=False)
+        check_attention(outs[0], lses[0], orc["out"], orc["lse"], dtype, "noalloc vs oracle")
+        for i in range(2):
+            kvc.kvc_decode_attn(g.pool, 0, qs[i], g.bt_dec, g.lens_post, ref_o, ref_l, scale=w.scale)
             torch.cuda.synchronize()
-            assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
-            _close(out, lse, ref_o, ref_l, dtype)
+            assert torch.equal(torch.isfinite(lses[i]), torch.isfinite(ref_l))
+            fin = torch.isfinite(ref_l)
+            assert float((outs[i] - ref_o).abs().max()) <= 1e-5
+            assert float((lses[i][fin] - ref_l[fin]).abs().max()) <= 1e-5
     finally:
         g.close()
 
