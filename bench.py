@@ -126,7 +126,7 @@ def peaks():
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, device_index: int):
         self.dev = device_index
@@ -160,17 +160,22 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             p = [x.strip() for x in line.split(",")]
-            if len(p) >= 9:
+            if len(p) >= 10:
                 rows.append(p)
         os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_under_load": 0}
+        num = lambda x: x.replace(".", "").isdigit()
+        busy = [r for r in rows if num(r[9]) and float(r[9]) >= 50]   # samples while the GPU was busy
+        load = busy or rows
+        sm = [float(r[1]) for r in load if num(r[1])]
+        mx = [float(r[2]) for r in rows if num(r[2])]
+        pw = [float(r[3]) for r in load if num(r[3])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        reasons = sorted({n for r in load for n, v in zip(names, r[5:9]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(busy),
+                "power_w_max": max(pw) if pw else None}
 
 
 # ---------------------------------------------------------------- oracle (CPU) side
@@ -270,17 +275,190 @@ def weak_scaling_value(bytes_per_rank: int, world: int, max_ms: float) -> float:
     return bytes_per_rank * world / (max_ms * 1e-3) / 1e9
 
 
+def step_stats(ms):
+    """Mean, median and 90th percentile of per-step times (ms)."""
+    a = np.asarray(ms, dtype=np.float64)
+    return {"mean": float(a.mean()), "median": float(np.median(a)), "p90": float(np.percentile(a, 90)),
+            "steps": int(a.size)}
+
+
+# ---------------------------------------------------------------- the other target workloads
+# The configurations beside the headline one, each timed in its own region: the
+# 32 GiB pool (32 layers, one CUDA graph per step), the e4m3 and bf16 GQA sweep
+# points, and MQA.  Their pools are filled on the device from a seeded
+# generator (N(0,1) rounded to bf16, then stored as each pool stores it), so a
+# 32 GiB pool is ready in seconds; the block tables and lengths are the
+# workload's own.
+EXTRA_WORKLOADS = "full_pool,sweep_hkv8_fp8,sweep_hkv8_bf16,sweep_hkv1_bf16,prefill_chunk"
+EXTRA_SECONDS = 1.5
+
+
+def fill_on_device(kvc, g, w, layer, gen):
+    """Write layer `layer`'s context through kvc_write_tokens from N(0,1) bf16 values drawn on the device."""
+    import torch
+    from harness import dev_i32
+    units = ([(0, 0, w.shared_prefix)] if w.shared_prefix else []) + \
+        [(b, w.shared_prefix, int(w.lens_pre[b])) for b in range(w.B)]
+    units = [u for u in units if u[2] > u[1]]
+    if not units:
+        return
+    rows = np.array([u[0] for u in units], np.int32)
+    start = np.array([u[1] for u in units], np.int32)
+    n = np.array([u[2] - u[1] for u in units], np.int64)
+    cu = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    shape = (int(cu[-1]), w.H_KV, w.d_h)
+    k = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    v = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    if w.dtype != "bf16":
+        kvc.kvc_calibrate_scales(g.pool, layer, k, v)
+    kvc.kvc_write_tokens(g.pool, layer, dev_i32(w.block_tables[rows]), dev_i32(start), dev_i32(cu), k, v,
+                         max_tokens=int(n.max()))
+    del k, v
+
+
+def bench_prefill_chunk(kvc, seed, local, seconds=EXTRA_SECONDS):
+    """The ragged workload's prefill chunk alone: 600 queries (positions 1 200 .. 1 799)
+    attending causally over the row's 1 200-token shared prefix and themselves
+    (kvc_prefill_attn), as TFLOP/s of scores and value mixture against the bf16 peak."""
+    import torch
+    import synth
+    from harness import GpuCase, dev_i32
+    w = synth.make_workload("ragged_prefix", seed=seed)
+    pf = w.prefill
+    g = GpuCase(kvc, w, fill_byte=0)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    try:
+        row = dev_i32(w.block_tables[pf.seq])
+        shape = (pf.total, w.H_KV, w.d_h)
+        k = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+        v = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+        kvc.kvc_write_tokens(g.pool, 0, row[None], dev_i32([0]), dev_i32([0, pf.total]), k, v)
+        q = torch.randn((pf.n_q, w.H_Q, w.d_h), generator=gen, device="cuda").to(torch.bfloat16)
+        out = torch.empty((pf.n_q, w.H_Q, w.d_h), device="cuda")
+        lse = torch.empty((pf.n_q, w.H_Q), device="cuda")
+        stream = torch.cuda.current_stream()
+        run = lambda: kvc.kvc_prefill_attn(g.pool, 0, q, row, pf.q_start, out, lse, scale=w.scale)
+        for _ in range(5):
+            run()
+        torch.cuda.synchronize()
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(5):
+            run()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        n = int(min(20000, max(20, seconds / (t0.elapsed_time(t1) / 5 * 1e-3))))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with ClockSampler(local) as clk:
+            torch.cuda.synchronize()
+            for a, b in ev:
+                a.record(stream)
+                run()
+                b.record(stream)
+            torch.cuda.synchronize()
+        st = step_stats([a.elapsed_time(b) for a, b in ev])
+        flops = prefill_flops(w)
+        tf = flops / (st["mean"] * 1e-3) / 1e12
+        peak = tensor_peak()
+        return {"queries": pf.n_q, "q_start": pf.q_start, "H_Q": w.H_Q, "H_KV": w.H_KV, "d_h": w.d_h,
+                "flops": flops, "ms": st["mean"], "ms_median": st["median"], "ms_p90": st["p90"], "launches": st["steps"],
+                "tflops": tf, "peak_tflops": peak[0], "peak_source": peak[1], "tensor_frac": tf / peak[0],
+                "clocks": clk.summary(),
+                "data": "synthetic: N(0,1) bf16 drawn on the device (seeded)"}
+    finally:
+        g.close()
+
+
+def tensor_peak():
+    """bf16 dense tensor peak (burst: the chunk is timed on its own), TFLOP/s."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(d["bf16_tflops"]), "measured bf16_tflops (burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def bench_extra(kvc, name, seed, hbm, local, seconds=EXTRA_SECONDS):
+    """Time one more workload's step (fused decode step per layer; a CUDA graph when multi-layer)."""
+    import torch
+    import synth
+    from harness import GpuCase
+    w = synth.make_workload(name, seed=seed)
+    g = GpuCase(kvc, w, fill_byte=0)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    try:
+        ins = []
+        for layer in range(w.L):
+            fill_on_device(kvc, g, w, layer, gen)
+            mk = lambda *shape: torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+            ins.append((mk(w.B, w.H_Q, w.d_h), mk(w.B, w.H_KV, w.d_h), mk(w.B, w.H_KV, w.d_h),
+                        torch.empty((w.B, w.H_Q, w.d_h), device="cuda"), torch.empty((w.B, w.H_Q), device="cuda")))
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+
+        def step():
+            for layer in range(w.L):
+                q, kn, vn, o, l_ = ins[layer]
+                kvc.kvc_decode_step(g.pool, layer, q, g.bt_dec, g.lens_pre, kn, vn, o, l_, scale=w.scale)
+
+        for _ in range(5):
+            step()
+        torch.cuda.synchronize()
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+        run = step
+        if w.L > 1:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step()
+            graph.replay()
+            torch.cuda.synchronize()
+            run = graph.replay
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(3):
+            run()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        n = int(min(20000, max(20, seconds / (t0.elapsed_time(t1) / 3 * 1e-3))))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with ClockSampler(local) as clk:
+            torch.cuda.synchronize()
+            for a, b in ev:
+                a.record(stream)
+                run()
+                b.record(stream)
+            torch.cuda.synchronize()
+        assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
+        st = step_stats([a.elapsed_time(b) for a, b in ev])
+        sb = step_bytes(w)
+        launch_ms = st["mean"] / w.L
+        achieved = sb["total"] / (launch_ms * 1e-3) / 1e9
+        return {"kv_dtype": w.dtype, "B": w.B, "H_Q": w.H_Q, "H_KV": w.H_KV, "d_h": w.d_h, "layers": w.L,
+                "attended": int(w.lens_post.max()), "ms_per_step": st["mean"], "ms_per_step_median": st["median"],
+                "ms_per_step_p90": st["p90"], "steps": st["steps"], "GB_per_s": sb["total"] * w.L / (st["mean"] * 1e-3) / 1e9,
+                "tokens_per_s": w.B / (st["mean"] * 1e-3), "launch_ms": launch_ms, "roofline_frac": achieved / hbm,
+                "algorithmic_bytes_per_launch": sb["total"], "clocks": clk.summary(),
+                "data": "synthetic: N(0,1) bf16 drawn on the device (seeded), stored as the pool stores it"}
+    finally:
+        g.close()
+
+
 # ---------------------------------------------------------------- GPU side
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=12000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="kvc", choices=["kvc", "reference"])
     ap.add_argument("--workload", default="llama_gqa")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra", default=EXTRA_WORKLOADS,
+                    help="comma-separated workloads timed after the headline one (their own regions); '' for none")
     args = ap.parse_args()
 
     import synth
@@ -392,7 +570,8 @@ def main():
         barrier()
     launches = kvc.kvc_launch_count() - launches0 if graph is None else K * L
     ms = t_start.elapsed_time(t_end) / K
-    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_a, ev_b)])) / L    # per launch
+    per_step = step_stats([a.elapsed_time(b) for a, b in zip(ev_a, ev_b)])
+    attn_ms = per_step["mean"] / L    # per launch
     clocks = clk.summary()
     assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
 
@@ -496,11 +675,18 @@ def main():
         rate, dt, k, desc, cores = oracle_sample(w, ld, args.cpu_budget)
         cpu = {"value": rate / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{desc}; {dt:.1f} s"}
+    extra = {}
+    if rank == 0 and args.extra:
+        g.close()                    # the headline pool's memory goes back before the next pools
+        for name in [x for x in args.extra.split(",") if x and x != w.name]:
+            extra[name] = (bench_prefill_chunk(kvc, args.seed + rank, local) if name == "prefill_chunk"
+                           else bench_extra(kvc, name, args.seed + rank, hbm, local))
     if rank == 0:
         splits_note = (f"{L} launches per step (one per layer)" + (", replayed as one CUDA graph" if graph else "")
                        if launches == K * L else f"{launches / K:.1f} launches per step")
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "ms_per_step": ms, "ms_per_step_median": per_step["median"], "ms_per_step_p90": per_step["p90"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": w.dtype, "data": "synthetic", "config": config_dict(w),
                 "tokens_per_s": w.B * world / (ms * 1e-3),
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -514,7 +700,7 @@ def main():
                              "algorithmic_bytes_per_launch": sb1["total"], "launch_ms": attn_ms,
                              "note": splits_note},
                 "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
-                "step_bytes": sb}
+                "step_bytes": sb, "configs": extra}
         if pf is not None:   # the chunk's causal attention rides in the same launch
             line["prefill"] = {"queries": pf.n_q, "q_start": pf.q_start, "flops_per_step": prefill_flops(w) * L,
                                "tflops_in_step": prefill_flops(w) * L / (ms * 1e-3) / 1e12}
