@@ -12,10 +12,13 @@
 // dependent mma chains leave HBM idle.  Here one thread issues 128-token MMAs
 // whose accumulators live in TMEM, and the registers hold one token's scores.
 //
-// CTA = one split of (b, h); 192 threads in three roles:
-//   warp 4      TMA producer: per 128-token tile, the 8 blocks' key rows and
-//               value rows (16-row boxes, 128-byte swizzle) into a ring of 3
-//               64 KiB stages: keys [2 bands][128 tokens][128 B], then values.
+// CTA = one split of (b, h); 224 threads in four roles:
+//   warps 4, 6  TMA producers, one for keys and one for values: per 128-token
+//               tile, the 8 blocks' key rows (or value rows) as 16-row boxes
+//               (128-byte swizzle) into a ring of 3 slots of 32 KiB
+//               ([2 bands][128 tokens][128 B]).  A key slot is released as soon
+//               as the tile's score MMA has completed and a value slot when its
+//               value MMA has: keys run ahead, values are fetched for later.
 //   warp 5      MMA issuer (one lane):
 //                 S^T[128 tok x G]  = K[128 x 128] . Q^T     (K-major A and B)
 //                 O^T[128 ch x 64] += V^T[128 x 128] . P^T    (MN-major A and B)
@@ -44,15 +47,16 @@ namespace kvc {
 
 constexpr int kTcTok = 128;                         // tokens per tile: the MMA's M
 constexpr int kTcBlocks = kTcTok / kBS;             // 8 blocks per tile
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;
 constexpr int kTcRing = 3;
 constexpr int kTcBand = kTcTok * 128;               // one 128-byte column band of 128 rows
-constexpr int kTcStage = 4 * kTcBand;               // keys (2 bands) then values (2 bands), d_h 128 bf16
-constexpr int kTcQ = kTcRing * kTcStage;            // Q: 2 bands x 32 head rows x 128 B
+constexpr int kTcSlot = 2 * kTcBand;                // the keys (or the values) of a tile: 2 bands, d_h 128 bf16
+constexpr int kTcV = kTcRing * kTcSlot;             // key slots first, then value slots
+constexpr int kTcQ = 2 * kTcRing * kTcSlot;         // Q: 2 bands x 32 head rows x 128 B
 constexpr int kTcP = kTcQ + 2 * 32 * 128;           // P^T: 128 token rows x 64 bf16 heads
 constexpr int kTcBars = kTcP + kTcTok * 128;
-// barriers: full[R], kvfree[R], s_full[2], s_free[2], p_full, pv_done, q_ready
-constexpr int kTcNumBars = 2 * kTcRing + 7;
+// barriers: kfull[R], kfree[R], vfull[R], vfree[R], s_full[2], s_free[2], p_full, pv_done, q_ready
+constexpr int kTcNumBars = 4 * kTcRing + 7;
 // float [4][32] reductions, then msh[32], ash[32], lsh[32] (16-byte aligned: read as float4)
 constexpr int kTcRed = kTcBars + ((kTcNumBars * 8 + 15) & ~15);
 constexpr int kTcTmemSlot = kTcRed + (4 * 32 + 3 * 32) * 4;
@@ -138,23 +142,25 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bars = sbase + kTcBars;
-    auto full_bar = [&](int s) { return bars + 8u * s; };
-    auto kvfree_bar = [&](int s) { return bars + 8u * (kTcRing + s); };
-    auto sfull_bar = [&](int sb) { return bars + 8u * (2 * kTcRing + sb); };
-    auto sfree_bar = [&](int sb) { return bars + 8u * (2 * kTcRing + 2 + sb); };
-    const uint32_t pfull_bar = bars + 8u * (2 * kTcRing + 4);
-    const uint32_t pvdone_bar = bars + 8u * (2 * kTcRing + 5);
-    const uint32_t qready_bar = bars + 8u * (2 * kTcRing + 6);
+    // kv = 0: key slots, 1: value slots
+    auto full_bar = [&](int kv, int s) { return bars + 8u * (2 * kv * kTcRing + s); };
+    auto free_bar = [&](int kv, int s) { return bars + 8u * (2 * kv * kTcRing + kTcRing + s); };
+    auto sfull_bar = [&](int sb) { return bars + 8u * (4 * kTcRing + sb); };
+    auto sfree_bar = [&](int sb) { return bars + 8u * (4 * kTcRing + 2 + sb); };
+    const uint32_t pfull_bar = bars + 8u * (4 * kTcRing + 4);
+    const uint32_t pvdone_bar = bars + 8u * (4 * kTcRing + 5);
+    const uint32_t qready_bar = bars + 8u * (4 * kTcRing + 6);
     float *red = reinterpret_cast<float *>(smem + kTcRed);   // [4][32]
     float *msh = red + 128, *ash = msh + 32, *lsh = ash + 32;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTcTmemSlot);
 
     // ---- set-up: barriers, TMEM, q rows (K-major B operand), reference maxima
     if (tid == 0) {
-        for (int s = 0; s < kTcRing; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(kvfree_bar(s), 1);
-        }
+        for (int kv = 0; kv < 2; ++kv)
+            for (int s = 0; s < kTcRing; ++s) {
+                mbar_init(full_bar(kv, s), 1);
+                mbar_init(free_bar(kv, s), 1);
+            }
         for (int sb = 0; sb < 2; ++sb) {
             mbar_init(sfull_bar(sb), 1);
             mbar_init(sfree_bar(sb), 128);
@@ -191,8 +197,9 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
     const int bbase = tile0 * kTcBlocks;
     auto load_entry = [&](int rel) -> int32_t { return bbase + rel < nblk ? __ldg(bt_row + bbase + rel) : -1; };
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == 4 || warp == 6) {
+        // ------------------------------------------------------------ TMA producers (4: keys, 6: values)
+        const int kv = warp == 6 ? 1 : 0;
         int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
         int j = 0;
         for (; j < nt; ++j) {
@@ -202,7 +209,7 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
             }
             const int s = j % kTcRing;
             if (j >= kTcRing) {
-                const bool ok = mbar_wait_bounded(kvfree_bar(s), static_cast<uint32_t>(((j / kTcRing) - 1) & 1));
+                const bool ok = mbar_wait_bounded(free_bar(kv, s), static_cast<uint32_t>(((j / kTcRing) - 1) & 1));
                 if (!__all_sync(kFull, ok)) {
                     timed_out = true;
                     break;
@@ -212,38 +219,37 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
             const int blk = bbase + j * kTcBlocks + lane;
             const bool in = lane < kTcBlocks && blk < nblk;
             const bool v = in && e >= 0 && static_cast<int64_t>(e) < p.N;
-            if (in && !v) atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
+            if (kv == 0 && in && !v) atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
             const uint32_t mask = __ballot_sync(kFull, v);
             if (lane == 0) {
-                if (mask == 0u) mbar_arrive(full_bar(s));
-                else mbar_arrive_expect_tx(full_bar(s), static_cast<uint32_t>(__popc(mask)) * 4u * (kBS * 128u));
+                if (mask == 0u) mbar_arrive(full_bar(kv, s));
+                else mbar_arrive_expect_tx(full_bar(kv, s), static_cast<uint32_t>(__popc(mask)) * 2u * (kBS * 128u));
             }
             __syncwarp();
             if (v) {
-                const int32_t y = static_cast<int32_t>(((row_layer + e) * p.H_KV + h) * (2 * kBS));
-                const uint32_t st = sbase + s * kTcStage + lane * (kBS * 128);
-#pragma unroll
-                for (int band = 0; band < 2; ++band) {
-                    tma_load_2d(st + band * kTcBand, &tmap16, full_bar(s), band * 64, y);                    // keys
-                    tma_load_2d(st + 2 * kTcBand + band * kTcBand, &tmap16, full_bar(s), band * 64, y + kBS); // values
-                }
+                const int32_t y = static_cast<int32_t>(((row_layer + e) * p.H_KV + h) * (2 * kBS) + kv * kBS);
+                const uint32_t st = sbase + kv * kTcV + s * kTcSlot + lane * (kBS * 128);
+                tma_load_2d(st, &tmap16, full_bar(kv, s), 0, y);
+                tma_load_2d(st + kTcBand, &tmap16, full_bar(kv, s), 64, y);
             }
         }
-        // before the CTA exits: the copies of the last stages have landed and their releases
+        // before the CTA exits: the copies of the last slots have landed and their releases
         // (tcgen05 commits, which arrive asynchronously) are in; both are immediate unless a
         // wait somewhere expired
         if (lane == 0)
             for (int jj = max(0, j - kTcRing); jj < j; ++jj) {
-                (void)mbar_wait_bounded(full_bar(jj % kTcRing), static_cast<uint32_t>((jj / kTcRing) & 1), 100000000ull);
-                (void)mbar_wait_bounded(kvfree_bar(jj % kTcRing), static_cast<uint32_t>((jj / kTcRing) & 1),
+                (void)mbar_wait_bounded(full_bar(kv, jj % kTcRing), static_cast<uint32_t>((jj / kTcRing) & 1),
+                                        100000000ull);
+                (void)mbar_wait_bounded(free_bar(kv, jj % kTcRing), static_cast<uint32_t>((jj / kTcRing) & 1),
                                         100000000ull);
             }
         __syncwarp();
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
-        // Issues whichever MMA is ready: the value MMA of tile jp once its weights are in
-        // shared memory (it releases the tile's stage), the score MMA of tile jq once its keys
-        // have landed and its score buffer is free; neither waits behind the other.
+        // Issues whichever MMA is ready: the score MMA of tile jq once its keys have landed and
+        // its score buffer is free (it releases the key slot), the value MMA of tile jp once its
+        // weights are in shared memory and its values have landed (it releases the value slot).
+        // Barriers are tested without blocking.
         constexpr uint32_t idesc_qk = tc_idesc_f16(128, G, true, false, false);
         constexpr uint32_t idesc_pv = tc_idesc_f16(128, 64, true, true, true);
         int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
@@ -253,22 +259,53 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
         };
         const uint64_t desc_q = tc_smem_desc(sbase + kTcQ, 16, 1024, kSwizzle128B);
         const uint64_t desc_p = tc_smem_desc(sbase + kTcP, kTcBand, 1024, kSwizzle128B);
+        // per tile in flight (3 at most between score and value MMA): its valid blocks, 8 bits each
+        uint32_t vmasks = 0u;
+        int32_t append_phys = -1;   // the block receiving the fused append (the sequence's last tile)
         bool q_ready = false;
         int jq = 0, jp = 0;
         uint64_t idle_since = 0;
         uint32_t idle = 0;
         while (jp < nt) {
             bool progressed = false;
-            if (jp < jq && ready(pfull_bar, static_cast<uint32_t>(jp & 1))) {
+            if (jp < jq && ready(pfull_bar, static_cast<uint32_t>(jp & 1)) &&
+                ready(full_bar(1, jp % kTcRing), static_cast<uint32_t>((jp / kTcRing) & 1))) {
+                const uint32_t vst = sbase + kTcV + (jp % kTcRing) * kTcSlot;
+                // positions that must contribute nothing: past the sequence end, or in a block whose
+                // table entry is bad; their value rows are zeroed (their weights are 0; 0 * NaN is not)
+                const int tok0 = (tile0 + jp) * kTcTok;
+                const uint32_t vmask = (vmasks >> (8 * (jp % kTcRing))) & 0xFFu;
+                bool fix = tok0 + kTcTok > len || vmask != 0xFFu;
+                if (fix) {
+                    for (int i = lane; i < kTcTok * 16; i += 32) {
+                        const int row = i >> 4, c = i & 15, tok = tok0 + row;
+                        if (tok >= len || !(vmask >> (row >> 4) & 1u))
+                            sts128_zero(vst + (c >> 3) * kTcBand + sw128(row, c & 7));
+                    }
+                }
+                // fused append: the step's own value row, into the pool and into the slot
+                if (p.k_new && tok0 <= len - 1 && len - 1 < tok0 + kTcTok && append_phys >= 0) {
+                    fix = true;
+                    if (lane < 16) {
+                        const int row = len - 1 - tok0, c = lane;
+                        const uint4 val = *reinterpret_cast<const uint4 *>(
+                            p.v_new + (static_cast<size_t>(b) * p.H_KV + h) * D + c * 8);
+                        const int64_t el =
+                            ((((row_layer + append_phys) * p.H_KV + h) * 2 + 1) * kBS + (row & 15)) * D + c * 8;
+                        *reinterpret_cast<uint4 *>(p.pool + el * 2) = val;
+                        sts128(vst + (c >> 3) * kTcBand + sw128(row, c & 7), val);
+                    }
+                }
+                if (fix) fence_proxy_async_smem();   // zeros / the appended row, before the tensor cores read them
+                __syncwarp();
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint64_t a0 = tc_smem_desc(sbase + (jp % kTcRing) * kTcStage + 2 * kTcBand, kTcBand, 1024,
-                                                     kSwizzle128B);
+                    const uint64_t a0 = tc_smem_desc(vst, kTcBand, 1024, kSwizzle128B);
 #pragma unroll
                     for (int kk = 0; kk < kTcTok / 16; ++kk)   // 16 tokens (2048 bytes of rows) per MMA
                         tc_mma_f16(tm_o, tc_desc_advance(a0, kk * 2048), tc_desc_advance(desc_p, kk * 2048), idesc_pv,
                                    (jp > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(kvfree_bar(jp % kTcRing));
+                    tc_commit(free_bar(1, jp % kTcRing));
                     tc_commit(pvdone_bar);
                 }
                 __syncwarp();
@@ -276,50 +313,50 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
                 progressed = true;
             }
             if (!q_ready) q_ready = ready(qready_bar, 0u);
-            if (jq < nt && q_ready && ready(full_bar(jq % kTcRing), static_cast<uint32_t>((jq / kTcRing) & 1)) &&
+            if (jq < nt && jq < jp + kTcRing && q_ready &&
+                ready(full_bar(0, jq % kTcRing), static_cast<uint32_t>((jq / kTcRing) & 1)) &&
                 (jq < 2 || ready(sfree_bar(jq & 1), static_cast<uint32_t>(((jq - 2) >> 1) & 1)))) {
                 if (jq > 0 && (jq & 3) == 0) {
                     ecur = enext;
                     enext = load_entry((jq / 4 + 1) * 32 + lane);
                 }
-                const uint32_t st = sbase + (jq % kTcRing) * kTcStage;
-                // positions that must contribute nothing: past the sequence end, or in a block whose
-                // table entry is bad; their value rows are zeroed (their scores are masked)
+                const uint32_t kst = sbase + (jq % kTcRing) * kTcSlot;
                 const int tok0 = (tile0 + jq) * kTcTok;
                 const int32_t e = __shfl_sync(kFull, ecur, (jq & 3) * kTcBlocks + (lane & 7));
                 const bool bv = bbase + jq * kTcBlocks + (lane & 7) < nblk && e >= 0 && static_cast<int64_t>(e) < p.N;
                 const uint32_t vmask = __ballot_sync(kFull, bv) & 0xFFu;
-                if (tok0 + kTcTok > len || vmask != 0xFFu) {
-                    for (int i = lane; i < kTcTok * 16; i += 32) {
-                        const int row = i >> 4, c = i & 15, tok = tok0 + row;
-                        if (tok >= len || !(vmask >> (row >> 4) & 1u))
-                            sts128_zero(st + 2 * kTcBand + (c >> 3) * kTcBand + sw128(row, c & 7));
-                    }
-                }
-                // fused append: the step's own key / value row, into the pool and into the stage
+                vmasks = (vmasks & ~(0xFFu << (8 * (jq % kTcRing)))) | (vmask << (8 * (jq % kTcRing)));
+                // fused append: the step's own key row, into the pool and into the slot (its value row
+                // goes in at the value MMA)
+                bool wrote = false;
                 if (p.k_new && tok0 <= len - 1 && len - 1 < tok0 + kTcTok) {
                     const int row = len - 1 - tok0;
                     const int32_t phys = __shfl_sync(kFull, e, row >> 4);
                     if ((vmask >> (row >> 4)) & 1u) {
-                        const int kv = lane >> 4, c = lane & 15;
-                        const uint4 val = *reinterpret_cast<const uint4 *>(
-                            (kv ? p.v_new : p.k_new) + (static_cast<size_t>(b) * p.H_KV + h) * D + c * 8);
-                        const int64_t el = ((((row_layer + phys) * p.H_KV + h) * 2 + kv) * kBS + (row & 15)) * D + c * 8;
-                        *reinterpret_cast<uint4 *>(p.pool + el * 2) = val;
-                        sts128(st + kv * 2 * kTcBand + (c >> 3) * kTcBand + sw128(row, c & 7), val);
+                        append_phys = phys;
+                        wrote = true;
+                        if (lane < 16) {
+                            const int c = lane;
+                            const uint4 val = *reinterpret_cast<const uint4 *>(
+                                p.k_new + (static_cast<size_t>(b) * p.H_KV + h) * D + c * 8);
+                            const int64_t el = ((((row_layer + phys) * p.H_KV + h) * 2) * kBS + (row & 15)) * D + c * 8;
+                            *reinterpret_cast<uint4 *>(p.pool + el * 2) = val;
+                            sts128(kst + (c >> 3) * kTcBand + sw128(row, c & 7), val);
+                        }
                     }
                 }
-                if (tok0 + kTcTok > len || vmask != 0xFFu) fence_proxy_async_smem();   // zeros / the appended row
+                if (wrote) fence_proxy_async_smem();
                 __syncwarp();
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint64_t a0 = tc_smem_desc(st, 16, 1024, kSwizzle128B);
+                    const uint64_t a0 = tc_smem_desc(kst, 16, 1024, kSwizzle128B);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)   // 16 channels (32 bytes) per MMA, 4 per 128-byte band
                         tc_mma_f16(tmem + (jq & 1) * 32, tc_desc_advance(a0, (kk >> 2) * kTcBand + (kk & 3) * 32),
                                    tc_desc_advance(desc_q, (kk >> 2) * (32 * 128) + (kk & 3) * 32), idesc_qk,
                                    kk > 0 ? 1u : 0u);
                     tc_commit(sfull_bar(jq & 1));
+                    tc_commit(free_bar(0, jq % kTcRing));
                 }
                 __syncwarp();
                 ++jq;
