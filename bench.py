@@ -78,7 +78,23 @@ def prefill_flops(w) -> int:
 KERNEL_SOURCES = {
     "decode": ["kvc_decode.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_attn.cu"],
     "mixed": ["kvc_decode.cuh", "kvc_prefill.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_attn.cu"],
+    "decode_tc": ["kvc_decode_tc.cuh", "kvc_tc.cuh", "kvc_decode.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_attn.cu"],
+    "prefill_tc": ["kvc_prefill_tc.cuh", "kvc_decode_tc.cuh", "kvc_tc.cuh", "kvc_decode.cuh", "kvc_ptx.cuh",
+                   "kvc_internal.h", "kvc_attn.cu"],
 }
+
+
+def step_kernel(w) -> str:
+    """The kernels the library picks for this workload's step (the same rule as its dispatch)."""
+    tc = os.environ.get("KVC_TC", "1")[:1] != "0" and w.dtype == "bf16" and w.bs == 16
+    if w.prefill is not None:
+        if tc:
+            return ("kvc_mixed_step: decode_kernel with fused append, then prefill_tc_kernel (tcgen05) as its "
+                    "programmatic dependent launch")
+        return "mixed_kernel: decode step with fused append and the prefill chunk in one launch (kvc_mixed_step)"
+    if tc and w.H_Q == 32 * w.H_KV and w.d_h == 128:
+        return "decode_tc_kernel (tcgen05, TMEM) with fused append, then merge_kernel (kvc_decode_step)"
+    return "decode_kernel with fused append (kvc_decode_step)"
 
 
 def source_digest(kind: str = "decode", read=None) -> str:
@@ -275,11 +291,39 @@ def weak_scaling_value(bytes_per_rank: int, world: int, max_ms: float) -> float:
     return bytes_per_rank * world / (max_ms * 1e-3) / 1e9
 
 
-def step_stats(ms):
+def step_stats(ms, steps=None):
     """Mean, median and 90th percentile of per-step times (ms)."""
     a = np.asarray(ms, dtype=np.float64)
     return {"mean": float(a.mean()), "median": float(np.median(a)), "p90": float(np.percentile(a, 90)),
-            "steps": int(a.size)}
+            "steps": int(a.size) if steps is None else int(steps)}
+
+
+STEP_GROUPS = 100   # events bracket groups of steps, never single steps
+
+
+def time_steps(run, K: int, stream):
+    """Time K back-to-back calls of run() on `stream`.
+
+    Events are recorded only between groups of ceil(K / STEP_GROUPS) calls: an
+    event between two steps would hold the next step's launch until the step
+    before it has drained, which the library's programmatic dependent launches
+    otherwise overlap (as in an untimed decode loop).  Returns (mean ms per step
+    over all K steps, step_stats over the groups' per-step times)."""
+    import torch
+    chunk = max(1, -(-K // STEP_GROUPS))
+    bounds = list(range(0, K, chunk)) + [K]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in bounds]
+    for j in range(len(bounds) - 1):
+        ev[j].record(stream)
+        for _ in range(bounds[j + 1] - bounds[j]):
+            run()
+    ev[-1].record(stream)
+    ev[-1].synchronize()
+    per = [ev[j].elapsed_time(ev[j + 1]) / (bounds[j + 1] - bounds[j]) for j in range(len(bounds) - 1)]
+    mean = ev[0].elapsed_time(ev[-1]) / K
+    st = step_stats(per, K)
+    st["mean"] = mean
+    return mean, st
 
 
 # ---------------------------------------------------------------- the other target workloads
@@ -350,15 +394,10 @@ def bench_prefill_chunk(kvc, seed, local, seconds=EXTRA_SECONDS):
         t1.record(stream)
         torch.cuda.synchronize()
         n = int(min(20000, max(20, seconds / (t0.elapsed_time(t1) / 5 * 1e-3))))
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         with ClockSampler(local) as clk:
             torch.cuda.synchronize()
-            for a, b in ev:
-                a.record(stream)
-                run()
-                b.record(stream)
+            _, st = time_steps(run, n, stream)
             torch.cuda.synchronize()
-        st = step_stats([a.elapsed_time(b) for a, b in ev])
         flops = prefill_flops(w)
         tf = flops / (st["mean"] * 1e-3) / 1e12
         peak = tensor_peak()
@@ -423,16 +462,11 @@ def bench_extra(kvc, name, seed, hbm, local, seconds=EXTRA_SECONDS):
         t1.record(stream)
         torch.cuda.synchronize()
         n = int(min(20000, max(20, seconds / (t0.elapsed_time(t1) / 3 * 1e-3))))
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         with ClockSampler(local) as clk:
             torch.cuda.synchronize()
-            for a, b in ev:
-                a.record(stream)
-                run()
-                b.record(stream)
+            _, st = time_steps(run, n, stream)
             torch.cuda.synchronize()
         assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
-        st = step_stats([a.elapsed_time(b) for a, b in ev])
         sb = step_bytes(w)
         launch_ms = st["mean"] / w.L
         achieved = sb["total"] / (launch_ms * 1e-3) / 1e9
@@ -553,25 +587,16 @@ def main():
         barrier()
         run = graph.replay
 
-    # ---- device-resident timed region; events on the launching stream bracket every step
+    # ---- device-resident timed region; events on the launching stream bracket the
+    # region and groups of steps (per-step median / p90 over the groups)
     K = args.steps
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = kvc.kvc_launch_count()
     with ClockSampler(local) as clk:
         barrier()
-        t_start.record(stream)
-        for i in range(K):
-            ev_a[i].record(stream)
-            run()
-            ev_b[i].record(stream)
-        t_end.record(stream)
+        ms, per_step = time_steps(run, K, stream)
         barrier()
     launches = kvc.kvc_launch_count() - launches0 if graph is None else K * L
-    ms = t_start.elapsed_time(t_end) / K
-    per_step = step_stats([a.elapsed_time(b) for a, b in zip(ev_a, ev_b)])
-    attn_ms = per_step["mean"] / L    # per launch
+    attn_ms = ms / L    # per launch
     clocks = clk.summary()
     assert kvc.kvc_pool_sync_status(g.pool) == kvc.KVC_OK
 
@@ -693,9 +718,7 @@ def main():
                         "ms_per_step": e2e_ms, "tokens_per_s": w.B * world / (e2e_ms * 1e-3)},
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                              "frac": achieved / hbm, "traffic": profiled_traffic(w.name),
-                             "kernel": ("mixed_kernel: decode step with fused append and the prefill chunk in "
-                                        "one launch (kvc_mixed_step)" if pf is not None else
-                                        "decode_kernel with fused append (kvc_decode_step)"),
+                             "kernel": step_kernel(w),
                              "peak_source": f"{peak_kind} hbm_gbs",
                              "algorithmic_bytes_per_launch": sb1["total"], "launch_ms": attn_ms,
                              "note": splits_note},

@@ -61,8 +61,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p)
     __shared__ float4 part[128];
     const int hq = blockIdx.x, pos = blockIdx.y, tid = threadIdx.x;
     const int d4 = tid % ND4, grp = tid / ND4;
+    allow_dependent_launch();            // the next step's attention may be scheduled (it waits for this grid)
     int len = seq_len(p, pos / p.ppu);   // a caller input: read before the wait
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    grid_dependency_wait();
 
     const int S = p.max_splits;
     const size_t bq = static_cast<size_t>(pos) * p.H_Q + hq;
@@ -344,9 +345,21 @@ static kvc_status run_decode_tc(kvc_pool *pool, DecodeParams &p, const DecodeKer
         p.part_o = ws_data(pool);
         p.part_ml = reinterpret_cast<float2 *>(p.part_o + n * pool->D);
     }
+    // a programmatic dependent of whatever precedes it on the stream (the kernel waits for
+    // that grid before touching global memory), so its launch and set-up overlap that
+    // kernel's tail: in a decode loop, the previous step's merge
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.max_splits, p.H_KV, p.B);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = k.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     void *args[] = {const_cast<CUtensorMap *>(&pool->tmap16), &p};
-    const cudaError_t e = cudaLaunchKernel(k.fn, dim3(p.max_splits, p.H_KV, p.B), dim3(kTcThreads), args, k.smem,
-                                           stream);
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, args);
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (p.max_splits > 1) return launch_split_merge(p, pool->D, stream);

@@ -750,6 +750,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &tmap, const Decode
 // before it reads anything the grid wrote.
 __device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// Holds the CTA until the grid it programmatically depends on (the kernel before it
+// on the stream, when launched with programmatic stream serialization) has finished
+// and its memory writes are visible; returns at once in an ordinary launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // grid (split, KV head, unit)
 template <int D, int NT, int KIND, bool PSPLIT, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmap,

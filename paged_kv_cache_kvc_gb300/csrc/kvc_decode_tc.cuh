@@ -119,27 +119,6 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hq0 = h * p.g;
 
-    int len = seq_len(p, b);
-    if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) {
-        if (split == 0 && tid == 0) atomicOr(p.err, KVC_EBIT_RANGE);
-        len = 0;
-    }
-    const int nblk = (len + kBS - 1) / kBS;
-    if (nblk == 0) {   // empty sequence: zero output, lse = -inf
-        if (split == 0) {
-            for (int i = tid; i < G * D; i += kTcThreads) p.out[(static_cast<size_t>(b) * p.H_Q + hq0) * D + i] = 0.f;
-            if (p.lse && tid < G) p.lse[static_cast<size_t>(b) * p.H_Q + hq0 + tid] = -INFINITY;
-        }
-        return;
-    }
-    const int blk0 = split * p.chunk;   // chunk: a multiple of 8 blocks
-    if (blk0 >= nblk) return;
-    const int tile0 = blk0 / kTcBlocks;
-    const int nt = (min(nblk, blk0 + p.chunk) - blk0 + kTcBlocks - 1) / kTcBlocks;
-    const int ns = (nblk + p.chunk - 1) / p.chunk;
-    const int32_t *bt_row = p.bt + static_cast<int64_t>(b) * p.bt_stride;
-    const int64_t row_layer = static_cast<int64_t>(p.layer) * p.N;
-
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bars = sbase + kTcBars;
     // kv = 0: key slots, 1: value slots
@@ -154,7 +133,7 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
     float *msh = red + 128, *ash = msh + 32, *lsh = ash + 32;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTcTmemSlot);
 
-    // ---- set-up: barriers, TMEM, q rows (K-major B operand), reference maxima
+    // ---- set-up, before any global memory access: barriers, TMEM, reference maxima
     if (tid == 0) {
         for (int kv = 0; kv < 2; ++kv)
             for (int s = 0; s < kTcRing; ++s) {
@@ -180,358 +159,388 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    if (tid < 128) {   // q rows (K-major B operand of the score MMA), while the first keys are in flight
-        for (int i = tid; i < G * 16; i += 128) {   // row hh, 16-byte chunk c of 16
-            const int hh = i >> 4, c = i & 15;
-            const uint4 v = *reinterpret_cast<const uint4 *>(p.q + (static_cast<size_t>(b) * p.H_Q + hq0 + hh) * D + c * 8);
-            sts128(sbase + kTcQ + (c >> 3) * (32 * 128) + sw128(hh, c & 7), v);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(qready_bar);
+    // Launched as a programmatic dependent of the kernel before it on the stream: the set-up
+    // above overlaps that kernel's tail, and this wait (a no-op in an ordinary launch) holds
+    // the CTA until that kernel has finished and its writes are visible.  Everything below
+    // reads or writes global memory.
+    grid_dependency_wait();
+
+    int len = seq_len(p, b);
+    if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(p.max_blocks) * kBS) {
+        if (split == 0 && tid == 0) atomicOr(p.err, KVC_EBIT_RANGE);
+        len = 0;
     }
-    const uint32_t tm_o = tmem + 64;
+    const int nblk = (len + kBS - 1) / kBS;
+    if (nblk == 0 && split == 0) {   // empty sequence: zero output, lse = -inf
+        for (int i = tid; i < G * D; i += kTcThreads) p.out[(static_cast<size_t>(b) * p.H_Q + hq0) * D + i] = 0.f;
+        if (p.lse && tid < G) p.lse[static_cast<size_t>(b) * p.H_Q + hq0 + tid] = -INFINITY;
+    }
+    const int blk0 = split * p.chunk;   // chunk: a multiple of 8 blocks
+    if (blk0 < nblk) {   // uniform over the CTA: this split holds blocks
+        const int tile0 = blk0 / kTcBlocks;
+        const int nt = (min(nblk, blk0 + p.chunk) - blk0 + kTcBlocks - 1) / kTcBlocks;
+        const int ns = (nblk + p.chunk - 1) / p.chunk;
+        const int32_t *bt_row = p.bt + static_cast<int64_t>(b) * p.bt_stride;
+        const int64_t row_layer = static_cast<int64_t>(p.layer) * p.N;
 
-    bool timed_out = false;
-    // table entries of the CTA's blocks, 32 (4 tiles) at a time in registers, one window ahead:
-    // lane l holds block 32 w + l of window w
-    const int bbase = tile0 * kTcBlocks;
-    auto load_entry = [&](int rel) -> int32_t { return bbase + rel < nblk ? __ldg(bt_row + bbase + rel) : -1; };
-
-    if (warp == 4 || warp == 6) {
-        // ------------------------------------------------------------ TMA producers (4: keys, 6: values)
-        const int kv = warp == 6 ? 1 : 0;
-        int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
-        int j = 0;
-        for (; j < nt; ++j) {
-            if (j > 0 && (j & 3) == 0) {
-                ecur = enext;
-                enext = load_entry((j / 4 + 1) * 32 + lane);
-            }
-            const int s = j % kTcRing;
-            if (j >= kTcRing) {
-                const bool ok = mbar_wait_bounded(free_bar(kv, s), static_cast<uint32_t>(((j / kTcRing) - 1) & 1));
-                if (!__all_sync(kFull, ok)) {
-                    timed_out = true;
-                    break;
-                }
-            }
-            const int32_t e = __shfl_sync(kFull, ecur, (j & 3) * kTcBlocks + (lane & 7));
-            const int blk = bbase + j * kTcBlocks + lane;
-            const bool in = lane < kTcBlocks && blk < nblk;
-            const bool v = in && e >= 0 && static_cast<int64_t>(e) < p.N;
-            if (kv == 0 && in && !v) atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
-            const uint32_t mask = __ballot_sync(kFull, v);
-            if (lane == 0) {
-                if (mask == 0u) mbar_arrive(full_bar(kv, s));
-                else mbar_arrive_expect_tx(full_bar(kv, s), static_cast<uint32_t>(__popc(mask)) * 2u * (kBS * 128u));
-            }
-            __syncwarp();
-            if (v) {
-                const int32_t y = static_cast<int32_t>(((row_layer + e) * p.H_KV + h) * (2 * kBS) + kv * kBS);
-                const uint32_t st = sbase + kv * kTcV + s * kTcSlot + lane * (kBS * 128);
-                tma_load_2d(st, &tmap16, full_bar(kv, s), 0, y);
-                tma_load_2d(st + kTcBand, &tmap16, full_bar(kv, s), 64, y);
-            }
-        }
-        // before the CTA exits: the copies of the last slots have landed and their releases
-        // (tcgen05 commits, which arrive asynchronously) are in; both are immediate unless a
-        // wait somewhere expired
-        if (lane == 0)
-            for (int jj = max(0, j - kTcRing); jj < j; ++jj) {
-                (void)mbar_wait_bounded(full_bar(kv, jj % kTcRing), static_cast<uint32_t>((jj / kTcRing) & 1),
-                                        100000000ull);
-                (void)mbar_wait_bounded(free_bar(kv, jj % kTcRing), static_cast<uint32_t>((jj / kTcRing) & 1),
-                                        100000000ull);
-            }
-        __syncwarp();
-    } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
-        // Issues whichever MMA is ready: the score MMA of tile jq once its keys have landed and
-        // its score buffer is free (it releases the key slot), the value MMA of tile jp once its
-        // weights are in shared memory and its values have landed (it releases the value slot).
-        // Barriers are tested without blocking.
-        constexpr uint32_t idesc_qk = tc_idesc_f16(128, G, true, false, false);
-        constexpr uint32_t idesc_pv = tc_idesc_f16(128, 64, true, true, true);
-        int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
-        auto ready = [&](uint32_t bar, uint32_t parity) {   // lane 0 tests (never blocks), the warp agrees
-            const uint32_t r = lane == 0 ? (mbar_test_wait(bar, parity) ? 1u : 0u) : 0u;
-            return __shfl_sync(kFull, r, 0) != 0u;
-        };
-        const uint64_t desc_q = tc_smem_desc(sbase + kTcQ, 16, 1024, kSwizzle128B);
-        const uint64_t desc_p = tc_smem_desc(sbase + kTcP, kTcBand, 1024, kSwizzle128B);
-        // per tile in flight (3 at most between score and value MMA): its valid blocks, 8 bits each
-        uint32_t vmasks = 0u;
-        int32_t append_phys = -1;   // the block receiving the fused append (the sequence's last tile)
-        bool q_ready = false;
-        int jq = 0, jp = 0;
-        uint64_t idle_since = 0;
-        uint32_t idle = 0;
-        while (jp < nt) {
-            bool progressed = false;
-            if (jp < jq && ready(pfull_bar, static_cast<uint32_t>(jp & 1)) &&
-                ready(full_bar(1, jp % kTcRing), static_cast<uint32_t>((jp / kTcRing) & 1))) {
-                const uint32_t vst = sbase + kTcV + (jp % kTcRing) * kTcSlot;
-                // positions that must contribute nothing: past the sequence end, or in a block whose
-                // table entry is bad; their value rows are zeroed (their weights are 0; 0 * NaN is not)
-                const int tok0 = (tile0 + jp) * kTcTok;
-                const uint32_t vmask = (vmasks >> (8 * (jp % kTcRing))) & 0xFFu;
-                bool fix = tok0 + kTcTok > len || vmask != 0xFFu;
-                if (fix) {
-                    for (int i = lane; i < kTcTok * 16; i += 32) {
-                        const int row = i >> 4, c = i & 15, tok = tok0 + row;
-                        if (tok >= len || !(vmask >> (row >> 4) & 1u))
-                            sts128_zero(vst + (c >> 3) * kTcBand + sw128(row, c & 7));
-                    }
-                }
-                // fused append: the step's own value row, into the pool and into the slot
-                if (p.k_new && tok0 <= len - 1 && len - 1 < tok0 + kTcTok && append_phys >= 0) {
-                    fix = true;
-                    if (lane < 16) {
-                        const int row = len - 1 - tok0, c = lane;
-                        const uint4 val = *reinterpret_cast<const uint4 *>(
-                            p.v_new + (static_cast<size_t>(b) * p.H_KV + h) * D + c * 8);
-                        const int64_t el =
-                            ((((row_layer + append_phys) * p.H_KV + h) * 2 + 1) * kBS + (row & 15)) * D + c * 8;
-                        *reinterpret_cast<uint4 *>(p.pool + el * 2) = val;
-                        sts128(vst + (c >> 3) * kTcBand + sw128(row, c & 7), val);
-                    }
-                }
-                if (fix) fence_proxy_async_smem();   // zeros / the appended row, before the tensor cores read them
-                __syncwarp();
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t a0 = tc_smem_desc(vst, kTcBand, 1024, kSwizzle128B);
-#pragma unroll
-                    for (int kk = 0; kk < kTcTok / 16; ++kk)   // 16 tokens (2048 bytes of rows) per MMA
-                        tc_mma_f16(tm_o, tc_desc_advance(a0, kk * 2048), tc_desc_advance(desc_p, kk * 2048), idesc_pv,
-                                   (jp > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(free_bar(1, jp % kTcRing));
-                    tc_commit(pvdone_bar);
-                }
-                __syncwarp();
-                ++jp;
-                progressed = true;
-            }
-            if (!q_ready) q_ready = ready(qready_bar, 0u);
-            if (jq < nt && jq < jp + kTcRing && q_ready &&
-                ready(full_bar(0, jq % kTcRing), static_cast<uint32_t>((jq / kTcRing) & 1)) &&
-                (jq < 2 || ready(sfree_bar(jq & 1), static_cast<uint32_t>(((jq - 2) >> 1) & 1)))) {
-                if (jq > 0 && (jq & 3) == 0) {
-                    ecur = enext;
-                    enext = load_entry((jq / 4 + 1) * 32 + lane);
-                }
-                const uint32_t kst = sbase + (jq % kTcRing) * kTcSlot;
-                const int tok0 = (tile0 + jq) * kTcTok;
-                const int32_t e = __shfl_sync(kFull, ecur, (jq & 3) * kTcBlocks + (lane & 7));
-                const bool bv = bbase + jq * kTcBlocks + (lane & 7) < nblk && e >= 0 && static_cast<int64_t>(e) < p.N;
-                const uint32_t vmask = __ballot_sync(kFull, bv) & 0xFFu;
-                vmasks = (vmasks & ~(0xFFu << (8 * (jq % kTcRing)))) | (vmask << (8 * (jq % kTcRing)));
-                // fused append: the step's own key row, into the pool and into the slot (its value row
-                // goes in at the value MMA)
-                bool wrote = false;
-                if (p.k_new && tok0 <= len - 1 && len - 1 < tok0 + kTcTok) {
-                    const int row = len - 1 - tok0;
-                    const int32_t phys = __shfl_sync(kFull, e, row >> 4);
-                    if ((vmask >> (row >> 4)) & 1u) {
-                        append_phys = phys;
-                        wrote = true;
-                        if (lane < 16) {
-                            const int c = lane;
-                            const uint4 val = *reinterpret_cast<const uint4 *>(
-                                p.k_new + (static_cast<size_t>(b) * p.H_KV + h) * D + c * 8);
-                            const int64_t el = ((((row_layer + phys) * p.H_KV + h) * 2) * kBS + (row & 15)) * D + c * 8;
-                            *reinterpret_cast<uint4 *>(p.pool + el * 2) = val;
-                            sts128(kst + (c >> 3) * kTcBand + sw128(row, c & 7), val);
-                        }
-                    }
-                }
-                if (wrote) fence_proxy_async_smem();
-                __syncwarp();
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t a0 = tc_smem_desc(kst, 16, 1024, kSwizzle128B);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)   // 16 channels (32 bytes) per MMA, 4 per 128-byte band
-                        tc_mma_f16(tmem + (jq & 1) * 32, tc_desc_advance(a0, (kk >> 2) * kTcBand + (kk & 3) * 32),
-                                   tc_desc_advance(desc_q, (kk >> 2) * (32 * 128) + (kk & 3) * 32), idesc_qk,
-                                   kk > 0 ? 1u : 0u);
-                    tc_commit(sfull_bar(jq & 1));
-                    tc_commit(free_bar(0, jq % kTcRing));
-                }
-                __syncwarp();
-                ++jq;
-                progressed = true;
-            }
-            if (progressed) {
-                idle = 0;
-                idle_since = 0;
-            } else if ((++idle & 63u) == 0u) {   // bounded: 2 s without progress is an expired wait
-                const uint64_t now = globaltimer_ns();
-                if (idle_since == 0) idle_since = now;
-                else if (now - idle_since > 2000000000ull) {
-                    timed_out = true;
-                    break;
-                }
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ softmax (128 threads)
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        // this token's partial sums per head; the reference maxima (the same for every thread) are
-        // read from their shared copy msh, which only the slow path below rewrites
-        float lp[G];
-#pragma unroll
-        for (int i = 0; i < G; ++i) lp[i] = 0.f;
-        auto load_refs = [&](float (&mv)[G]) {
-#pragma unroll
-            for (int i = 0; i < G; i += 4) {
-                const float4 t = *reinterpret_cast<const float4 *>(msh + i);
-                mv[i] = t.x;
-                mv[i + 1] = t.y;
-                mv[i + 2] = t.z;
-                mv[i + 3] = t.w;
-            }
-        };
-        // table entries in the same register windows as the other roles (a warp's token of
-        // tile j lies in block 8 j + 2 warp + lane / 16)
-        int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
-        int j = 0;
-        for (; j < nt; ++j) {
-            if (j > 0 && (j & 3) == 0) {
-                ecur = enext;
-                enext = load_entry((j / 4 + 1) * 32 + lane);
-            }
-            const int32_t e_tok = __shfl_sync(kFull, ecur, (j & 3) * kTcBlocks + 2 * warp + (lane >> 4));
-            const int sb = j & 1;
-            const bool ok1 = mbar_wait_bounded(sfull_bar(sb), static_cast<uint32_t>((j >> 1) & 1));
-            tc_fence_after();
-            uint32_t r[32];
-            tmem_ld32(tmem + sb * 32 + lane_off, r);
-            tmem_ld_wait(r);
-            tc_fence_before();
-            mbar_arrive(sfree_bar(sb));
-
-            const int tok = (tile0 + j) * kTcTok + tid;
-            const bool valid = tok < len && e_tok >= 0 && static_cast<int64_t>(e_tok) < p.N;
-            // d = scale s - m (log2 units) per head; a reference moves when some d exceeds the
-            // slack (a reference of -inf: d = +inf).  Invalid positions weigh nothing.
-            float d[G];
-            float dmax = -INFINITY;
-            if (valid) {
-                load_refs(d);
-#pragma unroll
-                for (int i = 0; i < G; ++i) {
-                    d[i] = fmaf(__uint_as_float(r[i]), p.scale_log2, -d[i]);
-                    dmax = fmaxf(dmax, d[i]);
-                }
-            }
-            // P^T and O^T are free once the previous tile's value MMA has completed
-            const bool ok2 = j == 0 || mbar_wait_bounded(pvdone_bar, static_cast<uint32_t>((j - 1) & 1));
-            tc_fence_after();
-            // one CTA-wide vote per tile: a wait that expired anywhere, or a reference to move
-            if (softmax_any(!ok1 || !ok2 || dmax > kRescaleSlack)) {
-                if (!softmax_all(ok1 && ok2)) {
-                    timed_out = true;
-                    break;
-                }
-                // per-head tile maxima over the 128 tokens, new references and rescale factors
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
-                red[warp * 32 + lane] = warp_transpose_reduce<true>(v, lane);
-                softmax_sync();
-                if (warp == 0) {
-                    const float M = fmaxf(fmaxf(red[lane], red[32 + lane]), fmaxf(red[64 + lane], red[96 + lane]));
-                    const float mo = msh[lane];
-                    const float mn = M > mo + kRescaleSlack ? M : mo;
-                    msh[lane] = mn;
-                    ash[lane] = mn == mo ? 1.f : fast_exp2(mo - mn);
-                }
-                softmax_sync();
-                bool moved = false;
-#pragma unroll
-                for (int i = 0; i < G; ++i) {
-                    const float a = ash[i];
-                    lp[i] *= a;
-                    moved |= a != 1.f;
-                }
-                if (moved && j > 0) {   // O^T lane = channel, column = head (high, then low part)
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t o[32];
-                        tmem_ld32(tm_o + half * 32 + lane_off, o);
-                        tmem_ld_wait(o);
-#pragma unroll
-                        for (int i = 0; i < G; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * ash[i]);
-                        tmem_st32(tm_o + half * 32 + lane_off, o);
-                    }
-                    tmem_st_wait();
-                }
-                if (valid) {   // against the new references (finite: this position's score is in the max)
-                    load_refs(d);
-#pragma unroll
-                    for (int i = 0; i < G; ++i) d[i] = fmaf(__uint_as_float(r[i]), p.scale_log2, -d[i]);
-                }
-            }
-            // weights of this token for every head, into row `tid` of P^T, 8 heads (one 16-byte
-            // chunk) at a time: bf16 high parts in columns 0..31, the bf16 of the remainders in 32..63
-#pragma unroll
-            for (int c = 0; c < G / 8; ++c) {
-                uint32_t pk[4] = {0u, 0u, 0u, 0u}, pl[4] = {0u, 0u, 0u, 0u};
-                if (valid) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int i = 8 * c + 2 * k;
-                        const float p0 = fast_exp2(d[i]), p1 = fast_exp2(d[i + 1]);
-                        lp[i] += p0;
-                        lp[i + 1] += p1;
-                        pk[k] = pack_bf16(p0, p1);
-                        pl[k] = pack_bf16(p0 - bf16_lo(pk[k]), p1 - bf16_hi(pk[k]));
-                    }
-                }
-                sts128(sbase + kTcP + sw128(tid, c), make_uint4(pk[0], pk[1], pk[2], pk[3]));
-                sts128(sbase + kTcP + sw128(tid, c + 4), make_uint4(pl[0], pl[1], pl[2], pl[3]));
+        if (tid < 128) {   // q rows (K-major B operand of the score MMA), while the first keys are in flight
+            for (int i = tid; i < G * 16; i += 128) {   // row hh, 16-byte chunk c of 16
+                const int hh = i >> 4, c = i & 15;
+                const size_t qi = (static_cast<size_t>(b) * p.H_Q + hq0 + hh) * D + c * 8;
+                const uint4 v = *reinterpret_cast<const uint4 *>(p.q + qi);
+                sts128(sbase + kTcQ + (c >> 3) * (32 * 128) + sw128(hh, c & 7), v);
             }
             fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(pfull_bar);
+            mbar_arrive(qready_bar);
         }
+        const uint32_t tm_o = tmem + 64;
 
-        // ---- epilogue: O^T (thread = channel), the per-head sums, output or split partial
-        bool ok = !timed_out && mbar_wait_bounded(pvdone_bar, static_cast<uint32_t>((nt - 1) & 1));
-        ok = softmax_all(ok);
-        if (!ok) {
-            timed_out = true;
+        bool timed_out = false;
+        // table entries of the CTA's blocks, 32 (4 tiles) at a time in registers, one window ahead:
+        // lane l holds block 32 w + l of window w
+        const int bbase = tile0 * kTcBlocks;
+        auto load_entry = [&](int rel) -> int32_t { return bbase + rel < nblk ? __ldg(bt_row + bbase + rel) : -1; };
+
+        if (warp == 4 || warp == 6) {
+            // ------------------------------------------------------------ TMA producers (4: keys, 6: values)
+            const int kv = warp == 6 ? 1 : 0;
+            int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
+            int j = 0;
+            for (; j < nt; ++j) {
+                if (j > 0 && (j & 3) == 0) {
+                    ecur = enext;
+                    enext = load_entry((j / 4 + 1) * 32 + lane);
+                }
+                const int s = j % kTcRing;
+                if (j >= kTcRing) {
+                    const bool ok = mbar_wait_bounded(free_bar(kv, s), static_cast<uint32_t>(((j / kTcRing) - 1) & 1));
+                    if (!__all_sync(kFull, ok)) {
+                        timed_out = true;
+                        break;
+                    }
+                }
+                const int32_t e = __shfl_sync(kFull, ecur, (j & 3) * kTcBlocks + (lane & 7));
+                const int blk = bbase + j * kTcBlocks + lane;
+                const bool in = lane < kTcBlocks && blk < nblk;
+                const bool v = in && e >= 0 && static_cast<int64_t>(e) < p.N;
+                if (kv == 0 && in && !v) atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
+                const uint32_t mask = __ballot_sync(kFull, v);
+                if (lane == 0) {
+                    if (mask == 0u) mbar_arrive(full_bar(kv, s));
+                    else
+                        mbar_arrive_expect_tx(full_bar(kv, s), static_cast<uint32_t>(__popc(mask)) * 2u * (kBS * 128u));
+                }
+                __syncwarp();
+                if (v) {
+                    const int32_t y = static_cast<int32_t>(((row_layer + e) * p.H_KV + h) * (2 * kBS) + kv * kBS);
+                    const uint32_t st = sbase + kv * kTcV + s * kTcSlot + lane * (kBS * 128);
+                    tma_load_2d(st, &tmap16, full_bar(kv, s), 0, y);
+                    tma_load_2d(st + kTcBand, &tmap16, full_bar(kv, s), 64, y);
+                }
+            }
+            // before the CTA exits: the copies of the last slots have landed and their releases
+            // (tcgen05 commits, which arrive asynchronously) are in; both are immediate unless a
+            // wait somewhere expired
+            if (lane == 0)
+                for (int jj = max(0, j - kTcRing); jj < j; ++jj) {
+                    (void)mbar_wait_bounded(full_bar(kv, jj % kTcRing), static_cast<uint32_t>((jj / kTcRing) & 1),
+                                            100000000ull);
+                    (void)mbar_wait_bounded(free_bar(kv, jj % kTcRing), static_cast<uint32_t>((jj / kTcRing) & 1),
+                                            100000000ull);
+                }
+            __syncwarp();
+        } else if (warp == 5) {
+            // ------------------------------------------------------------ MMA issuer
+            // Issues whichever MMA is ready: the score MMA of tile jq once its keys have landed and
+            // its score buffer is free (it releases the key slot), the value MMA of tile jp once its
+            // weights are in shared memory and its values have landed (it releases the value slot).
+            // Barriers are tested without blocking.
+            constexpr uint32_t idesc_qk = tc_idesc_f16(128, G, true, false, false);
+            constexpr uint32_t idesc_pv = tc_idesc_f16(128, 64, true, true, true);
+            int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
+            auto ready = [&](uint32_t bar, uint32_t parity) {   // lane 0 tests (never blocks), the warp agrees
+                const uint32_t r = lane == 0 ? (mbar_test_wait(bar, parity) ? 1u : 0u) : 0u;
+                return __shfl_sync(kFull, r, 0) != 0u;
+            };
+            const uint64_t desc_q = tc_smem_desc(sbase + kTcQ, 16, 1024, kSwizzle128B);
+            const uint64_t desc_p = tc_smem_desc(sbase + kTcP, kTcBand, 1024, kSwizzle128B);
+            // per tile in flight (3 at most between score and value MMA): its valid blocks, 8 bits each
+            uint32_t vmasks = 0u;
+            int32_t append_phys = -1;   // the block receiving the fused append (the sequence's last tile)
+            bool q_ready = false;
+            int jq = 0, jp = 0;
+            uint64_t idle_since = 0;
+            uint32_t idle = 0;
+            while (jp < nt) {
+                bool progressed = false;
+                if (jp < jq && ready(pfull_bar, static_cast<uint32_t>(jp & 1)) &&
+                    ready(full_bar(1, jp % kTcRing), static_cast<uint32_t>((jp / kTcRing) & 1))) {
+                    const uint32_t vst = sbase + kTcV + (jp % kTcRing) * kTcSlot;
+                    // positions that must contribute nothing: past the sequence end, or in a block whose
+                    // table entry is bad; their value rows are zeroed (their weights are 0; 0 * NaN is not)
+                    const int tok0 = (tile0 + jp) * kTcTok;
+                    const uint32_t vmask = (vmasks >> (8 * (jp % kTcRing))) & 0xFFu;
+                    bool fix = tok0 + kTcTok > len || vmask != 0xFFu;
+                    if (fix) {
+                        for (int i = lane; i < kTcTok * 16; i += 32) {
+                            const int row = i >> 4, c = i & 15, tok = tok0 + row;
+                            if (tok >= len || !(vmask >> (row >> 4) & 1u))
+                                sts128_zero(vst + (c >> 3) * kTcBand + sw128(row, c & 7));
+                        }
+                    }
+                    // fused append: the step's own value row, into the pool and into the slot
+                    if (p.k_new && tok0 <= len - 1 && len - 1 < tok0 + kTcTok && append_phys >= 0) {
+                        fix = true;
+                        if (lane < 16) {
+                            const int row = len - 1 - tok0, c = lane;
+                            const uint4 val = *reinterpret_cast<const uint4 *>(
+                                p.v_new + (static_cast<size_t>(b) * p.H_KV + h) * D + c * 8);
+                            const int64_t el =
+                                ((((row_layer + append_phys) * p.H_KV + h) * 2 + 1) * kBS + (row & 15)) * D + c * 8;
+                            *reinterpret_cast<uint4 *>(p.pool + el * 2) = val;
+                            sts128(vst + (c >> 3) * kTcBand + sw128(row, c & 7), val);
+                        }
+                    }
+                    if (fix) fence_proxy_async_smem();   // zeros / the appended row, before the tensor cores read them
+                    __syncwarp();
+                    tc_fence_after();
+                    {
+                        const uint64_t a0 = tc_smem_desc(vst, kTcBand, 1024, kSwizzle128B);
+#pragma unroll
+                        for (int kk = 0; kk < kTcTok / 16; ++kk)   // 16 tokens (2048 bytes of rows) per MMA
+                            tc_mma_f16_warp(tm_o, tc_desc_advance(a0, kk * 2048), tc_desc_advance(desc_p, kk * 2048),
+                                            idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit_warp(free_bar(1, jp % kTcRing));
+                        tc_commit_warp(pvdone_bar);
+                    }
+                    __syncwarp();
+                    ++jp;
+                    progressed = true;
+                }
+                if (!q_ready) q_ready = ready(qready_bar, 0u);
+                if (jq < nt && jq < jp + kTcRing && q_ready &&
+                    ready(full_bar(0, jq % kTcRing), static_cast<uint32_t>((jq / kTcRing) & 1)) &&
+                    (jq < 2 || ready(sfree_bar(jq & 1), static_cast<uint32_t>(((jq - 2) >> 1) & 1)))) {
+                    if (jq > 0 && (jq & 3) == 0) {
+                        ecur = enext;
+                        enext = load_entry((jq / 4 + 1) * 32 + lane);
+                    }
+                    const uint32_t kst = sbase + (jq % kTcRing) * kTcSlot;
+                    const int tok0 = (tile0 + jq) * kTcTok;
+                    const int32_t e = __shfl_sync(kFull, ecur, (jq & 3) * kTcBlocks + (lane & 7));
+                    const bool bv =
+                        bbase + jq * kTcBlocks + (lane & 7) < nblk && e >= 0 && static_cast<int64_t>(e) < p.N;
+                    const uint32_t vmask = __ballot_sync(kFull, bv) & 0xFFu;
+                    vmasks = (vmasks & ~(0xFFu << (8 * (jq % kTcRing)))) | (vmask << (8 * (jq % kTcRing)));
+                    // fused append: the step's own key row, into the pool and into the slot (its value row
+                    // goes in at the value MMA)
+                    bool wrote = false;
+                    if (p.k_new && tok0 <= len - 1 && len - 1 < tok0 + kTcTok) {
+                        const int row = len - 1 - tok0;
+                        const int32_t phys = __shfl_sync(kFull, e, row >> 4);
+                        if ((vmask >> (row >> 4)) & 1u) {
+                            append_phys = phys;
+                            wrote = true;
+                            if (lane < 16) {
+                                const int c = lane;
+                                const uint4 val = *reinterpret_cast<const uint4 *>(
+                                    p.k_new + (static_cast<size_t>(b) * p.H_KV + h) * D + c * 8);
+                                const int64_t el =
+                                    ((((row_layer + phys) * p.H_KV + h) * 2) * kBS + (row & 15)) * D + c * 8;
+                                *reinterpret_cast<uint4 *>(p.pool + el * 2) = val;
+                                sts128(kst + (c >> 3) * kTcBand + sw128(row, c & 7), val);
+                            }
+                        }
+                    }
+                    if (wrote) fence_proxy_async_smem();
+                    __syncwarp();
+                    tc_fence_after();
+                    {
+                        const uint64_t a0 = tc_smem_desc(kst, 16, 1024, kSwizzle128B);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)   // 16 channels (32 bytes) per MMA, 4 per 128-byte band
+                            tc_mma_f16_warp(tmem + (jq & 1) * 32,
+                                            tc_desc_advance(a0, (kk >> 2) * kTcBand + (kk & 3) * 32),
+                                            tc_desc_advance(desc_q, (kk >> 2) * (32 * 128) + (kk & 3) * 32), idesc_qk,
+                                            kk > 0 ? 1u : 0u);
+                        tc_commit_warp(sfull_bar(jq & 1));
+                        tc_commit_warp(free_bar(0, jq % kTcRing));
+                    }
+                    __syncwarp();
+                    ++jq;
+                    progressed = true;
+                }
+                if (progressed) {
+                    idle = 0;
+                    idle_since = 0;
+                } else if ((++idle & 63u) == 0u) {   // bounded: 2 s without progress is an expired wait
+                    const uint64_t now = globaltimer_ns();
+                    if (idle_since == 0) idle_since = now;
+                    else if (now - idle_since > 2000000000ull) {
+                        timed_out = true;
+                        break;
+                    }
+                }
+            }
         } else {
-            tc_fence_after();
-            uint32_t o[32], olo[32];
-            tmem_ld32(tm_o + lane_off, o);
-            tmem_ld_wait(o);
-            tmem_ld32(tm_o + 32 + lane_off, olo);
-            tmem_ld_wait(olo);
+            // ------------------------------------------------------------ softmax (128 threads)
+            const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+            // this token's partial sums per head; the reference maxima (the same for every thread) are
+            // read from their shared copy msh, which only the slow path below rewrites
+            float lp[G];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) + __uint_as_float(olo[i]));
-            float v[32];
+            for (int i = 0; i < G; ++i) lp[i] = 0.f;
+            auto load_refs = [&](float (&mv)[G]) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = lp[i];
-            red[warp * 32 + lane] = warp_transpose_reduce<false>(v, lane);
-            softmax_sync();
-            if (warp == 0) lsh[lane] = (red[lane] + red[32 + lane]) + (red[64 + lane] + red[96 + lane]);
-            softmax_sync();
-            const size_t row0 = static_cast<size_t>(b) * p.H_Q + hq0;
-            if (ns == 1) {
+                for (int i = 0; i < G; i += 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(msh + i);
+                    mv[i] = t.x;
+                    mv[i + 1] = t.y;
+                    mv[i + 2] = t.z;
+                    mv[i + 3] = t.w;
+                }
+            };
+            // table entries in the same register windows as the other roles (a warp's token of
+            // tile j lies in block 8 j + 2 warp + lane / 16)
+            int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
+            int j = 0;
+            for (; j < nt; ++j) {
+                if (j > 0 && (j & 3) == 0) {
+                    ecur = enext;
+                    enext = load_entry((j / 4 + 1) * 32 + lane);
+                }
+                const int32_t e_tok = __shfl_sync(kFull, ecur, (j & 3) * kTcBlocks + 2 * warp + (lane >> 4));
+                const int sb = j & 1;
+                const bool ok1 = mbar_wait_bounded(sfull_bar(sb), static_cast<uint32_t>((j >> 1) & 1));
+                tc_fence_after();
+                uint32_t r[32];
+                tmem_ld32(tmem + sb * 32 + lane_off, r);
+                tmem_ld_wait(r);
+                tc_fence_before();
+                mbar_arrive(sfree_bar(sb));
+
+                const int tok = (tile0 + j) * kTcTok + tid;
+                const bool valid = tok < len && e_tok >= 0 && static_cast<int64_t>(e_tok) < p.N;
+                // d = scale s - m (log2 units) per head; a reference moves when some d exceeds the
+                // slack (a reference of -inf: d = +inf).  Invalid positions weigh nothing.
+                float d[G];
+                float dmax = -INFINITY;
+                if (valid) {
+                    load_refs(d);
 #pragma unroll
-                for (int i = 0; i < G; ++i) p.out[(row0 + i) * D + tid] = __uint_as_float(o[i]) / lsh[i];
-                if (p.lse && tid < G) p.lse[row0 + tid] = (msh[tid] + log2f(lsh[tid])) * kLn2;
+                    for (int i = 0; i < G; ++i) {
+                        d[i] = fmaf(__uint_as_float(r[i]), p.scale_log2, -d[i]);
+                        dmax = fmaxf(dmax, d[i]);
+                    }
+                }
+                // P^T and O^T are free once the previous tile's value MMA has completed
+                const bool ok2 = j == 0 || mbar_wait_bounded(pvdone_bar, static_cast<uint32_t>((j - 1) & 1));
+                tc_fence_after();
+                // one CTA-wide vote per tile: a wait that expired anywhere, or a reference to move
+                if (softmax_any(!ok1 || !ok2 || dmax > kRescaleSlack)) {
+                    if (!softmax_all(ok1 && ok2)) {
+                        timed_out = true;
+                        break;
+                    }
+                    // per-head tile maxima over the 128 tokens, new references and rescale factors
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+                    red[warp * 32 + lane] = warp_transpose_reduce<true>(v, lane);
+                    softmax_sync();
+                    if (warp == 0) {
+                        const float M = fmaxf(fmaxf(red[lane], red[32 + lane]), fmaxf(red[64 + lane], red[96 + lane]));
+                        const float mo = msh[lane];
+                        const float mn = M > mo + kRescaleSlack ? M : mo;
+                        msh[lane] = mn;
+                        ash[lane] = mn == mo ? 1.f : fast_exp2(mo - mn);
+                    }
+                    softmax_sync();
+                    bool moved = false;
+#pragma unroll
+                    for (int i = 0; i < G; ++i) {
+                        const float a = ash[i];
+                        lp[i] *= a;
+                        moved |= a != 1.f;
+                    }
+                    if (moved && j > 0) {   // O^T lane = channel, column = head (high, then low part)
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t o[32];
+                            tmem_ld32(tm_o + half * 32 + lane_off, o);
+                            tmem_ld_wait(o);
+#pragma unroll
+                            for (int i = 0; i < G; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * ash[i]);
+                            tmem_st32(tm_o + half * 32 + lane_off, o);
+                        }
+                        tmem_st_wait();
+                    }
+                    if (valid) {   // against the new references (finite: this position's score is in the max)
+                        load_refs(d);
+#pragma unroll
+                        for (int i = 0; i < G; ++i) d[i] = fmaf(__uint_as_float(r[i]), p.scale_log2, -d[i]);
+                    }
+                }
+                // weights of this token for every head, into row `tid` of P^T, 8 heads (one 16-byte
+                // chunk) at a time: bf16 high parts in columns 0..31, the bf16 of the remainders in 32..63
+#pragma unroll
+                for (int c = 0; c < G / 8; ++c) {
+                    uint32_t pk[4] = {0u, 0u, 0u, 0u}, pl[4] = {0u, 0u, 0u, 0u};
+                    if (valid) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int i = 8 * c + 2 * k;
+                            const float p0 = fast_exp2(d[i]), p1 = fast_exp2(d[i + 1]);
+                            lp[i] += p0;
+                            lp[i + 1] += p1;
+                            pk[k] = pack_bf16(p0, p1);
+                            pl[k] = pack_bf16(p0 - bf16_lo(pk[k]), p1 - bf16_hi(pk[k]));
+                        }
+                    }
+                    sts128(sbase + kTcP + sw128(tid, c), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                    sts128(sbase + kTcP + sw128(tid, c + 4), make_uint4(pl[0], pl[1], pl[2], pl[3]));
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(pfull_bar);
+            }
+
+            // ---- epilogue: O^T (thread = channel), the per-head sums, output or split partial
+            bool ok = !timed_out && mbar_wait_bounded(pvdone_bar, static_cast<uint32_t>((nt - 1) & 1));
+            ok = softmax_all(ok);
+            if (!ok) {
+                timed_out = true;
             } else {
+                tc_fence_after();
+                uint32_t o[32], olo[32];
+                tmem_ld32(tm_o + lane_off, o);
+                tmem_ld_wait(o);
+                tmem_ld32(tm_o + 32 + lane_off, olo);
+                tmem_ld_wait(olo);
 #pragma unroll
-                for (int i = 0; i < G; ++i)
-                    p.part_o[((row0 + i) * p.max_splits + split) * D + tid] = __uint_as_float(o[i]);
-                if (tid < G) p.part_ml[(row0 + tid) * p.max_splits + split] = make_float2(msh[tid], lsh[tid]);
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) + __uint_as_float(olo[i]));
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = lp[i];
+                red[warp * 32 + lane] = warp_transpose_reduce<false>(v, lane);
+                softmax_sync();
+                if (warp == 0) lsh[lane] = (red[lane] + red[32 + lane]) + (red[64 + lane] + red[96 + lane]);
+                softmax_sync();
+                const size_t row0 = static_cast<size_t>(b) * p.H_Q + hq0;
+                if (ns == 1) {
+#pragma unroll
+                    for (int i = 0; i < G; ++i) p.out[(row0 + i) * D + tid] = __uint_as_float(o[i]) / lsh[i];
+                    if (p.lse && tid < G) p.lse[row0 + tid] = (msh[tid] + log2f(lsh[tid])) * kLn2;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < G; ++i)
+                        p.part_o[((row0 + i) * p.max_splits + split) * D + tid] = __uint_as_float(o[i]);
+                    if (tid < G) p.part_ml[(row0 + tid) * p.max_splits + split] = make_float2(msh[tid], lsh[tid]);
+                }
             }
         }
+        if (timed_out && lane == 0) atomicOr(p.err, KVC_EBIT_TIMEOUT);
     }
-    if (timed_out && lane == 0) atomicOr(p.err, KVC_EBIT_TIMEOUT);
 
     tc_fence_before();
     __syncthreads();
@@ -541,7 +550,7 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
     }
 }
 
-// grid (split, KV head, sequence), 192 threads
+// grid (split, KV head, sequence), 224 threads
 template <int G>
 __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_constant__ CUtensorMap tmap16,
                                                                   const DecodeParams p)

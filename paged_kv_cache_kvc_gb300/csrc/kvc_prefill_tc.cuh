@@ -16,13 +16,16 @@
 //   warp 5      MMA issuer (one lane), per stage j:
 //                 S[128 x 64]  = Q[128 x D] . K^T        (K-major A and B)
 //                 O[128 x D]  += P[128 x 64] . V[64 x D]  (K-major A, MN-major B)
-//               S double-buffered in TMEM, so the scores of stage j + 1 are
-//               computed while the softmax of stage j runs.
+//               S and P double-buffered (S in TMEM, P in shared memory), so
+//               the scores of stage j + 1 are computed while the softmax of
+//               stage j runs, and the softmax of stage j + 1 writes its
+//               weights while the value MMA of stage j reads the other buffer.
 //   warps 0..3  softmax, thread r = row r (TMEM lane r): the causal mask
 //               (key < q_start + position + 1), the row's running maximum as a
 //               reference that moves only when a score exceeds it by more than
 //               8 (log2 units), then the row's O in TMEM and its sum are
-//               rescaled (the warp does it together when any lane needs it);
+//               rescaled (the warp does it together when any lane needs it,
+//               after the value MMA of the stage before has landed in O);
 //               P row r as bf16 into shared memory.
 // Value rows of positions past the row's end are zeroed before the value MMA
 // (a zero weight times NaN is NaN).  The epilogue divides each row by its sum.
@@ -42,9 +45,9 @@ struct PrefillTcCfg {
     static constexpr int STAGE = 2 * BANDS * KBAND;           // keys, then values
     static constexpr int QBAND = 128 * 128;                   // one band of the 128 query rows
     static constexpr int Q = kPtRing * STAGE;
-    static constexpr int P = Q + BANDS * QBAND;               // P: 128 rows x 64 keys bf16 (one band)
-    static constexpr int BARS = P + 128 * 128;
-    static constexpr int NUM_BARS = 2 * kPtRing + 6;          // full, kvfree, s_full[2], s_free[2], p_full, pv_done
+    static constexpr int P = Q + BANDS * QBAND;               // P[2]: 128 rows x 64 keys bf16 (one band) each
+    static constexpr int BARS = P + 2 * 128 * 128;
+    static constexpr int NUM_BARS = 2 * kPtRing + 8;          // full, kvfree, s_full[2], s_free[2], p_full[2], pv_done[2]
     static constexpr int SLOT = BARS + NUM_BARS * 8;
     static constexpr int SMEM = 1024 + SLOT + 16;
     static constexpr uint32_t COLS = 256;                     // S[0] 0..63, S[1] 64..127, O from column 128
@@ -73,8 +76,8 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
     auto kvfree_bar = [&](int s) { return bars + 8u * (kPtRing + s); };
     auto sfull_bar = [&](int sb) { return bars + 8u * (2 * kPtRing + sb); };
     auto sfree_bar = [&](int sb) { return bars + 8u * (2 * kPtRing + 2 + sb); };
-    const uint32_t pfull_bar = bars + 8u * (2 * kPtRing + 4);
-    const uint32_t pvdone_bar = bars + 8u * (2 * kPtRing + 5);
+    auto pfull_bar = [&](int pb) { return bars + 8u * (2 * kPtRing + 4 + pb); };
+    auto pvdone_bar = [&](int pb) { return bars + 8u * (2 * kPtRing + 6 + pb); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SLOT);
 
     if (tid == 0) {
@@ -85,9 +88,9 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
         for (int sb = 0; sb < 2; ++sb) {
             mbar_init(sfull_bar(sb), 1);
             mbar_init(sfree_bar(sb), 128);
+            mbar_init(pfull_bar(sb), 128);
+            mbar_init(pvdone_bar(sb), 1);
         }
-        mbar_init(pfull_bar, 128);
-        mbar_init(pvdone_bar, 1);
         fence_barrier_init();
         prefetch_tensormap(&tmap16);
     }
@@ -166,31 +169,33 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
         constexpr uint32_t idesc_qk = tc_idesc_f16(128, kPtKeys, true, false, false);
         constexpr uint32_t idesc_pv = tc_idesc_f16(128, D, true, false, true);
         // Issues whichever MMA is ready: the value MMA of stage jp once its weights are in
-        // shared memory (it releases the stage), the score MMA of stage jq once its keys have
-        // landed and its score buffer is free.  Barriers are tested without blocking.
+        // shared memory (it releases the stage and the weight buffer), the score MMA of stage
+        // jq once its keys have landed and its score buffer is free.  Barriers are tested
+        // without blocking.
         int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
         auto ready = [&](uint32_t bar, uint32_t parity) {   // lane 0 tests, the warp agrees
             const uint32_t r = lane == 0 ? (mbar_test_wait(bar, parity) ? 1u : 0u) : 0u;
             return __shfl_sync(kFull, r, 0) != 0u;
         };
         const uint64_t desc_q = tc_smem_desc(sbase + C::Q, 16, 1024, kSwizzle128B);
-        const uint64_t desc_p = tc_smem_desc(sbase + C::P, 16, 1024, kSwizzle128B);
+        const uint64_t desc_p0 = tc_smem_desc(sbase + C::P, 16, 1024, kSwizzle128B);
         int jq = 0, jp = 0;
         uint64_t idle_since = 0;
         uint32_t idle = 0;
         while (jp < nt) {
             bool progressed = false;
-            if (jp < jq && ready(pfull_bar, static_cast<uint32_t>(jp & 1))) {
+            if (jp < jq && ready(pfull_bar(jp & 1), static_cast<uint32_t>((jp >> 1) & 1))) {
                 tc_fence_after();
-                if (lane == 0) {
+                {
+                    const uint64_t desc_p = tc_desc_advance(desc_p0, (jp & 1) * (128 * 128));
                     const uint64_t b0 = tc_smem_desc(sbase + (jp % kPtRing) * C::STAGE + C::BANDS * C::KBAND, C::KBAND,
                                                      1024, kSwizzle128B);
 #pragma unroll
                     for (int kk = 0; kk < kPtKeys / 16; ++kk)   // 16 keys: 32 bytes of P rows, 2048 of V rows
-                        tc_mma_f16(tm_o, tc_desc_advance(desc_p, kk * 32), tc_desc_advance(b0, kk * 2048), idesc_pv,
-                                   (jp > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(kvfree_bar(jp % kPtRing));
-                    tc_commit(pvdone_bar);
+                        tc_mma_f16_warp(tm_o, tc_desc_advance(desc_p, kk * 32), tc_desc_advance(b0, kk * 2048),
+                                        idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit_warp(kvfree_bar(jp % kPtRing));
+                    tc_commit_warp(pvdone_bar(jp & 1));
                 }
                 __syncwarp();
                 ++jp;
@@ -219,14 +224,15 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
                 }
                 __syncwarp();
                 tc_fence_after();
-                if (lane == 0) {
+                {
                     const uint64_t b0 = tc_smem_desc(st, 16, 1024, kSwizzle128B);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)   // 16 channels (32 bytes) per MMA, 4 per 128-byte band
-                        tc_mma_f16(tmem + (jq & 1) * kPtKeys,
-                                   tc_desc_advance(desc_q, (kk >> 2) * C::QBAND + (kk & 3) * 32),
-                                   tc_desc_advance(b0, (kk >> 2) * C::KBAND + (kk & 3) * 32), idesc_qk, kk > 0 ? 1u : 0u);
-                    tc_commit(sfull_bar(jq & 1));
+                        tc_mma_f16_warp(tmem + (jq & 1) * kPtKeys,
+                                        tc_desc_advance(desc_q, (kk >> 2) * C::QBAND + (kk & 3) * 32),
+                                        tc_desc_advance(b0, (kk >> 2) * C::KBAND + (kk & 3) * 32), idesc_qk,
+                                        kk > 0 ? 1u : 0u);
+                    tc_commit_warp(sfull_bar(jq & 1));
                 }
                 __syncwarp();
                 ++jq;
@@ -280,13 +286,8 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
 #pragma unroll
             for (int c = 1; c < 64; ++c) bm = fmaxf(bm, sv[c]);
             bm *= p.scale_log2;                           // scale > 0: the max of the scaled scores
-            // the previous stage's value MMA has read P and updated O
-            const bool ok2 = j == 0 || mbar_wait_bounded(pvdone_bar, static_cast<uint32_t>((j - 1) & 1));
-            if (!softmax_all(ok1 && ok2)) {   // one CTA-wide vote per stage: a wait expired anywhere
-                timed_out = true;
-                break;
-            }
-            tc_fence_after();
+            // the value MMA of stage j - 2 has read this stage's weight buffer
+            const bool ok2 = j < 2 || mbar_wait_bounded(pvdone_bar(j & 1), static_cast<uint32_t>(((j - 2) >> 1) & 1));
             const bool move = bm > m + kRescaleSlack;   // the first visible key always moves a -inf maximum
             float alpha = 1.f;
             if (move) {
@@ -294,7 +295,15 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
                 m = bm;
                 l *= alpha;
             }
-            if (j > 0 && __any_sync(kFull, move && alpha != 1.f)) {   // the warp rescales its O rows together
+            // the warp rescales its O rows together, once the value MMA of stage j - 1 is in O
+            const bool rescale = j > 0 && __any_sync(kFull, move && alpha != 1.f);
+            const bool ok3 = !rescale || mbar_wait_bounded(pvdone_bar((j - 1) & 1), static_cast<uint32_t>(((j - 1) >> 1) & 1));
+            if (!softmax_all(ok1 && ok2 && ok3)) {   // one CTA-wide vote per stage: a wait expired anywhere
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            if (rescale) {
 #pragma unroll
                 for (int part = 0; part < D / 32; ++part) {
                     uint32_t o[32];
@@ -319,13 +328,15 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
             }
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-                sts128(sbase + C::P + sw128(tid, c), make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+                sts128(sbase + C::P + (j & 1) * (128 * 128) + sw128(tid, c),
+                       make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(pfull_bar);
+            mbar_arrive(pfull_bar(j & 1));
         }
 
-        bool ok = !timed_out && mbar_wait_bounded(pvdone_bar, static_cast<uint32_t>((nt - 1) & 1));
+        bool ok = !timed_out &&
+                  mbar_wait_bounded(pvdone_bar((nt - 1) & 1), static_cast<uint32_t>(((nt - 1) >> 1) & 1));
         ok = softmax_all(ok);
         if (!ok) {
             timed_out = true;
