@@ -209,6 +209,27 @@ static size_t workspace_bytes(int B, int H_Q, int max_splits, int D)
     return n * D * sizeof(float) + n * sizeof(float2);
 }
 
+// Launches a decode attention kernel as a programmatic dependent of whatever precedes it
+// on the stream.  The kernels wait (griddepcontrol.wait) for that grid before their first
+// global access, so their launch and set-up overlap its tail: in a decode loop, the
+// previous step's attention or merge.  When what precedes it is not a kernel, the launch
+// behaves as an ordinary one.
+static cudaError_t launch_programmatic_dependent(const void *fn, dim3 grid, dim3 block, int smem, cudaStream_t stream,
+                                                 void **args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream)
 {
     kvc_pool *pool = const_cast<kvc_pool *>(cpool);
@@ -230,9 +251,9 @@ kvc_status run_decode(const kvc_pool *cpool, DecodeParams &p, const DecodeKernel
         p.part_ml = nullptr;
         p.counters = nullptr;
     }
-    const dim3 grid(p.max_splits, p.H_KV, p.B);
     void *args[] = {const_cast<CUtensorMap *>(&pool->tmap), &p};
-    cudaError_t e = cudaLaunchKernel(k.fn, grid, dim3(kThreads), args, k.smem, stream);
+    const cudaError_t e =
+        launch_programmatic_dependent(k.fn, dim3(p.max_splits, p.H_KV, p.B), dim3(kThreads), k.smem, stream, args);
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (p.max_splits > 1 && !p.counters) return launch_split_merge(p, pool->D, stream);
@@ -345,21 +366,9 @@ static kvc_status run_decode_tc(kvc_pool *pool, DecodeParams &p, const DecodeKer
         p.part_o = ws_data(pool);
         p.part_ml = reinterpret_cast<float2 *>(p.part_o + n * pool->D);
     }
-    // a programmatic dependent of whatever precedes it on the stream (the kernel waits for
-    // that grid before touching global memory), so its launch and set-up overlap that
-    // kernel's tail: in a decode loop, the previous step's merge
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.max_splits, p.H_KV, p.B);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = k.smem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     void *args[] = {const_cast<CUtensorMap *>(&pool->tmap16), &p};
-    const cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, args);
+    const cudaError_t e =
+        launch_programmatic_dependent(k.fn, dim3(p.max_splits, p.H_KV, p.B), dim3(kTcThreads), k.smem, stream, args);
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (p.max_splits > 1) return launch_split_merge(p, pool->D, stream);

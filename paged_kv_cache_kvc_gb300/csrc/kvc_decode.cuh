@@ -761,6 +761,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                                                           const DecodeParams p)
 {
     allow_dependent_launch();
+    grid_dependency_wait();   // launched as a programmatic dependent: nothing global is touched before this
     decode_cta<D, NT, KIND, PSPLIT, CAUSAL>(tmap, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
