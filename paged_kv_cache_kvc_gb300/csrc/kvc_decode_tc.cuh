@@ -231,11 +231,12 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
                         mbar_arrive_expect_tx(full_bar(kv, s), static_cast<uint32_t>(__popc(mask)) * 2u * (kBS * 128u));
                 }
                 __syncwarp();
-                if (v) {
+                // one box per lane, all in one instruction: lane = (band, block); every lane
+                // already holds the entry of block lane mod 8
+                if (lane < 2 * kTcBlocks && ((mask >> (lane & 7)) & 1u)) {
                     const int32_t y = static_cast<int32_t>(((row_layer + e) * p.H_KV + h) * (2 * kBS) + kv * kBS);
-                    const uint32_t st = sbase + kv * kTcV + s * kTcSlot + lane * (kBS * 128);
-                    tma_load_2d(st, &tmap16, full_bar(kv, s), 0, y);
-                    tma_load_2d(st + kTcBand, &tmap16, full_bar(kv, s), 64, y);
+                    tma_load_2d(sbase + kv * kTcV + s * kTcSlot + (lane >> 3) * kTcBand + (lane & 7) * (kBS * 128),
+                                &tmap16, full_bar(kv, s), (lane >> 3) * 64, y);
                 }
             }
             // before the CTA exits: the copies of the last slots have landed and their releases

@@ -9,11 +9,13 @@
 // 0 .. q_start + i.  A CTA takes KV head h and 128 query rows: 128 / g
 // consecutive chunk positions x the g query heads of h (row r = position
 // r / g, head h * g + r mod g), so every staged key / value tile serves all g
-// heads.  192 threads in three roles:
-//   warp 4      TMA producer: 64 keys per stage (4 blocks of the row), key
-//               rows and value rows of each block as separate 16-row boxes
-//               (128-byte swizzle), a ring of 3 stages.
-//   warp 5      MMA issuer (one lane), per stage j:
+// heads.  224 threads in three roles:
+//   warps 4, 6  TMA producers, warp 4 the key rows and warp 6 the value rows
+//               of a stage: 64 keys per stage (4 blocks of the row), each
+//               block's rows a 16-row box per 128-byte band (128-byte
+//               swizzle), a ring of 5 stages.  Two warps because one warp's
+//               boxes are issued one after the other (about 40 ns each).
+//   warp 5      MMA issuer (one elected lane), per stage j:
 //                 S[128 x 64]  = Q[128 x D] . K^T        (K-major A and B)
 //                 O[128 x D]  += P[128 x 64] . V[64 x D]  (K-major A, MN-major B)
 //               S and P double-buffered (S in TMEM, P in shared memory), so
@@ -35,8 +37,8 @@
 namespace kvc {
 
 constexpr int kPtKeys = 64;                     // keys per stage
-constexpr int kPtRing = 3;
-constexpr int kPtThreads = 192;
+constexpr int kPtRing = 5;
+constexpr int kPtThreads = 224;
 
 template <int D>
 struct PrefillTcCfg {
@@ -82,7 +84,7 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
 
     if (tid == 0) {
         for (int s = 0; s < kPtRing; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), 2);   // the key producer and the value producer
             mbar_init(kvfree_bar(s), 1);
         }
         for (int sb = 0; sb < 2; ++sb) {
@@ -120,8 +122,9 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
     auto load_entry = [&](int blk) -> int32_t { return blk < nblk ? __ldg(p.bt + blk) : -1; };
 
     bool timed_out = false;
-    if (warp == 4) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == 4 || warp == 6) {
+        // ------------------------------------------------------------ TMA producers (4: keys, 6: values)
+        const int kvp = warp == 6 ? 1 : 0;
         int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
         int j = 0;
         for (; j < nt; ++j) {
@@ -140,21 +143,20 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
             const int blk = j * BPS + lane;
             const int32_t e = __shfl_sync(kFull, ecur, (j % (32 / BPS)) * BPS + (lane & (BPS - 1)));
             const bool v = lane < BPS && blk < nblk && e >= 0 && static_cast<int64_t>(e) < p.N;
-            if (lane < BPS && blk < nblk && !v) atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
+            if (kvp == 0 && lane < BPS && blk < nblk && !v) atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
             const uint32_t mask = __ballot_sync(kFull, v);
             if (lane == 0) {
                 if (mask == 0u) mbar_arrive(full_bar(s));
-                else mbar_arrive_expect_tx(full_bar(s), static_cast<uint32_t>(__popc(mask)) * 2u * C::BANDS * (kBS * 128u));
+                else mbar_arrive_expect_tx(full_bar(s), static_cast<uint32_t>(__popc(mask)) * C::BANDS * (kBS * 128u));
             }
             __syncwarp();
-            if (v) {
-                const int32_t y = static_cast<int32_t>(((row_layer + e) * p.H_KV + h) * (2 * kBS));
-                const uint32_t st = sbase + s * C::STAGE + lane * (kBS * 128);
-#pragma unroll
-                for (int band = 0; band < C::BANDS; ++band) {
-                    tma_load_2d(st + band * C::KBAND, &tmap16, full_bar(s), band * 64, y);
-                    tma_load_2d(st + (C::BANDS + band) * C::KBAND, &tmap16, full_bar(s), band * 64, y + kBS);
-                }
+            // one box per lane, all in one instruction: lane = (band, block); every lane
+            // already holds the entry of block lane mod BPS
+            const int bl = lane % BPS, band = lane / BPS;
+            if (lane < BPS * C::BANDS && ((mask >> bl) & 1u)) {
+                const int32_t y = static_cast<int32_t>(((row_layer + e) * p.H_KV + h) * (2 * kBS)) + kvp * kBS;
+                tma_load_2d(sbase + s * C::STAGE + (kvp * C::BANDS + band) * C::KBAND + bl * (kBS * 128), &tmap16,
+                            full_bar(s), band * 64, y);
             }
         }
         if (lane == 0)
@@ -250,7 +252,7 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
                 }
             }
         }
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------------------ softmax: thread = query row
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
         const int pos = pos0 + tid / g;
@@ -263,8 +265,8 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
             tc_fence_after();
             uint32_t r0[32], r1[32];
             tmem_ld32(tmem + sb * kPtKeys + lane_off, r0);
-            tmem_ld_wait(r0);
             tmem_ld32(tmem + sb * kPtKeys + 32 + lane_off, r1);
+            tmem_ld_wait(r0);
             tmem_ld_wait(r1);
             tc_fence_before();
             mbar_arrive(sfree_bar(sb));
@@ -282,12 +284,18 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
 #pragma unroll
                 for (int c = 0; c < 64; ++c) sv[c] = c < nvis ? sv[c] : -INFINITY;
             }
-            float bm = sv[0];
+            float b0 = sv[0], b1 = sv[1], b2 = sv[2], b3 = sv[3];   // four chains of 3-input maxima
 #pragma unroll
-            for (int c = 1; c < 64; ++c) bm = fmaxf(bm, sv[c]);
+            for (int c = 4; c < 60; c += 8) {
+                b0 = max3f(b0, sv[c], sv[c + 1]);
+                b1 = max3f(b1, sv[c + 2], sv[c + 3]);
+                b2 = max3f(b2, sv[c + 4], sv[c + 5]);
+                b3 = max3f(b3, sv[c + 6], sv[c + 7]);
+            }
+            b0 = max3f(b0, sv[60], sv[61]);
+            b1 = max3f(b1, sv[62], sv[63]);
+            float bm = max3f(b0, b1, fmaxf(b2, b3));
             bm *= p.scale_log2;                           // scale > 0: the max of the scaled scores
-            // the value MMA of stage j - 2 has read this stage's weight buffer
-            const bool ok2 = j < 2 || mbar_wait_bounded(pvdone_bar(j & 1), static_cast<uint32_t>(((j - 2) >> 1) & 1));
             const bool move = bm > m + kRescaleSlack;   // the first visible key always moves a -inf maximum
             float alpha = 1.f;
             if (move) {
@@ -298,12 +306,8 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
             // the warp rescales its O rows together, once the value MMA of stage j - 1 is in O
             const bool rescale = j > 0 && __any_sync(kFull, move && alpha != 1.f);
             const bool ok3 = !rescale || mbar_wait_bounded(pvdone_bar((j - 1) & 1), static_cast<uint32_t>(((j - 1) >> 1) & 1));
-            if (!softmax_all(ok1 && ok2 && ok3)) {   // one CTA-wide vote per stage: a wait expired anywhere
-                timed_out = true;
-                break;
-            }
-            tc_fence_after();
-            if (rescale) {
+            if (rescale && ok3) {
+                tc_fence_after();
 #pragma unroll
                 for (int part = 0; part < D / 32; ++part) {
                     uint32_t o[32];
@@ -319,12 +323,21 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
             // every row), and a masked score (-inf) weighs 0
             const float neg_m = -m;
             uint32_t pk[32];
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};   // four partial sums: short dependency chains
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
                 const float p0 = fast_exp2(fmaf(sv[c], p.scale_log2, neg_m));
                 const float p1 = fast_exp2(fmaf(sv[c + 1], p.scale_log2, neg_m));
-                l += p0 + p1;
+                ls[(c / 2) & 3] += p0 + p1;
                 pk[c / 2] = pack_bf16(p0, p1);
+            }
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            // the value MMA of stage j - 2 has read this stage's weight buffer (waited for only
+            // now, behind the exponentials)
+            const bool ok2 = j < 2 || mbar_wait_bounded(pvdone_bar(j & 1), static_cast<uint32_t>(((j - 2) >> 1) & 1));
+            if (!softmax_all(ok1 && ok2 && ok3)) {   // one CTA-wide vote per stage: a wait expired anywhere
+                timed_out = true;
+                break;
             }
 #pragma unroll
             for (int c = 0; c < 8; ++c)
@@ -371,7 +384,7 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
     }
 }
 
-// grid (1, KV head, tile of 128 / g positions), 192 threads.  Launched as a
+// grid (1, KV head, tile of 128 / g positions), 224 threads.  Launched as a
 // programmatic dependent in the mixed step: it reads only the chunk's row,
 // which the step before it does not write, so it never waits on that step.
 template <int D>
