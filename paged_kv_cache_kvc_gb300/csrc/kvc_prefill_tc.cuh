@@ -9,36 +9,43 @@
 // 0 .. q_start + i.  A CTA takes KV head h and 128 query rows: 128 / g
 // consecutive chunk positions x the g query heads of h (row r = position
 // r / g, head h * g + r mod g), so every staged key / value tile serves all g
-// heads.  224 threads in three roles:
-//   warps 4, 6  TMA producers, warp 4 the key rows and warp 6 the value rows
-//               of a stage: 64 keys per stage (4 blocks of the row), each
-//               block's rows a 16-row box per 128-byte band (128-byte
-//               swizzle), a ring of 5 stages.  Two warps because one warp's
-//               boxes are issued one after the other (about 40 ns each).
-//   warp 5      MMA issuer (one elected lane), per stage j:
-//                 S[128 x 64]  = Q[128 x D] . K^T        (K-major A and B)
-//                 O[128 x D]  += P[128 x 64] . V[64 x D]  (K-major A, MN-major B)
-//               S and P double-buffered (S in TMEM, P in shared memory), so
-//               the scores of stage j + 1 are computed while the softmax of
-//               stage j runs, and the softmax of stage j + 1 writes its
-//               weights while the value MMA of stage j reads the other buffer.
-//   warps 0..3  softmax, thread r = row r (TMEM lane r): the causal mask
-//               (key < q_start + position + 1), the row's running maximum as a
-//               reference that moves only when a score exceeds it by more than
-//               8 (log2 units), then the row's O in TMEM and its sum are
-//               rescaled (the warp does it together when any lane needs it,
-//               after the value MMA of the stage before has landed in O);
-//               P row r as bf16 into shared memory.
-// Value rows of positions past the row's end are zeroed before the value MMA
-// (a zero weight times NaN is NaN).  The epilogue divides each row by its sum.
+// heads.
+//
+// The CTA's keys (64 per stage) are split into two streams, stream 0 the first
+// half of its stages and stream 1 the rest, each with its own staging ring,
+// score, weight and output accumulators in TMEM and softmax warps; the epilogue merges
+// the two partial softmaxes of every row (the log-sum-exp merge of split
+// attention).  One stream's chain of score MMA -> softmax -> value MMA leaves
+// the tensor cores and the single MMA-issuing thread idle most of the time;
+// two independent chains fill each other's gaps.  352 threads:
+//   warps 8, 9    TMA producers of stream 0 and 1: per stage the key rows and
+//                 value rows of its 4 blocks, one 16-row box per block, 128-byte
+//                 band and keys / values (128-byte swizzle), a ring of 3 stages.
+//   warp 10       MMA issuer (one elected lane), for both streams, per stage:
+//                   S[128 x 64]  = Q[128 x D] . K^T        (K-major A and B)
+//                   O[128 x D]  += P[128 x 64] . V[64 x D]  (A from TMEM, MN-major B)
+//                 S double-buffered per stream in TMEM; the softmax writes P as
+//                 bf16 pairs over the first 32 columns of its own S buffer, so
+//                 the buffer is reused by the score MMA two stages later only
+//                 after the value MMA has read P.
+//   warps 0..3    softmax of stream 0, warps 4..7 of stream 1; thread = query
+//                 row (TMEM lane): the causal mask (key < q_start + position +
+//                 1), the row's running maximum as a reference that moves only
+//                 when a score exceeds it by more than 8 (log2 units), then the
+//                 row's O and sum are rescaled (the warp together, after the
+//                 stream's previous value MMA has landed); P row as bf16 into
+//                 TMEM.
+// Value rows of keys past the row's end or of blocks not loaded are zeroed
+// before the value MMA (a zero weight times NaN is NaN).  The epilogue merges
+// the streams with weights 2^(m_s - max m) and divides by the merged sum.
 #pragma once
 #include "kvc_decode_tc.cuh"
 
 namespace kvc {
 
 constexpr int kPtKeys = 64;                     // keys per stage
-constexpr int kPtRing = 5;
-constexpr int kPtThreads = 224;
+constexpr int kPtRing = 3;                      // stages in flight per stream
+constexpr int kPtThreads = 352;
 
 template <int D>
 struct PrefillTcCfg {
@@ -46,14 +53,29 @@ struct PrefillTcCfg {
     static constexpr int KBAND = kPtKeys * 128;               // one band of the stage's 64 key rows
     static constexpr int STAGE = 2 * BANDS * KBAND;           // keys, then values
     static constexpr int QBAND = 128 * 128;                   // one band of the 128 query rows
-    static constexpr int Q = kPtRing * STAGE;
-    static constexpr int P = Q + BANDS * QBAND;               // P[2]: 128 rows x 64 keys bf16 (one band) each
-    static constexpr int BARS = P + 2 * 128 * 128;
-    static constexpr int NUM_BARS = 2 * kPtRing + 8;          // full, kvfree, s_full[2], s_free[2], p_full[2], pv_done[2]
-    static constexpr int SLOT = BARS + NUM_BARS * 8;
+    static constexpr int Q = 0;
+    static constexpr int RING = Q + BANDS * QBAND;            // [stream][slot] stages
+    static constexpr int BARS = RING + 2 * kPtRing * STAGE;
+    // per stream: full[R], kvfree[R], s_full[2], p_full[2], pv_done[2]
+    static constexpr int BARS_PER_STREAM = 2 * kPtRing + 6;
+    static constexpr int VMASK = BARS + 2 * BARS_PER_STREAM * 8;   // [stream][slot] loaded-block masks
+    static constexpr int XCH = VMASK + 2 * kPtRing * 4;            // stream 1's (m, l) per row for the merge
+    static constexpr int SLOT = XCH + 128 * 8;
     static constexpr int SMEM = 1024 + SLOT + 16;
-    static constexpr uint32_t COLS = 256;                     // S[0] 0..63, S[1] 64..127, O from column 128
+    static constexpr uint32_t COLS = 512;   // stream s: S/P[0] s*256 + 0..63, S/P[1] + 64..127, O from s*256 + 128
 };
+
+// A vote of the 128 threads of one softmax group (named barrier `id`).
+__device__ __forceinline__ bool group_all(bool v, uint32_t id)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, 128, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"(v ? 1u : 0u), "r"(id)
+                 : "memory");
+    return r != 0;
+}
 
 template <int D>
 __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const DecodeParams &p, const int tile,
@@ -71,27 +93,35 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
     const int nt = (n_keys + kPtKeys - 1) / kPtKeys;
     const int nblk = (n_keys + kBS - 1) / kBS;
     const int64_t row_layer = static_cast<int64_t>(p.layer) * p.N;
+    // stream 0: stages [0, split), stream 1: [split, nt) (empty when nt == 1)
+    const int split = (nt + 1) / 2;
+    auto s_begin = [&](int s) { return s == 0 ? 0 : split; };
+    auto s_count = [&](int s) { return s == 0 ? split : nt - split; };
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bars = sbase + C::BARS;
-    auto full_bar = [&](int s) { return bars + 8u * s; };
-    auto kvfree_bar = [&](int s) { return bars + 8u * (kPtRing + s); };
-    auto sfull_bar = [&](int sb) { return bars + 8u * (2 * kPtRing + sb); };
-    auto sfree_bar = [&](int sb) { return bars + 8u * (2 * kPtRing + 2 + sb); };
-    auto pfull_bar = [&](int pb) { return bars + 8u * (2 * kPtRing + 4 + pb); };
-    auto pvdone_bar = [&](int pb) { return bars + 8u * (2 * kPtRing + 6 + pb); };
+    auto sbar = [&](int s, int i) { return bars + 8u * (s * C::BARS_PER_STREAM + i); };
+    auto full_bar = [&](int s, int r) { return sbar(s, r); };
+    auto kvfree_bar = [&](int s, int r) { return sbar(s, kPtRing + r); };
+    auto sfull_bar = [&](int s, int b) { return sbar(s, 2 * kPtRing + b); };
+    auto pfull_bar = [&](int s, int b) { return sbar(s, 2 * kPtRing + 2 + b); };
+    auto pvdone_bar = [&](int s, int b) { return sbar(s, 2 * kPtRing + 4 + b); };
+    auto stage_addr = [&](int s, int r) { return sbase + C::RING + (s * kPtRing + r) * C::STAGE; };
+    volatile uint32_t *vmask_sh = reinterpret_cast<volatile uint32_t *>(smem + C::VMASK);
+    float2 *xch = reinterpret_cast<float2 *>(smem + C::XCH);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SLOT);
 
     if (tid == 0) {
-        for (int s = 0; s < kPtRing; ++s) {
-            mbar_init(full_bar(s), 2);   // the key producer and the value producer
-            mbar_init(kvfree_bar(s), 1);
-        }
-        for (int sb = 0; sb < 2; ++sb) {
-            mbar_init(sfull_bar(sb), 1);
-            mbar_init(sfree_bar(sb), 128);
-            mbar_init(pfull_bar(sb), 128);
-            mbar_init(pvdone_bar(sb), 1);
+        for (int s = 0; s < 2; ++s) {
+            for (int r = 0; r < kPtRing; ++r) {
+                mbar_init(full_bar(s, r), 1);
+                mbar_init(kvfree_bar(s, r), 1);
+            }
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(sfull_bar(s, b), 1);
+                mbar_init(pfull_bar(s, b), 128);
+                mbar_init(pvdone_bar(s, b), 1);
+            }
         }
         fence_barrier_init();
         prefetch_tensormap(&tmap16);
@@ -114,131 +144,132 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tm_o = tmem + 128;
 
-    // the row's table entries, 32 (8 stages) at a time in registers, one window ahead: lane l
-    // holds block 32 w + l of window w
     constexpr int BPS = kPtKeys / kBS;                // blocks per stage
+    constexpr int SPW = 32 / BPS;                     // stages per 32-entry table window
     auto load_entry = [&](int blk) -> int32_t { return blk < nblk ? __ldg(p.bt + blk) : -1; };
 
     bool timed_out = false;
-    if (warp == 4 || warp == 6) {
-        // ------------------------------------------------------------ TMA producers (4: keys, 6: values)
-        const int kvp = warp == 6 ? 1 : 0;
-        int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
-        int j = 0;
-        for (; j < nt; ++j) {
-            if (j > 0 && (j % (32 / BPS)) == 0) {
+    if (warp == 8 || warp == 9) {
+        // ------------------------------------------------------------ TMA producer of stream s
+        const int s = warp - 8, b = s_begin(s), n = s_count(s);
+        // lane l holds entry 32 w + l of table window w (the stages of window w: SPW w .. SPW w + SPW - 1)
+        int w = b / SPW;
+        int32_t ecur = load_entry(32 * w + lane), enext = load_entry(32 * (w + 1) + lane);
+        int i = 0;
+        for (; i < n; ++i) {
+            const int j = b + i, r = i % kPtRing;
+            if (j / SPW != w) {
+                ++w;
                 ecur = enext;
-                enext = load_entry((j / (32 / BPS) + 1) * 32 + lane);
+                enext = load_entry(32 * (w + 1) + lane);
             }
-            const int s = j % kPtRing;
-            if (j >= kPtRing) {
-                const bool ok = mbar_wait_bounded(kvfree_bar(s), static_cast<uint32_t>(((j / kPtRing) - 1) & 1));
+            if (i >= kPtRing) {
+                const bool ok = mbar_wait_bounded(kvfree_bar(s, r), static_cast<uint32_t>(((i / kPtRing) - 1) & 1));
                 if (!__all_sync(kFull, ok)) {
                     timed_out = true;
                     break;
                 }
             }
             const int blk = j * BPS + lane;
-            const int32_t e = __shfl_sync(kFull, ecur, (j % (32 / BPS)) * BPS + (lane & (BPS - 1)));
+            const int32_t e = __shfl_sync(kFull, ecur, (j % SPW) * BPS + (lane & (BPS - 1)));
             const bool v = lane < BPS && blk < nblk && e >= 0 && static_cast<int64_t>(e) < p.N;
-            if (kvp == 0 && lane < BPS && blk < nblk && !v) atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
-            const uint32_t mask = __ballot_sync(kFull, v);
+            if (lane < BPS && blk < nblk && !v) atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
+            const uint32_t mask = __ballot_sync(kFull, v) & ((1u << BPS) - 1u);
             if (lane == 0) {
-                if (mask == 0u) mbar_arrive(full_bar(s));
-                else mbar_arrive_expect_tx(full_bar(s), static_cast<uint32_t>(__popc(mask)) * C::BANDS * (kBS * 128u));
+                vmask_sh[s * kPtRing + r] = mask;   // published by the arrive below
+                if (mask == 0u) mbar_arrive(full_bar(s, r));
+                else
+                    mbar_arrive_expect_tx(full_bar(s, r),
+                                          static_cast<uint32_t>(__popc(mask)) * 2u * C::BANDS * (kBS * 128u));
             }
             __syncwarp();
-            // one box per lane, all in one instruction: lane = (band, block); every lane
-            // already holds the entry of block lane mod BPS
-            const int bl = lane % BPS, band = lane / BPS;
-            if (lane < BPS * C::BANDS && ((mask >> bl) & 1u)) {
+            // one box per lane, all in one instruction: lane = (band, keys / values, block);
+            // every lane already holds the entry of block lane mod BPS
+            const int bl = lane % BPS, kvp = (lane / BPS) & 1, band = lane / (2 * BPS);
+            if (lane < 2 * BPS * C::BANDS && ((mask >> bl) & 1u)) {
                 const int32_t y = static_cast<int32_t>(((row_layer + e) * p.H_KV + h) * (2 * kBS)) + kvp * kBS;
-                tma_load_2d(sbase + s * C::STAGE + (kvp * C::BANDS + band) * C::KBAND + bl * (kBS * 128), &tmap16,
-                            full_bar(s), band * 64, y);
+                tma_load_2d(stage_addr(s, r) + (kvp * C::BANDS + band) * C::KBAND + bl * (kBS * 128), &tmap16,
+                            full_bar(s, r), band * 64, y);
             }
         }
+        // before the CTA exits: the copies of the last slots have landed and their releases
+        // are in (immediate unless a wait expired)
         if (lane == 0)
-            for (int jj = max(0, j - kPtRing); jj < j; ++jj) {
-                (void)mbar_wait_bounded(full_bar(jj % kPtRing), static_cast<uint32_t>((jj / kPtRing) & 1), 100000000ull);
-                (void)mbar_wait_bounded(kvfree_bar(jj % kPtRing), static_cast<uint32_t>((jj / kPtRing) & 1),
+            for (int ii = max(0, i - kPtRing); ii < i; ++ii) {
+                (void)mbar_wait_bounded(full_bar(s, ii % kPtRing), static_cast<uint32_t>((ii / kPtRing) & 1),
+                                        100000000ull);
+                (void)mbar_wait_bounded(kvfree_bar(s, ii % kPtRing), static_cast<uint32_t>((ii / kPtRing) & 1),
                                         100000000ull);
             }
         __syncwarp();
-    } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 10) {
+        // ------------------------------------------------------------ MMA issuer (both streams)
         constexpr uint32_t idesc_qk = tc_idesc_f16(128, kPtKeys, true, false, false);
         constexpr uint32_t idesc_pv = tc_idesc_f16(128, D, true, false, true);
-        // Issues whichever MMA is ready: the value MMA of stage jp once its weights are in
-        // shared memory (it releases the stage and the weight buffer), the score MMA of stage
-        // jq once its keys have landed and its score buffer is free.  Barriers are tested
-        // without blocking.
-        int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
-        auto ready = [&](uint32_t bar, uint32_t parity) {   // lane 0 tests, the warp agrees
+        // Issues whichever MMA is ready, stream by stream: the value MMA of a stream's stage
+        // once its weights are in TMEM (it releases the stage), the score MMA of a stage once
+        // its keys have landed and the value MMA two stages back has read the weights in its
+        // score buffer.  Barriers are tested without blocking, lane 0 testing for the warp.
+        auto ready = [&](uint32_t bar, uint32_t parity) {
             const uint32_t r = lane == 0 ? (mbar_test_wait(bar, parity) ? 1u : 0u) : 0u;
             return __shfl_sync(kFull, r, 0) != 0u;
         };
         const uint64_t desc_q = tc_smem_desc(sbase + C::Q, 16, 1024, kSwizzle128B);
-        const uint64_t desc_p0 = tc_smem_desc(sbase + C::P, 16, 1024, kSwizzle128B);
-        int jq = 0, jp = 0;
+        int jq[2] = {0, 0}, jp[2] = {0, 0};
+        const int n[2] = {s_count(0), s_count(1)};
         uint64_t idle_since = 0;
         uint32_t idle = 0;
-        while (jp < nt) {
+        while (jp[0] < n[0] || jp[1] < n[1]) {
             bool progressed = false;
-            if (jp < jq && ready(pfull_bar(jp & 1), static_cast<uint32_t>((jp >> 1) & 1))) {
-                tc_fence_after();
-                {
-                    const uint64_t desc_p = tc_desc_advance(desc_p0, (jp & 1) * (128 * 128));
-                    const uint64_t b0 = tc_smem_desc(sbase + (jp % kPtRing) * C::STAGE + C::BANDS * C::KBAND, C::KBAND,
-                                                     1024, kSwizzle128B);
 #pragma unroll
-                    for (int kk = 0; kk < kPtKeys / 16; ++kk)   // 16 keys: 32 bytes of P rows, 2048 of V rows
-                        tc_mma_f16_warp(tm_o, tc_desc_advance(desc_p, kk * 32), tc_desc_advance(b0, kk * 2048),
-                                        idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit_warp(kvfree_bar(jp % kPtRing));
-                    tc_commit_warp(pvdone_bar(jp & 1));
+            for (int s = 0; s < 2; ++s) {
+                const uint32_t tm_s = tmem + s * 256;
+                if (jp[s] < jq[s] && ready(pfull_bar(s, jp[s] & 1), static_cast<uint32_t>((jp[s] >> 1) & 1))) {
+                    const int i = jp[s];
+                    tc_fence_after();
+                    const uint64_t b0 = tc_smem_desc(stage_addr(s, i % kPtRing) + C::BANDS * C::KBAND, C::KBAND, 1024,
+                                                     kSwizzle128B);
+#pragma unroll
+                    for (int kk = 0; kk < kPtKeys / 16; ++kk)   // 16 keys: 8 TMEM columns of P, 2048 bytes of V rows
+                        tc_mma_f16_tmem_a_warp(tm_s + 128, tm_s + (i & 1) * kPtKeys + kk * 8,
+                                               tc_desc_advance(b0, kk * 2048), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit_warp(kvfree_bar(s, i % kPtRing));
+                    tc_commit_warp(pvdone_bar(s, i & 1));
+                    __syncwarp();
+                    ++jp[s];
+                    progressed = true;
                 }
-                __syncwarp();
-                ++jp;
-                progressed = true;
-            }
-            if (jq < nt && ready(full_bar(jq % kPtRing), static_cast<uint32_t>((jq / kPtRing) & 1)) &&
-                (jq < 2 || ready(sfree_bar(jq & 1), static_cast<uint32_t>(((jq - 2) >> 1) & 1)))) {
-                if (jq > 0 && (jq % (32 / BPS)) == 0) {
-                    ecur = enext;
-                    enext = load_entry((jq / (32 / BPS) + 1) * 32 + lane);
-                }
-                const uint32_t st = sbase + (jq % kPtRing) * C::STAGE;
-                // value rows of keys past the row's end or in a block whose entry is bad: zero
-                const int key0 = jq * kPtKeys;
-                const int blk = jq * BPS + (lane & (BPS - 1));
-                const int32_t e = __shfl_sync(kFull, ecur, (jq % (32 / BPS)) * BPS + (lane & (BPS - 1)));
-                const bool bv = blk < nblk && e >= 0 && static_cast<int64_t>(e) < p.N;
-                const uint32_t vmask = __ballot_sync(kFull, bv) & ((1u << BPS) - 1u);
-                if (key0 + kPtKeys > total || vmask != (1u << BPS) - 1u) {
-                    for (int i = lane; i < kPtKeys * 8 * C::BANDS; i += 32) {
-                        const int row = i / (8 * C::BANDS), c = i % (8 * C::BANDS);
-                        if (key0 + row >= total || !(vmask >> (row >> 4) & 1u))
-                            sts128_zero(st + (C::BANDS + (c >> 3)) * C::KBAND + sw128(row, c & 7));
+                if (jq[s] < n[s] && ready(full_bar(s, jq[s] % kPtRing), static_cast<uint32_t>((jq[s] / kPtRing) & 1)) &&
+                    (jq[s] < 2 ||
+                     (jq[s] - 2 < jp[s] &&
+                      ready(pvdone_bar(s, jq[s] & 1), static_cast<uint32_t>(((jq[s] - 2) >> 1) & 1))))) {
+                    const int i = jq[s], j = s_begin(s) + i, key0 = j * kPtKeys;
+                    const uint32_t st = stage_addr(s, i % kPtRing);
+                    // value rows of keys past the row's end or of blocks not loaded: zero
+                    const uint32_t vmask = vmask_sh[s * kPtRing + i % kPtRing];
+                    if (key0 + kPtKeys > total || vmask != (1u << BPS) - 1u) {
+                        for (int x = lane; x < kPtKeys * 8 * C::BANDS; x += 32) {
+                            const int row = x / (8 * C::BANDS), c = x % (8 * C::BANDS);
+                            if (key0 + row >= total || !(vmask >> (row >> 4) & 1u))
+                                sts128_zero(st + (C::BANDS + (c >> 3)) * C::KBAND + sw128(row, c & 7));
+                        }
+                        fence_proxy_async_smem();
                     }
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                tc_fence_after();
-                {
+                    __syncwarp();
+                    tc_fence_after();
                     const uint64_t b0 = tc_smem_desc(st, 16, 1024, kSwizzle128B);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)   // 16 channels (32 bytes) per MMA, 4 per 128-byte band
-                        tc_mma_f16_warp(tmem + (jq & 1) * kPtKeys,
+                        tc_mma_f16_warp(tm_s + (i & 1) * kPtKeys,
                                         tc_desc_advance(desc_q, (kk >> 2) * C::QBAND + (kk & 3) * 32),
                                         tc_desc_advance(b0, (kk >> 2) * C::KBAND + (kk & 3) * 32), idesc_qk,
                                         kk > 0 ? 1u : 0u);
-                    tc_commit_warp(sfull_bar(jq & 1));
+                    tc_commit_warp(sfull_bar(s, i & 1));
+                    __syncwarp();
+                    ++jq[s];
+                    progressed = true;
                 }
-                __syncwarp();
-                ++jq;
-                progressed = true;
             }
             if (progressed) {
                 idle = 0;
@@ -252,24 +283,25 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
                 }
             }
         }
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ softmax: thread = query row
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const int pos = pos0 + tid / g;
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ softmax of stream s: thread = query row
+        const int s = warp >> 2, row = tid & 127, b = s_begin(s), n = s_count(s);
+        const uint32_t vote_id = 1u + static_cast<uint32_t>(s);
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tm_s = tmem + s * 256, tm_o = tm_s + 128;
+        const int pos = pos0 + row / g;
         const int vis = min(q_start + pos + 1, total);   // keys this row may read (rows past the chunk: all)
         float m = -INFINITY, l = 0.f;
-        int j = 0;
-        for (; j < nt; ++j) {
-            const int sb = j & 1;
-            const bool ok1 = mbar_wait_bounded(sfull_bar(sb), static_cast<uint32_t>((j >> 1) & 1));
+        int i = 0;
+        for (; i < n; ++i) {
+            const int j = b + i, sb = i & 1;
+            const bool ok1 = mbar_wait_bounded(sfull_bar(s, sb), static_cast<uint32_t>((i >> 1) & 1));
             tc_fence_after();
             uint32_t r0[32], r1[32];
-            tmem_ld32(tmem + sb * kPtKeys + lane_off, r0);
-            tmem_ld32(tmem + sb * kPtKeys + 32 + lane_off, r1);
+            tmem_ld32(tm_s + sb * kPtKeys + lane_off, r0);
+            tmem_ld32(tm_s + sb * kPtKeys + 32 + lane_off, r1);
             tmem_ld_wait(r0);
             tmem_ld_wait(r1);
-            tc_fence_before();
-            mbar_arrive(sfree_bar(sb));
 
             // keys past the row's visible end (the causal diagonal, or the row's end) count
             // nothing; stages wholly visible to the row skip the masking
@@ -295,17 +327,18 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
             b0 = max3f(b0, sv[60], sv[61]);
             b1 = max3f(b1, sv[62], sv[63]);
             float bm = max3f(b0, b1, fmaxf(b2, b3));
-            bm *= p.scale_log2;                           // scale > 0: the max of the scaled scores
-            const bool move = bm > m + kRescaleSlack;   // the first visible key always moves a -inf maximum
+            bm *= p.scale_log2;                         // scale > 0: the max of the scaled scores
+            const bool move = bm > m + kRescaleSlack;   // -inf (nothing visible yet) never moves
             float alpha = 1.f;
             if (move) {
                 alpha = fast_exp2(m - bm);              // 0 while nothing was visible
                 m = bm;
                 l *= alpha;
             }
-            // the warp rescales its O rows together, once the value MMA of stage j - 1 is in O
-            const bool rescale = j > 0 && __any_sync(kFull, move && alpha != 1.f);
-            const bool ok3 = !rescale || mbar_wait_bounded(pvdone_bar((j - 1) & 1), static_cast<uint32_t>(((j - 1) >> 1) & 1));
+            // the warp rescales its O rows together, once the stream's previous value MMA is in O
+            const bool rescale = i > 0 && __any_sync(kFull, move && alpha != 1.f);
+            const bool ok3 = !rescale || mbar_wait_bounded(pvdone_bar(s, (i - 1) & 1),
+                                                           static_cast<uint32_t>(((i - 1) >> 1) & 1));
             if (rescale && ok3) {
                 tc_fence_after();
 #pragma unroll
@@ -319,9 +352,10 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
                 }
                 tmem_st_wait();
             }
-            // weights 2^(scale s - m): m is finite from the first stage on (key 0 is visible to
-            // every row), and a masked score (-inf) weighs 0
-            const float neg_m = -m;
+            // weights 2^(scale s - m); a masked score (-inf) weighs 0, and so does every key
+            // while none has been visible to the row (m = -inf: stream 1 can start past the
+            // causal end of a row at the tile's start)
+            const float neg_m = m == -INFINITY ? 0.f : -m;
             uint32_t pk[32];
             float ls[4] = {0.f, 0.f, 0.f, 0.f};   // four partial sums: short dependency chains
 #pragma unroll
@@ -332,46 +366,72 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
                 pk[c / 2] = pack_bf16(p0, p1);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            // the value MMA of stage j - 2 has read this stage's weight buffer (waited for only
-            // now, behind the exponentials)
-            const bool ok2 = j < 2 || mbar_wait_bounded(pvdone_bar(j & 1), static_cast<uint32_t>(((j - 2) >> 1) & 1));
-            if (!softmax_all(ok1 && ok2 && ok3)) {   // one CTA-wide vote per stage: a wait expired anywhere
+            if (!group_all(ok1 && ok3, vote_id)) {   // one vote per stage: a wait expired in the group
                 timed_out = true;
                 break;
             }
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                sts128(sbase + C::P + (j & 1) * (128 * 128) + sw128(tid, c),
-                       make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-            fence_proxy_async_smem();
+            // P row over the first 32 columns of this stage's score buffer (its scores are in
+            // registers): the A operand of the value MMA
+            tmem_st32(tm_s + sb * kPtKeys + lane_off, pk);
+            tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(pfull_bar(j & 1));
+            mbar_arrive(pfull_bar(s, sb));
         }
 
-        bool ok = !timed_out &&
-                  mbar_wait_bounded(pvdone_bar((nt - 1) & 1), static_cast<uint32_t>(((nt - 1) >> 1) & 1));
-        ok = softmax_all(ok);
-        if (!ok) {
-            timed_out = true;
+        bool ok = !timed_out && (n == 0 || mbar_wait_bounded(pvdone_bar(s, (n - 1) & 1),
+                                                             static_cast<uint32_t>(((n - 1) >> 1) & 1)));
+        ok = group_all(ok, vote_id);
+        if (!ok) timed_out = true;
+        if (s == 1) {
+            // stream 1 hands its (m, l) to stream 0's thread of the same row; l < 0 marks an
+            // expired wait (its O must not be read)
+            xch[row] = make_float2(m, ok ? l : -1.f);
+            asm volatile("bar.arrive 3, 256;" ::: "memory");
         } else {
-            tc_fence_after();
-            const bool real = pos < n_q;
-            const size_t orow = (static_cast<size_t>(pos) * p.H_Q + h * g + tid % g);
-            const float inv = 1.f / l;
+            asm volatile("bar.sync 3, 256;" ::: "memory");
+            const float2 o1 = xch[row];
+            const bool use1 = s_count(1) > 0 && o1.x != -INFINITY;   // stream 1 saw keys of this row
+            const int n1 = s_count(1);   // stream 1's last value MMA, observed here too before its O is read
+            const bool ok1 = n1 == 0 || o1.y < 0.f ||
+                             mbar_wait_bounded(pvdone_bar(1, (n1 - 1) & 1),
+                                               static_cast<uint32_t>(((n1 - 1) >> 1) & 1));
+            if (ok && ok1 && o1.y >= 0.f) {
+                tc_fence_after();
+                const float M = use1 ? fmaxf(m, o1.x) : m;   // m is finite: key 0 is visible to every row
+                const float w0 = fast_exp2(m - M), w1 = use1 ? fast_exp2(o1.x - M) : 0.f;
+                const float L = w0 * l + w1 * o1.y;
+                const bool real = pos < n_q;
+                const size_t orow = (static_cast<size_t>(pos) * p.H_Q + h * g + row % g);
+                const float a0 = w0 / L, a1 = w1 / L;
 #pragma unroll
-            for (int part = 0; part < D / 32; ++part) {
-                uint32_t o[32];
-                tmem_ld32(tm_o + part * 32 + lane_off, o);
-                tmem_ld_wait(o);
-                if (real) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.out + orow * D + part * 32);
+                for (int part = 0; part < D / 32; ++part) {
+                    uint32_t o[32], u[32];
+                    tmem_ld32(tm_o + part * 32 + lane_off, o);
+                    tmem_ld_wait(o);
+                    if (s_count(1) > 0) {   // uniform: stream 1's O exists (finite: zero weights x finite rows)
+                        tmem_ld32(tmem + 256 + 128 + part * 32 + lane_off, u);
+                        tmem_ld_wait(u);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv, __uint_as_float(o[4 * c + 1]) * inv,
-                                             __uint_as_float(o[4 * c + 2]) * inv, __uint_as_float(o[4 * c + 3]) * inv);
+                        for (int c = 0; c < 32; ++c) u[c] = 0u;
+                    }
+                    if (real) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.out + orow * D + part * 32);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            float4 v;
+                            v.x = fmaf(__uint_as_float(o[4 * c]), a0, __uint_as_float(u[4 * c]) * a1);
+                            v.y = fmaf(__uint_as_float(o[4 * c + 1]), a0, __uint_as_float(u[4 * c + 1]) * a1);
+                            v.z = fmaf(__uint_as_float(o[4 * c + 2]), a0, __uint_as_float(u[4 * c + 2]) * a1);
+                            v.w = fmaf(__uint_as_float(o[4 * c + 3]), a0, __uint_as_float(u[4 * c + 3]) * a1);
+                            dst[c] = v;
+                        }
+                    }
                 }
+                if (real && p.lse) p.lse[orow] = (M + log2f(L)) * kLn2;
+            } else {
+                timed_out = true;
             }
-            if (real && p.lse) p.lse[orow] = (m + log2f(l)) * kLn2;
         }
     }
     if (timed_out && lane == 0) atomicOr(p.err, KVC_EBIT_TIMEOUT);
@@ -384,7 +444,7 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
     }
 }
 
-// grid (1, KV head, tile of 128 / g positions), 224 threads.  Launched as a
+// grid (1, KV head, tile of 128 / g positions), 352 threads.  Launched as a
 // programmatic dependent in the mixed step: it reads only the chunk's row,
 // which the step before it does not write, so it never waits on that step.
 template <int D>

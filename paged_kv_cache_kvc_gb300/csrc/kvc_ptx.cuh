@@ -84,22 +84,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
-// The same wait without suspending in the barrier: the phase is tested, and the
-// thread sleeps ~`sleep_ns` between tests, so it sees the completion within about
-// that time (a suspended try_wait can wake up much later than its phase completes).
-__device__ __forceinline__ bool mbar_poll_bounded(uint32_t bar, uint32_t parity, uint32_t sleep_ns = 32,
-                                                  uint64_t limit_ns = 2000000000ull)
-{
-    if (mbar_test_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1; it < (1u << 26); ++it) {
-        __nanosleep(sleep_ns);
-        if (mbar_test_wait(bar, parity)) return true;
-        if ((it & 255u) == 0u && globaltimer_ns() - t0 > limit_ns) return false;
-    }
-    return false;
-}
-
 // Order this thread's earlier generic-proxy shared-memory accesses before
 // later async-proxy (TMA) writes to the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem()

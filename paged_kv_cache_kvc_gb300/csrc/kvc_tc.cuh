@@ -119,6 +119,21 @@ __device__ __forceinline__ void tc_mma_f16_warp(uint32_t d_tmem, uint64_t a_desc
         : "memory");
 }
 
+// The MMA with its A operand in tensor memory (warp-wide, one elected lane issues): row i of
+// A in lane i, 16-bit elements k = 2c, 2c + 1 in the low and high halves of column a_tmem + c
+// (K-major); B from shared memory as above.
+__device__ __forceinline__ void tc_mma_f16_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                       uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_commit_warp(uint32_t bar)
 {
     asm volatile(
