@@ -17,11 +17,13 @@
 // the two partial softmaxes of every row (the log-sum-exp merge of split
 // attention).  One stream's chain of score MMA -> softmax -> value MMA leaves
 // the tensor cores and the single MMA-issuing thread idle most of the time;
-// two independent chains fill each other's gaps.  352 threads:
+// two independent chains fill each other's gaps.  384 threads:
 //   warps 8, 9    TMA producers of stream 0 and 1: per stage the key rows and
 //                 value rows of its 4 blocks, one 16-row box per block, 128-byte
 //                 band and keys / values (128-byte swizzle), a ring of 3 stages.
-//   warp 10       MMA issuer (one elected lane), for both streams, per stage:
+//   warps 10, 11  MMA issuers of stream 0 and 1 (one elected lane each; the
+//                 issue of an MMA holds its thread while the pipe takes it, so
+//                 one thread per stream), per stage:
 //                   S[128 x 64]  = Q[128 x D] . K^T        (K-major A and B)
 //                   O[128 x D]  += P[128 x 64] . V[64 x D]  (A from TMEM, MN-major B)
 //                 S double-buffered per stream in TMEM; the softmax writes P as
@@ -45,7 +47,7 @@ namespace kvc {
 
 constexpr int kPtKeys = 64;                     // keys per stage
 constexpr int kPtRing = 3;                      // stages in flight per stream
-constexpr int kPtThreads = 352;
+constexpr int kPtThreads = 384;
 
 template <int D>
 struct PrefillTcCfg {
@@ -130,16 +132,18 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
         tmem_alloc(smem_u32(tmem_slot), C::COLS);
         tmem_relinquish();
     }
-    if (tid < 128) {   // query row tid (zero past the chunk): the K-major A operand of the score MMA
-        const int pos = pos0 + tid / g;
-        const uint16_t *qrow = p.q + (static_cast<size_t>(min(pos, n_q - 1)) * p.H_Q + h * g + tid % g) * D;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 v = pos < n_q ? *reinterpret_cast<const uint4 *>(qrow + c * 8) : make_uint4(0u, 0u, 0u, 0u);
-            sts128(sbase + C::Q + (c >> 3) * C::QBAND + sw128(tid, c & 7), v);
-        }
-        fence_proxy_async_smem();
+    // the query rows (zero past the chunk), the K-major A operand of the score MMA: row r is
+    // position pos0 + r / g, head h g + r mod g; consecutive threads take consecutive 16-byte
+    // chunks of a row, so a warp reads whole rows (g rows of a position are contiguous)
+#pragma unroll 2
+    for (int x = tid; x < 128 * (D / 8); x += kPtThreads) {
+        const int r = x / (D / 8), c = x % (D / 8), pos = pos0 + r / g;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (pos < n_q)
+            v = *reinterpret_cast<const uint4 *>(p.q + (static_cast<size_t>(pos) * p.H_Q + h * g + r % g) * D + c * 8);
+        sts128(sbase + C::Q + (c >> 3) * C::QBAND + sw128(r, c & 7), v);
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -203,11 +207,11 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
                                         100000000ull);
             }
         __syncwarp();
-    } else if (warp == 10) {
-        // ------------------------------------------------------------ MMA issuer (both streams)
+    } else if (warp == 10 || warp == 11) {
+        // ------------------------------------------------------------ MMA issuer of stream warp - 10
         constexpr uint32_t idesc_qk = tc_idesc_f16(128, kPtKeys, true, false, false);
         constexpr uint32_t idesc_pv = tc_idesc_f16(128, D, true, false, true);
-        // Issues whichever MMA is ready, stream by stream: the value MMA of a stream's stage
+        // Issues whichever MMA of its stream is ready: the value MMA of a stage
         // once its weights are in TMEM (it releases the stage), the score MMA of a stage once
         // its keys have landed and the value MMA two stages back has read the weights in its
         // score buffer.  Barriers are tested without blocking, lane 0 testing for the warp.
@@ -216,60 +220,57 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
             return __shfl_sync(kFull, r, 0) != 0u;
         };
         const uint64_t desc_q = tc_smem_desc(sbase + C::Q, 16, 1024, kSwizzle128B);
-        int jq[2] = {0, 0}, jp[2] = {0, 0};
-        const int n[2] = {s_count(0), s_count(1)};
+        const int s = warp - 10, n = s_count(s);
+        const uint32_t tm_s = tmem + s * 256;
+        int jq = 0, jp = 0;
         uint64_t idle_since = 0;
         uint32_t idle = 0;
-        while (jp[0] < n[0] || jp[1] < n[1]) {
+        while (jp < n) {
             bool progressed = false;
+            if (jp < jq && ready(pfull_bar(s, jp & 1), static_cast<uint32_t>((jp >> 1) & 1))) {
+                const int i = jp;
+                tc_fence_after();
+                const uint64_t b0 = tc_smem_desc(stage_addr(s, i % kPtRing) + C::BANDS * C::KBAND, C::KBAND, 1024,
+                                                 kSwizzle128B);
 #pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                const uint32_t tm_s = tmem + s * 256;
-                if (jp[s] < jq[s] && ready(pfull_bar(s, jp[s] & 1), static_cast<uint32_t>((jp[s] >> 1) & 1))) {
-                    const int i = jp[s];
-                    tc_fence_after();
-                    const uint64_t b0 = tc_smem_desc(stage_addr(s, i % kPtRing) + C::BANDS * C::KBAND, C::KBAND, 1024,
-                                                     kSwizzle128B);
-#pragma unroll
-                    for (int kk = 0; kk < kPtKeys / 16; ++kk)   // 16 keys: 8 TMEM columns of P, 2048 bytes of V rows
-                        tc_mma_f16_tmem_a_warp(tm_s + 128, tm_s + (i & 1) * kPtKeys + kk * 8,
-                                               tc_desc_advance(b0, kk * 2048), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit_warp(kvfree_bar(s, i % kPtRing));
-                    tc_commit_warp(pvdone_bar(s, i & 1));
-                    __syncwarp();
-                    ++jp[s];
-                    progressed = true;
-                }
-                if (jq[s] < n[s] && ready(full_bar(s, jq[s] % kPtRing), static_cast<uint32_t>((jq[s] / kPtRing) & 1)) &&
-                    (jq[s] < 2 ||
-                     (jq[s] - 2 < jp[s] &&
-                      ready(pvdone_bar(s, jq[s] & 1), static_cast<uint32_t>(((jq[s] - 2) >> 1) & 1))))) {
-                    const int i = jq[s], j = s_begin(s) + i, key0 = j * kPtKeys;
-                    const uint32_t st = stage_addr(s, i % kPtRing);
-                    // value rows of keys past the row's end or of blocks not loaded: zero
-                    const uint32_t vmask = vmask_sh[s * kPtRing + i % kPtRing];
-                    if (key0 + kPtKeys > total || vmask != (1u << BPS) - 1u) {
-                        for (int x = lane; x < kPtKeys * 8 * C::BANDS; x += 32) {
-                            const int row = x / (8 * C::BANDS), c = x % (8 * C::BANDS);
-                            if (key0 + row >= total || !(vmask >> (row >> 4) & 1u))
-                                sts128_zero(st + (C::BANDS + (c >> 3)) * C::KBAND + sw128(row, c & 7));
-                        }
-                        fence_proxy_async_smem();
+                for (int kk = 0; kk < kPtKeys / 16; ++kk)   // 16 keys: 8 TMEM columns of P, 2048 bytes of V rows
+                    tc_mma_f16_tmem_a_warp(tm_s + 128, tm_s + (i & 1) * kPtKeys + kk * 8,
+                                           tc_desc_advance(b0, kk * 2048), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                tc_commit_warp(kvfree_bar(s, i % kPtRing));
+                tc_commit_warp(pvdone_bar(s, i & 1));
+                __syncwarp();
+                ++jp;
+                progressed = true;
+            }
+            if (jq < n && ready(full_bar(s, jq % kPtRing), static_cast<uint32_t>((jq / kPtRing) & 1)) &&
+                (jq < 2 ||
+                 (jq - 2 < jp &&
+                  ready(pvdone_bar(s, jq & 1), static_cast<uint32_t>(((jq - 2) >> 1) & 1))))) {
+                const int i = jq, j = s_begin(s) + i, key0 = j * kPtKeys;
+                const uint32_t st = stage_addr(s, i % kPtRing);
+                // value rows of keys past the row's end or of blocks not loaded: zero
+                const uint32_t vmask = vmask_sh[s * kPtRing + i % kPtRing];
+                if (key0 + kPtKeys > total || vmask != (1u << BPS) - 1u) {
+                    for (int x = lane; x < kPtKeys * 8 * C::BANDS; x += 32) {
+                        const int row = x / (8 * C::BANDS), c = x % (8 * C::BANDS);
+                        if (key0 + row >= total || !(vmask >> (row >> 4) & 1u))
+                            sts128_zero(st + (C::BANDS + (c >> 3)) * C::KBAND + sw128(row, c & 7));
                     }
-                    __syncwarp();
-                    tc_fence_after();
-                    const uint64_t b0 = tc_smem_desc(st, 16, 1024, kSwizzle128B);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)   // 16 channels (32 bytes) per MMA, 4 per 128-byte band
-                        tc_mma_f16_warp(tm_s + (i & 1) * kPtKeys,
-                                        tc_desc_advance(desc_q, (kk >> 2) * C::QBAND + (kk & 3) * 32),
-                                        tc_desc_advance(b0, (kk >> 2) * C::KBAND + (kk & 3) * 32), idesc_qk,
-                                        kk > 0 ? 1u : 0u);
-                    tc_commit_warp(sfull_bar(s, i & 1));
-                    __syncwarp();
-                    ++jq[s];
-                    progressed = true;
+                    fence_proxy_async_smem();
                 }
+                __syncwarp();
+                tc_fence_after();
+                const uint64_t b0 = tc_smem_desc(st, 16, 1024, kSwizzle128B);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)   // 16 channels (32 bytes) per MMA, 4 per 128-byte band
+                    tc_mma_f16_warp(tm_s + (i & 1) * kPtKeys,
+                                    tc_desc_advance(desc_q, (kk >> 2) * C::QBAND + (kk & 3) * 32),
+                                    tc_desc_advance(b0, (kk >> 2) * C::KBAND + (kk & 3) * 32), idesc_qk,
+                                    kk > 0 ? 1u : 0u);
+                tc_commit_warp(sfull_bar(s, i & 1));
+                __syncwarp();
+                ++jq;
+                progressed = true;
             }
             if (progressed) {
                 idle = 0;
@@ -444,7 +445,7 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
     }
 }
 
-// grid (1, KV head, tile of 128 / g positions), 352 threads.  Launched as a
+// grid (1, KV head, tile of 128 / g positions), 384 threads.  Launched as a
 // programmatic dependent in the mixed step: it reads only the chunk's row,
 // which the step before it does not write, so it never waits on that step.
 template <int D>
