@@ -61,7 +61,8 @@ struct PrefillTcCfg {
     // per stream: full[R], kvfree[R], s_full[2], p_full[2], pv_done[2]
     static constexpr int BARS_PER_STREAM = 2 * kPtRing + 6;
     static constexpr int VMASK = BARS + 2 * BARS_PER_STREAM * 8;   // [stream][slot] loaded-block masks
-    static constexpr int XCH = VMASK + 2 * kPtRing * 4;            // stream 1's (m, l) per row for the merge
+    static constexpr int ABORT = VMASK + 2 * kPtRing * 4;          // set when a wait expires anywhere
+    static constexpr int XCH = ABORT + 8;                          // stream 1's (m, l) per row for the merge
     static constexpr int SLOT = XCH + 128 * 8;
     static constexpr int SMEM = 1024 + SLOT + 16;
     static constexpr uint32_t COLS = 512;   // stream s: S/P[0] s*256 + 0..63, S/P[1] + 64..127, O from s*256 + 128
@@ -110,6 +111,7 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
     auto pvdone_bar = [&](int s, int b) { return sbar(s, 2 * kPtRing + 4 + b); };
     auto stage_addr = [&](int s, int r) { return sbase + C::RING + (s * kPtRing + r) * C::STAGE; };
     volatile uint32_t *vmask_sh = reinterpret_cast<volatile uint32_t *>(smem + C::VMASK);
+    volatile uint32_t *abort_sh = reinterpret_cast<volatile uint32_t *>(smem + C::ABORT);
     float2 *xch = reinterpret_cast<float2 *>(smem + C::XCH);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SLOT);
 
@@ -127,6 +129,7 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
         }
         fence_barrier_init();
         prefetch_tensormap(&tmap16);
+        *abort_sh = 0u;
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), C::COLS);
@@ -171,6 +174,7 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
             if (i >= kPtRing) {
                 const bool ok = mbar_wait_bounded(kvfree_bar(s, r), static_cast<uint32_t>(((i / kPtRing) - 1) & 1));
                 if (!__all_sync(kFull, ok)) {
+                    if (lane == 0) *abort_sh = 1u;
                     timed_out = true;
                     break;
                 }
@@ -278,7 +282,8 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
             } else if ((++idle & 63u) == 0u) {   // bounded: 2 s without progress is an expired wait
                 const uint64_t now = globaltimer_ns();
                 if (idle_since == 0) idle_since = now;
-                else if (now - idle_since > 2000000000ull) {
+                if (__any_sync(kFull, *abort_sh != 0u) || now - idle_since > 2000000000ull) {
+                    if (lane == 0) *abort_sh = 1u;
                     timed_out = true;
                     break;
                 }
@@ -296,6 +301,10 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
         int i = 0;
         for (; i < n; ++i) {
             const int j = b + i, sb = i & 1;
+            if (__any_sync(kFull, *abort_sh != 0u)) {   // a wait expired elsewhere in the CTA
+                timed_out = true;
+                break;
+            }
             const bool ok1 = mbar_wait_bounded(sfull_bar(s, sb), static_cast<uint32_t>((i >> 1) & 1));
             tc_fence_after();
             uint32_t r0[32], r1[32];
@@ -367,7 +376,11 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
                 pk[c / 2] = pack_bf16(p0, p1);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            if (!group_all(ok1 && ok3, vote_id)) {   // one vote per stage: a wait expired in the group
+            // a wait expired: the warp leaves the loop together and tells the others, which leave
+            // theirs at their next stage (their waits are bounded); the group's vote below
+            // gathers the warps again
+            if (!__all_sync(kFull, ok1 && ok3)) {
+                if (lane == 0) *abort_sh = 1u;
                 timed_out = true;
                 break;
             }
