@@ -448,6 +448,7 @@ static void fill_common(DecodeParams &p, const kvc_pool *pool, int32_t layer, co
     p.out = out;
     p.lse = lse;
     p.err = pool->err;
+    p.pool = pool->base;   // the fused append's stores and the kernels' speculative L2 prefetch
 }
 
 static kvc_status dispatch(kvc_pool *pool, DecodeParams &p, cudaStream_t stream)

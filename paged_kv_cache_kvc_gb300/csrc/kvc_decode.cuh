@@ -760,7 +760,22 @@ template <int D, int NT, int KIND, bool PSPLIT, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmap,
                                                           const DecodeParams p)
 {
+    using C = DecodeCfg<D, KIND>;
     allow_dependent_launch();
+    // While the kernel before it drains: a speculative L2 prefetch of the blocks the CTA's
+    // rings load first, from the lengths and table as they stand now (they may still change;
+    // nothing here is used but as a cache hint, and the CTA reads them again after the wait).
+    if (!CAUSAL && p.lens && p.pool && threadIdx.x < kWarps * C::R) {
+        const int b = blockIdx.z, h = blockIdx.y;
+        const int len_s = p.lens[b] + (p.k_new ? 1 : 0);
+        const int blk = blockIdx.x * p.chunk + threadIdx.x;
+        if (blk < p.max_blocks && blk * kBS < len_s) {
+            const int32_t e = p.bt[static_cast<int64_t>(b) * p.bt_stride + blk];
+            if (e >= 0 && static_cast<int64_t>(e) < p.N)
+                prefetch_l2_bulk(p.pool + ((static_cast<int64_t>(p.layer) * p.N + e) * p.H_KV + h) * C::STAGE,
+                                 C::STAGE);
+        }
+    }
     grid_dependency_wait();   // launched as a programmatic dependent: nothing global is touched before this
     decode_cta<D, NT, KIND, PSPLIT, CAUSAL>(tmap, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }

@@ -159,6 +159,19 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // While the kernel before it drains: a speculative L2 prefetch of the split's first 3
+    // tiles, from the lengths and table as they stand now (they may still change; nothing
+    // here is used but as a cache hint, and everything below the wait reads them again).
+    if (tid < kTcRing * kTcBlocks && p.lens && p.pool) {
+        const int len_s = p.lens[b] + (p.k_new ? 1 : 0);
+        const int blk = split * p.chunk + tid;
+        if (blk < p.max_blocks && blk * kBS < len_s) {
+            const int32_t e = p.bt[static_cast<int64_t>(b) * p.bt_stride + blk];
+            if (e >= 0 && static_cast<int64_t>(e) < p.N)
+                prefetch_l2_bulk(p.pool + ((static_cast<int64_t>(p.layer) * p.N + e) * p.H_KV + h) * (2 * kBS * D * 2),
+                                 2 * kBS * D * 2);
+        }
+    }
     // Launched as a programmatic dependent of the kernel before it on the stream: the set-up
     // above overlaps that kernel's tail, and this wait (a no-op in an ordinary launch) holds
     // the CTA until that kernel has finished and its writes are visible.  Everything below

@@ -62,7 +62,7 @@ struct DecodeParams {
     // written at position lens[b] before attending to lens[b] + 1 positions; nullptr = none
     const uint16_t *k_new;
     const uint16_t *v_new;
-    uint8_t *pool;           // pool base (the fused append's global store)
+    uint8_t *pool;           // pool base (the fused append's global store, the L2 prefetch)
     // split-K arrival counters [B][H_KV], zero between launches; nullptr = merge in a separate kernel
     uint32_t *counters;
 };

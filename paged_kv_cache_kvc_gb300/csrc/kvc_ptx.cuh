@@ -120,6 +120,14 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return pol;
 }
 
+// A hint to bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2
+// through the copy engine; nothing is written and no completion is tracked.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
