@@ -449,6 +449,7 @@ static void fill_common(DecodeParams &p, const kvc_pool *pool, int32_t layer, co
     p.lse = lse;
     p.err = pool->err;
     p.pool = pool->base;   // the fused append's stores and the kernels' speculative L2 prefetch
+    p.stall_loads = std::getenv("KVC_TEST_STALL") ? 1 : 0;
 }
 
 static kvc_status dispatch(kvc_pool *pool, DecodeParams &p, cudaStream_t stream)

@@ -488,7 +488,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &tmap, const Decode
     };
     auto issue = [&](int jj, int jbase) {   // warp-collective; lane 0 issues
         const int32_t phys = entry(jj, jbase);
-        if (lane == 0) {
+        if (lane == 0 && !p.stall_loads) {
             const uint32_t bar = bar_base + 8u * static_cast<uint32_t>(jj % C::R);
             if (phys < 0 || static_cast<int64_t>(phys) >= p.N) {
                 atomicOr(p.err, KVC_EBIT_BAD_BLOCK);

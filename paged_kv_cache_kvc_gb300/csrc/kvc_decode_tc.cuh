@@ -218,8 +218,9 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
             // ------------------------------------------------------------ TMA producers (4: keys, 6: values)
             const int kv = warp == 6 ? 1 : 0;
             int32_t ecur = load_entry(lane), enext = load_entry(32 + lane);
+            const int nload = p.stall_loads ? 0 : nt;   // the test hook withholds every load
             int j = 0;
-            for (; j < nt; ++j) {
+            for (; j < nload; ++j) {
                 if (j > 0 && (j & 3) == 0) {
                     ecur = enext;
                     enext = load_entry((j / 4 + 1) * 32 + lane);

@@ -65,6 +65,9 @@ struct DecodeParams {
     uint8_t *pool;           // pool base (the fused append's global store, the L2 prefetch)
     // split-K arrival counters [B][H_KV], zero between launches; nullptr = merge in a separate kernel
     uint32_t *counters;
+    // test hook (KVC_TEST_STALL set): the copy producers issue no load and never arrive, so every
+    // bounded wait expires and the launch reports KVC_ERR_TIMEOUT
+    int32_t stall_loads;
 };
 
 kvc_status cuda_status(cudaError_t e);

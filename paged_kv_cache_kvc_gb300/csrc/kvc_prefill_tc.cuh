@@ -163,8 +163,9 @@ __device__ __forceinline__ void prefill_tc_cta(const CUtensorMap &tmap16, const 
         // lane l holds entry 32 w + l of table window w (the stages of window w: SPW w .. SPW w + SPW - 1)
         int w = b / SPW;
         int32_t ecur = load_entry(32 * w + lane), enext = load_entry(32 * (w + 1) + lane);
+        const int nload = p.stall_loads ? 0 : n;   // the test hook withholds every load
         int i = 0;
-        for (; i < n; ++i) {
+        for (; i < nload; ++i) {
             const int j = b + i, r = i % kPtRing;
             if (j / SPW != w) {
                 ++w;
