@@ -72,8 +72,8 @@ typedef enum {
     KVC_ERR_STALE = 6,        /* a lease stamp no longer current: the sequence was released or one of its
                                * table entries was replaced (kvc_alloc_check) */
     KVC_ERR_TIMEOUT = 7,      /* a bounded device-side wait expired (2 s); results of that call are invalid.
-                                 The environment variable KVC_TEST_STALL (a test hook) makes every call's
-                                 copies be withheld so that its waits expire */
+                               * The environment variable KVC_TEST_STALL (a test hook) withholds every
+                               * call's copies so that its waits expire */
     KVC_ERR_CUDA = 8,         /* a CUDA runtime call failed */
     KVC_ERR_UNSUPPORTED = 9   /* a valid shape this build has no kernel for (see each call) */
 } kvc_status;
