@@ -79,6 +79,8 @@ KERNEL_SOURCES = {
     "decode": ["kvc_decode.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_attn.cu"],
     "mixed": ["kvc_decode.cuh", "kvc_prefill.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_attn.cu"],
     "decode_tc": ["kvc_decode_tc.cuh", "kvc_tc.cuh", "kvc_decode.cuh", "kvc_ptx.cuh", "kvc_internal.h", "kvc_attn.cu"],
+    "decode_tc8": ["kvc_decode_tc8.cuh", "kvc_decode_tc.cuh", "kvc_tc.cuh", "kvc_decode.cuh", "kvc_ptx.cuh",
+                   "kvc_internal.h", "kvc_attn.cu"],
     "prefill_tc": ["kvc_prefill_tc.cuh", "kvc_decode_tc.cuh", "kvc_tc.cuh", "kvc_decode.cuh", "kvc_ptx.cuh",
                    "kvc_internal.h", "kvc_attn.cu"],
 }
@@ -86,7 +88,8 @@ KERNEL_SOURCES = {
 
 def step_kernel(w) -> str:
     """The kernels the library picks for this workload's step (the same rule as its dispatch)."""
-    tc = os.environ.get("KVC_TC", "1")[:1] != "0" and w.dtype == "bf16" and w.bs == 16
+    tc_on = os.environ.get("KVC_TC", "1")[:1] != "0" and w.bs == 16
+    tc = tc_on and w.dtype == "bf16"
     if w.prefill is not None:
         if tc:
             return ("kvc_mixed_step: decode_kernel with fused append, then prefill_tc_kernel (tcgen05) as its "
@@ -94,6 +97,9 @@ def step_kernel(w) -> str:
         return "mixed_kernel: decode step with fused append and the prefill chunk in one launch (kvc_mixed_step)"
     if tc and w.H_Q == 32 * w.H_KV and w.d_h == 128:
         return "decode_tc_kernel (tcgen05, TMEM) with fused append, then merge_kernel (kvc_decode_step)"
+    if tc_on and w.dtype == "fp8" and w.H_Q == 32 * w.H_KV and w.d_h == 128:
+        return ("decode_tc8_kernel (tcgen05, TMEM; e4m3 codes widened to f16 in shared memory) with fused append, "
+                "then merge_kernel (kvc_decode_step)")
     return "decode_kernel with fused append (kvc_decode_step)"
 
 
@@ -333,7 +339,7 @@ def time_steps(run, K: int, stream):
 # generator (N(0,1) rounded to bf16, then stored as each pool stores it), so a
 # 32 GiB pool is ready in seconds; the block tables and lengths are the
 # workload's own.
-EXTRA_WORKLOADS = "full_pool,sweep_hkv8_fp8,sweep_hkv8_bf16,sweep_hkv1_bf16,prefill_chunk"
+EXTRA_WORKLOADS = "full_pool,sweep_hkv8_fp8,sweep_hkv8_bf16,sweep_hkv1_bf16,sweep_hkv1_fp8,prefill_chunk"
 EXTRA_SECONDS = 1.5
 
 

@@ -11,7 +11,8 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libkvc.so")
 ROOT = os.path.dirname(HERE)
 
-SOURCES = ["kvc_core.cu", "kvc_attn.cu", "kvc_decode_bf16.cu", "kvc_decode_fp8.cu", "kvc_decode_int4.cu", "kvc_decode_tc.cu", "kvc_prefill_tc.cu", "kvc_noalloc.cu", "kvc_alloc.cu"]
+SOURCES = ["kvc_core.cu", "kvc_attn.cu", "kvc_decode_bf16.cu", "kvc_decode_fp8.cu", "kvc_decode_int4.cu",
+           "kvc_decode_tc.cu", "kvc_decode_tc8.cu", "kvc_prefill_tc.cu", "kvc_noalloc.cu", "kvc_alloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr",
               "-I" + os.path.join(ROOT, "include")]

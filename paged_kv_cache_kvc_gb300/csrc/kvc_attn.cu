@@ -340,14 +340,15 @@ void choose_split_tc(const kvc_pool *pool, int units, int max_blocks, int ctas_p
     *max_splits = (max_blocks + *chunk - 1) / *chunk;
 }
 
-// The tensor-memory kernel serves decode steps of 32-head groups on d_h 128 bf16 pools
-// (KVC_TC=0 selects the split kernel for them).
+// The tensor-memory kernels serve decode steps of 32-head groups on d_h 128 bf16 and
+// e4m3 pools (KVC_TC=0 selects the split kernel for them).
 DecodeKernel tc_kernel_for(const kvc_pool *pool, const DecodeParams &p)
 {
     const char *e = std::getenv("KVC_TC");
-    if ((e && e[0] == '0') || !p.lens || p.ppu != 1 || !pool->tmap16_ok || pool->bs != kBS)
-        return DecodeKernel{nullptr, 0, 0};
-    return select_decode_tc(pool->D, p.g, pool->dtype);
+    if ((e && e[0] == '0') || !p.lens || p.ppu != 1 || pool->bs != kBS) return DecodeKernel{nullptr, 0, 0};
+    const DecodeKernel k = select_decode_tc(pool->D, p.g, pool->dtype);
+    if (!k.fn || !(k.tmap16 ? pool->tmap16_ok : pool->tmap_ok)) return DecodeKernel{nullptr, 0, 0};
+    return k;
 }
 
 static kvc_status run_decode_tc(kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream)
@@ -366,9 +367,9 @@ static kvc_status run_decode_tc(kvc_pool *pool, DecodeParams &p, const DecodeKer
         p.part_o = ws_data(pool);
         p.part_ml = reinterpret_cast<float2 *>(p.part_o + n * pool->D);
     }
-    void *args[] = {const_cast<CUtensorMap *>(&pool->tmap16), &p};
+    void *args[] = {const_cast<CUtensorMap *>(k.tmap16 ? &pool->tmap16 : &pool->tmap), &p};
     const cudaError_t e =
-        launch_programmatic_dependent(k.fn, dim3(p.max_splits, p.H_KV, p.B), dim3(kTcThreads), k.smem, stream, args);
+        launch_programmatic_dependent(k.fn, dim3(p.max_splits, p.H_KV, p.B), dim3(k.threads), k.smem, stream, args);
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (p.max_splits > 1) return launch_split_merge(p, pool->D, stream);

@@ -785,6 +785,8 @@ struct DecodeKernel {
     const void *fn;
     int smem;
     int ctas_per_sm;
+    int threads = kThreads;   // block size
+    bool tmap16 = false;      // takes the pool's 16-row tensor map (else the map of whole blocks)
 };
 
 template <int D, int NT, int KIND, bool PSPLIT, bool CAUSAL = false>

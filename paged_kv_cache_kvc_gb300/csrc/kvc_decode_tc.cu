@@ -1,4 +1,4 @@
-// Instances of the tensor-memory (tcgen05) decode kernel.
+// Instances of the tensor-memory (tcgen05) decode kernels (bf16 pools; e4m3 pools in kvc_decode_tc8.cu).
 #include "kvc_decode_tc.cuh"
 
 namespace kvc {
@@ -11,6 +11,8 @@ static DecodeKernel decode_tc_instance()
         r.fn = reinterpret_cast<const void *>(&decode_tc_kernel<G>);
         r.smem = kTcSmem;
         r.ctas_per_sm = 0;
+        r.threads = kTcThreads;
+        r.tmap16 = true;
         if (cudaFuncSetAttribute(&decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem) ==
             cudaSuccess) {
             int n = 0;
@@ -25,8 +27,10 @@ static DecodeKernel decode_tc_instance()
 
 DecodeKernel select_decode_tc(int D, int g, int dtype)
 {
-    if (D != 128 || dtype != KVC_BF16 || g != 32) return DecodeKernel{nullptr, 0, 0};
-    return decode_tc_instance<32>();
+    if (D != 128 || g != 32) return DecodeKernel{nullptr, 0, 0};
+    if (dtype == KVC_BF16) return decode_tc_instance<32>();
+    if (dtype == KVC_FP8_E4M3) return select_decode_tc8(D, g);
+    return DecodeKernel{nullptr, 0, 0};
 }
 
 }  // namespace kvc

@@ -574,8 +574,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
     decode_tc_cta<G>(tmap16, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
-// The tensor-memory decode kernel for a shape, or fn = nullptr (d_h 128 bf16 pools, 32-head groups).
+// The tensor-memory decode kernel for a shape, or fn = nullptr (d_h 128 bf16 or e4m3 pools, 32-head groups).
 DecodeKernel select_decode_tc(int D, int g, int dtype);
+// The e4m3 form alone (kvc_decode_tc8.cu).
+DecodeKernel select_decode_tc8(int D, int g);
 // The same for a launch's parameters (decode steps only; fn = nullptr when KVC_TC=0).
 DecodeKernel tc_kernel_for(const kvc_pool *pool, const DecodeParams &p);
 

@@ -146,8 +146,8 @@ extern "C" kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, con
         p.part_ml = reinterpret_cast<float2 *>(scratch + n * pool->D);
     }
     const dim3 grid(p.max_splits, p.H_KV, p.B);
-    void *args[] = {const_cast<CUtensorMap *>(tc.fn ? &pool->tmap16 : &pool->tmap), &p};
-    const cudaError_t e = cudaLaunchKernel(k.fn, grid, dim3(tc.fn ? kTcThreads : kThreads), args, k.smem,
+    void *args[] = {const_cast<CUtensorMap *>(k.tmap16 ? &pool->tmap16 : &pool->tmap), &p};
+    const cudaError_t e = cudaLaunchKernel(k.fn, grid, dim3(k.threads), args, k.smem,
                                            static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_status(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -1,6 +1,6 @@
 """The tensor-memory (tcgen05) kernels against the oracle, through the C ABI.
 
-MQA decode (32 query heads per KV head, bf16, d_h 128) and the prefill chunk
+MQA decode (32 query heads per KV head, bf16 and e4m3, d_h 128) and the prefill chunk
 (bf16, d_h 64 / 128, every group size) run on tensor-memory kernels; every
 case here also runs with KVC_TC=0 (the warp-level kernels) so both paths are
 held to the same oracle.  Shapes start small (one sequence of two blocks, one
@@ -58,32 +58,41 @@ MQA_LENS = [[20], [127], [128], [129], [5, 300, 1000], [4000, 1, 2500, 17], [819
 
 @pytest.mark.parametrize("lens", MQA_LENS, ids=[f"B{len(x)}_max{max(x)}" for x in MQA_LENS])
 @pytest.mark.parametrize("fused", [False, True], ids=["append_then_attend", "fused_step"])
-def test_mqa_tensor_memory_decode(kvc, lens, fused):
-    w = synth.make_workload("custom", B=len(lens), H_Q=32, H_KV=1, d_h=128, lens=lens, seed=sum(lens) % 97)
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_mqa_tensor_memory_decode(kvc, lens, fused, dtype):
+    w = synth.make_workload("custom", B=len(lens), H_Q=32, H_KV=1, d_h=128, lens=lens, dtype=dtype,
+                            seed=sum(lens) % 97)
     _, _, (err_tc, _) = _case(kvc, w, fused)
     _, _, (err_mma, _) = _case(kvc, w, fused, {"KVC_TC": "0"})
-    # the tensor-memory kernel feeds ~16-bit weights (bf16 high + low parts) to the value
-    # mixture; the split kernel's 32-head groups feed one bf16 part
-    assert err_tc <= max(2e-4, err_mma), (err_tc, err_mma)
+    # the tensor-memory kernels feed ~16-bit weights (high + low parts, bf16 or f16) to the
+    # value mixture; the split kernel's 32-head groups feed one part.  On e4m3 pools both
+    # kernels round q s_K to f16 (11 bits), the error that dominates, and accumulate the scores
+    # in different orders: there the tensor-memory kernel is held to 1.5x the split kernel's
+    # error (both stay ~100x inside the e4m3 tolerance)
+    assert err_tc <= max(2e-4, (1.5 if dtype == "fp8" else 1.0) * err_mma), (err_tc, err_mma)
 
 
 @pytest.mark.parametrize("chunk", ["8", "16", "24", "4096"])
-def test_mqa_tensor_memory_split_sizes(kvc, chunk):
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_mqa_tensor_memory_split_sizes(kvc, chunk, dtype):
     """One tile per split up to one split per sequence (partials merged or not)."""
-    w = synth.make_workload("custom", B=3, H_Q=32, H_KV=1, d_h=128, lens=[3000, 129, 700], seed=5)
+    w = synth.make_workload("custom", B=3, H_Q=32, H_KV=1, d_h=128, lens=[3000, 129, 700], dtype=dtype, seed=5)
     _case(kvc, w, True, {"KVC_SPLIT_CHUNK": chunk})
 
 
-def test_mqa_tensor_memory_several_kv_heads(kvc):
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_mqa_tensor_memory_several_kv_heads(kvc, dtype):
     """H_Q = 64 over 2 KV heads: 32-head groups, grid over (split, KV head, sequence)."""
-    w = synth.make_workload("custom", B=2, H_Q=64, H_KV=2, d_h=128, lens=[1500, 260], seed=9)
+    w = synth.make_workload("custom", B=2, H_Q=64, H_KV=2, d_h=128, lens=[1500, 260], dtype=dtype, seed=9)
     _case(kvc, w, True)
 
 
-def test_mqa_tensor_memory_empty_and_bad_entries(kvc):
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_mqa_tensor_memory_empty_and_bad_entries(kvc, dtype):
     """An empty sequence gives 0 / -inf; a table entry outside the pool is skipped
     and reported, and the pool stays usable."""
-    w = synth.make_workload("custom", B=3, H_Q=32, H_KV=1, d_h=128, lens=[0, 300, 40], seed=13, spare_blocks=2)
+    w = synth.make_workload("custom", B=3, H_Q=32, H_KV=1, d_h=128, lens=[0, 300, 40], dtype=dtype, seed=13,
+                            spare_blocks=2)
     g = GpuCase(kvc, w, fill_byte=0)
     try:
         ld = layer_data(w, 0)

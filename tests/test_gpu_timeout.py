@@ -8,7 +8,8 @@ first wait of every consumer runs out -- nothing is in flight, nothing faults.
 Each case checks the status, then runs the same call without the hook on the
 same pool and compares it with the oracle: the context and the pool stay
 usable.  Cases: the split kernel (bf16 GQA and e4m3), the tensor-memory MQA
-kernel through the fused step, and the tensor-memory prefill kernel.
+kernels (bf16 and e4m3) through the fused step, and the tensor-memory prefill
+kernel.
 """
 import os
 
@@ -31,7 +32,7 @@ def _stalled(fn):
         os.environ.pop("KVC_TEST_STALL", None)
 
 
-DECODE_CASES = [("bf16", 8, [300, 40]), ("fp8", 8, [500, 17]), ("bf16", 1, [700, 129])]
+DECODE_CASES = [("bf16", 8, [300, 40]), ("fp8", 8, [500, 17]), ("bf16", 1, [700, 129]), ("fp8", 1, [900, 33])]
 
 
 @pytest.mark.parametrize("dtype,H_KV,lens", DECODE_CASES,
