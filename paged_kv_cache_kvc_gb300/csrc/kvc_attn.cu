@@ -321,22 +321,28 @@ static kvc_status run_mixed(kvc_pool *pool, DecodeParams &pd, DecodeParams &pp, 
     return KVC_OK;
 }
 
-// Splits of the tensor-memory decode kernel: whole 128-token tiles, and about one
-// CTA per resident slot (one per SM): its 3-stage ring keeps 128 KiB in flight,
-// so more CTAs than slots only add split partials.  KVC_SPLIT_CHUNK overrides
-// (rounded up to whole tiles).
-void choose_split_tc(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits)
+// Splits of the tensor-memory decode kernels: about one CTA per resident slot (one
+// per SM; the ring keeps ~100 KiB in flight, so more CTAs than slots only add split
+// partials), the longest row's blocks shared evenly among them, rounded up to a
+// multiple of `unit` blocks.  A split walks 128-token tiles from its first block, so
+// the kernels take any split; the e4m3 kernel runs fastest with even shares (unit 1:
+// the CTA with the most bytes stays close to the mean), the bf16 kernel with whole
+// tiles (unit 8; even shares measured 8 % slower).  KVC_SPLIT_CHUNK overrides
+// (blocks per split, rounded up to the unit).
+void choose_split_tc(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int unit, int *chunk,
+                     int *max_splits)
 {
     const int tiles = (max_blocks + kTcBlocks - 1) / kTcBlocks;
-    int ct = 0;
-    if (const char *e = std::getenv("KVC_SPLIT_CHUNK")) ct = (std::atoi(e) + kTcBlocks - 1) / kTcBlocks;
-    if (ct <= 0) {
+    unit = std::max(unit, 1);
+    int cb = 0;
+    if (const char *e = std::getenv("KVC_SPLIT_CHUNK")) cb = std::atoi(e);
+    if (cb <= 0) {
         const double slots = static_cast<double>(pool->num_sms) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
         long ns = units > 0 ? std::lround(slots / units) : 1;
         ns = std::max(1L, std::min(ns, static_cast<long>(tiles)));
-        ct = static_cast<int>((tiles + ns - 1) / ns);
+        cb = static_cast<int>((max_blocks + ns - 1) / ns);
     }
-    *chunk = ct * kTcBlocks;
+    *chunk = (cb + unit - 1) / unit * unit;
     *max_splits = (max_blocks + *chunk - 1) / *chunk;
 }
 
@@ -354,7 +360,7 @@ DecodeKernel tc_kernel_for(const kvc_pool *pool, const DecodeParams &p)
 static kvc_status run_decode_tc(kvc_pool *pool, DecodeParams &p, const DecodeKernel &k, cudaStream_t stream)
 {
     if (k.ctas_per_sm <= 0) return KVC_ERR_CUDA;
-    choose_split_tc(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits);
+    choose_split_tc(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, k.split_unit, &p.chunk, &p.max_splits);
     if (p.max_splits > 65535) return KVC_ERR_UNSUPPORTED;
     p.counters = nullptr;   // splits are merged by merge_kernel
     p.part_o = nullptr;

@@ -787,6 +787,7 @@ struct DecodeKernel {
     int ctas_per_sm;
     int threads = kThreads;   // block size
     bool tmap16 = false;      // takes the pool's 16-row tensor map (else the map of whole blocks)
+    int split_unit = 1;       // tensor-memory kernels: blocks per split a multiple of this
 };
 
 template <int D, int NT, int KIND, bool PSPLIT, bool CAUSAL = false>

@@ -13,6 +13,7 @@ static DecodeKernel decode_tc_instance()
         r.ctas_per_sm = 0;
         r.threads = kTcThreads;
         r.tmap16 = true;
+        r.split_unit = kTcBlocks;   // whole tiles
         if (cudaFuncSetAttribute(&decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem) ==
             cudaSuccess) {
             int n = 0;

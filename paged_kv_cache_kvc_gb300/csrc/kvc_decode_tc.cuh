@@ -188,10 +188,12 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
         for (int i = tid; i < G * D; i += kTcThreads) p.out[(static_cast<size_t>(b) * p.H_Q + hq0) * D + i] = 0.f;
         if (p.lse && tid < G) p.lse[static_cast<size_t>(b) * p.H_Q + hq0 + tid] = -INFINITY;
     }
-    const int blk0 = split * p.chunk;   // chunk: a multiple of 8 blocks
+    // split: blocks blk0 .. blk_end - 1, walked as 128-token tiles from blk0 (the last one may be partial;
+    // blocks past blk_end belong to the next split and count here as unstaged)
+    const int blk0 = split * p.chunk;
     if (blk0 < nblk) {   // uniform over the CTA: this split holds blocks
-        const int tile0 = blk0 / kTcBlocks;
-        const int nt = (min(nblk, blk0 + p.chunk) - blk0 + kTcBlocks - 1) / kTcBlocks;
+        const int blk_end = min(nblk, blk0 + p.chunk);
+        const int nt = (blk_end - blk0 + kTcBlocks - 1) / kTcBlocks;
         const int ns = (nblk + p.chunk - 1) / p.chunk;
         const int32_t *bt_row = p.bt + static_cast<int64_t>(b) * p.bt_stride;
         const int64_t row_layer = static_cast<int64_t>(p.layer) * p.N;
@@ -211,8 +213,8 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
         bool timed_out = false;
         // table entries of the CTA's blocks, 32 (4 tiles) at a time in registers, one window ahead:
         // lane l holds block 32 w + l of window w
-        const int bbase = tile0 * kTcBlocks;
-        auto load_entry = [&](int rel) -> int32_t { return bbase + rel < nblk ? __ldg(bt_row + bbase + rel) : -1; };
+        const int bbase = blk0;
+        auto load_entry = [&](int rel) -> int32_t { return bbase + rel < blk_end ? __ldg(bt_row + bbase + rel) : -1; };
 
         if (warp == 4 || warp == 6) {
             // ------------------------------------------------------------ TMA producers (4: keys, 6: values)
@@ -235,7 +237,7 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
                 }
                 const int32_t e = __shfl_sync(kFull, ecur, (j & 3) * kTcBlocks + (lane & 7));
                 const int blk = bbase + j * kTcBlocks + lane;
-                const bool in = lane < kTcBlocks && blk < nblk;
+                const bool in = lane < kTcBlocks && blk < blk_end;
                 const bool v = in && e >= 0 && static_cast<int64_t>(e) < p.N;
                 if (kv == 0 && in && !v) atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
                 const uint32_t mask = __ballot_sync(kFull, v);
@@ -293,7 +295,7 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
                     const uint32_t vst = sbase + kTcV + (jp % kTcRing) * kTcSlot;
                     // positions that must contribute nothing: past the sequence end, or in a block whose
                     // table entry is bad; their value rows are zeroed (their weights are 0; 0 * NaN is not)
-                    const int tok0 = (tile0 + jp) * kTcTok;
+                    const int tok0 = blk0 * kBS + jp * kTcTok;
                     const uint32_t vmask = (vmasks >> (8 * (jp % kTcRing))) & 0xFFu;
                     bool fix = tok0 + kTcTok > len || vmask != 0xFFu;
                     if (fix) {
@@ -341,10 +343,10 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
                         enext = load_entry((jq / 4 + 1) * 32 + lane);
                     }
                     const uint32_t kst = sbase + (jq % kTcRing) * kTcSlot;
-                    const int tok0 = (tile0 + jq) * kTcTok;
+                    const int tok0 = blk0 * kBS + jq * kTcTok;
                     const int32_t e = __shfl_sync(kFull, ecur, (jq & 3) * kTcBlocks + (lane & 7));
                     const bool bv =
-                        bbase + jq * kTcBlocks + (lane & 7) < nblk && e >= 0 && static_cast<int64_t>(e) < p.N;
+                        bbase + jq * kTcBlocks + (lane & 7) < blk_end && e >= 0 && static_cast<int64_t>(e) < p.N;
                     const uint32_t vmask = __ballot_sync(kFull, bv) & 0xFFu;
                     vmasks = (vmasks & ~(0xFFu << (8 * (jq % kTcRing)))) | (vmask << (8 * (jq % kTcRing)));
                     // fused append: the step's own key row, into the pool and into the slot (its value row
@@ -434,7 +436,7 @@ __device__ __forceinline__ void decode_tc_cta(const CUtensorMap &tmap16, const D
                 tc_fence_before();
                 mbar_arrive(sfree_bar(sb));
 
-                const int tok = (tile0 + j) * kTcTok + tid;
+                const int tok = blk0 * kBS + j * kTcTok + tid;
                 const bool valid = tok < len && e_tok >= 0 && static_cast<int64_t>(e_tok) < p.N;
                 // d = scale s - m (log2 units) per head; a reference moves when some d exceeds the
                 // slack (a reference of -inf: d = +inf).  Invalid positions weigh nothing.

@@ -13,6 +13,7 @@ static DecodeKernel decode_tc8_instance()
         r.ctas_per_sm = 0;
         r.threads = kT8Threads;
         r.tmap16 = false;   // boxes of whole blocks (keys and values, 32 rows of 128 codes)
+        r.split_unit = 1;   // even shares of the blocks
         if (cudaFuncSetAttribute(&decode_tc8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem) ==
             cudaSuccess) {
             int n = 0;

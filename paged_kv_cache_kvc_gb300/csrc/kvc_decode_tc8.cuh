@@ -146,10 +146,12 @@ __device__ __forceinline__ void decode_tc8_cta(const CUtensorMap &tmap, const De
         for (int i = tid; i < G * D; i += kT8Threads) p.out[(static_cast<size_t>(b) * p.H_Q + hq0) * D + i] = 0.f;
         if (p.lse && tid < G) p.lse[static_cast<size_t>(b) * p.H_Q + hq0 + tid] = -INFINITY;
     }
-    const int blk0 = split * p.chunk;   // chunk: a multiple of 8 blocks
-    if (blk0 < nblk) {                  // uniform over the CTA: this split holds blocks
-        const int tile0 = blk0 / kTcBlocks;
-        const int nt = (min(nblk, blk0 + p.chunk) - blk0 + kTcBlocks - 1) / kTcBlocks;
+    // split: blocks blk0 .. blk_end - 1, walked as 128-token tiles from blk0 (the last one may be partial;
+    // blocks past blk_end belong to the next split and count here as unstaged)
+    const int blk0 = split * p.chunk;
+    if (blk0 < nblk) {   // uniform over the CTA: this split holds blocks
+        const int blk_end = min(nblk, blk0 + p.chunk);
+        const int nt = (blk_end - blk0 + kTcBlocks - 1) / kTcBlocks;
         const int ns = (nblk + p.chunk - 1) / p.chunk;
         const int32_t *bt_row = p.bt + static_cast<int64_t>(b) * p.bt_stride;
         const int64_t row_layer = static_cast<int64_t>(p.layer) * p.N;
@@ -174,8 +176,8 @@ __device__ __forceinline__ void decode_tc8_cta(const CUtensorMap &tmap, const De
         const uint32_t tm_o = tmem + 64, tm_k = tmem + 128;
 
         bool timed_out = false;
-        const int bbase = tile0 * kTcBlocks;
-        auto load_entry = [&](int rel) -> int32_t { return bbase + rel < nblk ? __ldg(bt_row + bbase + rel) : -1; };
+        const int bbase = blk0;
+        auto load_entry = [&](int rel) -> int32_t { return bbase + rel < blk_end ? __ldg(bt_row + bbase + rel) : -1; };
         // the step's own position (fused append); it lies in this split if it is in one of its tiles
         const int app = p.k_new ? len - 1 : -1;
         const int32_t app_phys = app >= 0 ? __ldg(bt_row + app / kBS) : -1;   // valid where its block is loaded
@@ -204,7 +206,7 @@ __device__ __forceinline__ void decode_tc8_cta(const CUtensorMap &tmap, const De
                     }
                     const int32_t e = __shfl_sync(kFull, ecur, (j & 3) * kTcBlocks + (lane & 7));
                     const int blk = bbase + j * kTcBlocks + lane;
-                    const bool in = lane < kTcBlocks && blk < nblk;
+                    const bool in = lane < kTcBlocks && blk < blk_end;
                     const bool v = in && e >= 0 && static_cast<int64_t>(e) < p.N;
                     if (in && !v) atomicOr(p.err, KVC_EBIT_BAD_BLOCK);
                     const uint32_t mask = __ballot_sync(kFull, v) & 0xFFu;
@@ -309,7 +311,7 @@ __device__ __forceinline__ void decode_tc8_cta(const CUtensorMap &tmap, const De
                     }
                     const uint32_t mask = vmask_sh[s];
                     const uint32_t code = sbase + s * kT8CodeSlot;
-                    const int tok0 = (tile0 + j) * kTcTok;
+                    const int tok0 = blk0 * kBS + j * kTcTok;
                     // item (lane, k): token t = 64 half + lane / 8 + 4 k, 16-channel chunk c = lane mod 8
                     // (channels 16 c .. 16 c + 15: band c / 4, 16-byte chunks 2 (c mod 4) and + 1 of the f16
                     // row).  The upper band's lanes store their two chunks in the other order, so that each
@@ -385,7 +387,7 @@ __device__ __forceinline__ void decode_tc8_cta(const CUtensorMap &tmap, const De
                 }
                 tc_fence_after();
                 const uint32_t mask = vmask_sh[s];
-                const int tok0 = (tile0 + jj) * kTcTok;
+                const int tok0 = blk0 * kBS + jj * kTcTok;
                 const bool use = ((mask >> (tq >> 4)) & 1u) && tok0 + tq < len;
                 const uint32_t code = sbase + s * kT8CodeSlot;
                 const int row = (tq >> 4) * 2 * kBS + (tq & 15);   // key row of the code slot
@@ -463,7 +465,7 @@ __device__ __forceinline__ void decode_tc8_cta(const CUtensorMap &tmap, const De
                 tc_fence_before();
                 mbar_arrive(sfree_bar(sb));
 
-                const int tok0 = (tile0 + j) * kTcTok;
+                const int tok0 = blk0 * kBS + j * kTcTok;
                 const int tok = tok0 + tid;
                 const bool valid = tok < len && e_tok >= 0 && static_cast<int64_t>(e_tok) < p.N;
                 float d[G];

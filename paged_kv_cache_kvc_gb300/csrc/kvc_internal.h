@@ -47,7 +47,7 @@ struct DecodeParams {
     int32_t ppu;             // query positions per unit: 1 for decode, a tile of a prefill chunk
     int32_t n_pos;           // query positions in all (decode: B; prefill: n_q)
     int32_t layer;
-    int32_t chunk;           // logical blocks per split (multiple of 4)
+    int32_t chunk;           // logical blocks per split (the split kernel: a multiple of 4; tcgen05: any)
     int32_t max_splits;
     int64_t N;
     float scale_log2;        // softmax scale * log2(e)
@@ -82,7 +82,8 @@ kvc_status launch_decode_int4(const kvc_pool *pool, DecodeParams &p, cudaStream_
 void choose_split(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits,
                   int n_tiles);
 // Split sizing of the tensor-memory decode kernel (whole 128-token tiles).
-void choose_split_tc(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int *chunk, int *max_splits);
+void choose_split_tc(const kvc_pool *pool, int units, int max_blocks, int ctas_per_sm, int unit, int *chunk,
+                     int *max_splits);
 
 // Look up (and so reserve) the allocation-free decode's scratch array for the current
 // context of `device`; kvc_pool_create calls it.

@@ -135,7 +135,8 @@ extern "C" kvc_status kvc_decode_attn_noalloc(kvc_pool *pool, int32_t layer, con
                                     : select_decode_bf16(pool->D, p.g);
     if (!k.fn) return KVC_ERR_UNSUPPORTED;
     if (k.ctas_per_sm <= 0) return KVC_ERR_CUDA;
-    if (tc.fn) choose_split_tc(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits);
+    if (tc.fn)
+        choose_split_tc(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, k.split_unit, &p.chunk, &p.max_splits);
     else choose_split(pool, p.B * p.H_KV, p.max_blocks, k.ctas_per_sm, &p.chunk, &p.max_splits, n_tiles(p.g));
     if (p.max_splits > 65535) return KVC_ERR_UNSUPPORTED;
     if (p.max_splits > 1) {

@@ -72,10 +72,12 @@ def test_mqa_tensor_memory_decode(kvc, lens, fused, dtype):
     assert err_tc <= max(2e-4, (1.5 if dtype == "fp8" else 1.0) * err_mma), (err_tc, err_mma)
 
 
-@pytest.mark.parametrize("chunk", ["8", "16", "24", "4096"])
+@pytest.mark.parametrize("chunk", ["8", "16", "24", "4096", "5", "12", "100"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 def test_mqa_tensor_memory_split_sizes(kvc, chunk, dtype):
-    """One tile per split up to one split per sequence (partials merged or not)."""
+    """One tile per split up to one split per sequence (partials merged or not).  The e4m3 kernel takes
+    splits that are not whole tiles (5, 12, 100 blocks: the last tile is partial, its blocks past the split
+    belong to the next one); for the bf16 kernel they are rounded up to whole tiles."""
     w = synth.make_workload("custom", B=3, H_Q=32, H_KV=1, d_h=128, lens=[3000, 129, 700], dtype=dtype, seed=5)
     _case(kvc, w, True, {"KVC_SPLIT_CHUNK": chunk})
 
