@@ -210,10 +210,11 @@ KVC_API kvc_status kvc_write_tokens(kvc_pool *pool, int32_t layer, const int32_t
  * Requires H_Q % H_KV == 0 (else KVC_ERR_ARG), block_size 16 and
  * H_Q / H_KV <= 32 (else KVC_ERR_UNSUPPORTED); head_dim is 64 or 128 (bf16)
  * or 128 (e4m3, int4), as kvc_pool_create admits.  Groups of 32 query heads
- * on d_h 128 bf16 pools (MQA) run on a tensor-memory (tcgen05) kernel: one
- * CTA per SM streams 128-position tiles, with scores and outputs in tensor
- * memory; the environment variable KVC_TC=0 selects the split kernel for
- * them too.  The pool's workspace for
+ * on d_h 128 bf16 or e4m3 pools (MQA) run on tensor-memory (tcgen05)
+ * kernels: one CTA per SM streams 128-position tiles, with scores and
+ * outputs in tensor memory (e4m3 codes widened to f16, exactly, on the way);
+ * the environment variable KVC_TC=0 selects the split kernel for them too.
+ * The pool's workspace for
  * split partials grows on first use with a larger batch (a cudaMalloc, so
  * make one call before capturing a CUDA graph; see kvc_pool_reserve).
  * Device-detected errors as for kvc_append; the affected sequence's outputs
