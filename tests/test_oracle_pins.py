@@ -253,6 +253,14 @@ def test_e4m3_decode_all_codes_vs_torch():
     assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0x01) == 2.0 ** -9
 
 
+def test_e4m3_values_are_exact_in_f16():
+    """Every finite e4m3 value is an f16 value (4 significant bits, exponents 2^-9 .. 2^8 inside f16's
+    2^-24 .. 2^15), so widening the codes to f16 before a tensor-core product loses nothing."""
+    vals = np.array([oracle.e4m3_decode(c) for c in range(256) if c & 0x7F != 0x7F])
+    assert len(vals) == 254 and np.all(np.isfinite(vals))
+    assert np.array_equal(vals.astype(np.float16).astype(np.float64), vals)
+
+
 def test_e4m3_encode_every_bf16_vs_torch():
     bits = np.arange(65536, dtype=np.uint32)
     x = ((bits << 16).astype(np.uint32)).view(np.float32)
